@@ -1,0 +1,191 @@
+"""CPU oracle for the W12 tree-verify pass -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It wraps ``w12_oracle.c`` (plain C,
+FP64 accumulation, ``-ffp-contract=off``) through ctypes and shares no code
+with the CUDA library.  Each wrapper names the passage it follows; the C file
+lists the readings taken where the pages are silent.
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+(exhaustive round trip, hand-computed window cases, NumPy cross-check,
+exact integer GEMM, brute-force tree and acceptance enumeration, the greedy
+autoregressive invariant and the planted-defect mutation).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+from typing import Optional, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "w12_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+TILE_N, TILE_K, REC_BYTES = 128, 64, 12288
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (host code; same flags on x86 and Arm)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp.%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                               "-fno-fast-math", "-pthread", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = C.CDLL(_LIB)
+        p = C.c_void_p
+        i64, i32 = C.c_int64, C.c_int32
+        L.orc_w12_layout.argtypes = [p, i64, i64, p, p]
+        L.orc_w12_pack.argtypes = [p, i64, i64, p, p, p, p]
+        L.orc_w12_unpack_rows.argtypes = [p, p, p, p, i64, i64, i64, i64, p]
+        L.orc_gemm_f64.argtypes = [p, i64, p, i64, i64, p, C.c_int]
+        L.orc_head_argmax.argtypes = [p, i64, p, i64, i64, p, p, p, p, C.c_int]
+        L.orc_tree_build.argtypes = [i32, i32, i32, i32, p, p, p, p, i32, p, p, p, p, p, p, p, p]
+        L.orc_tree_accept.argtypes = [i32, p, p, p, p, i32, i32, p, p, p, p]
+        for f in (L.orc_w12_layout, L.orc_w12_pack, L.orc_w12_unpack_rows, L.orc_gemm_f64,
+                  L.orc_head_argmax, L.orc_tree_build, L.orc_tree_accept):
+            f.restype = C.c_int
+        _lib = L
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(C.c_void_p)
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise ValueError(f"oracle {what} failed with status {rc}")
+
+
+# ---------------------------------------------------------------------------
+# W12 (SpecPilot explainer "4.1 W12: a 12-bit lossless weight format")
+# ---------------------------------------------------------------------------
+
+class Packed:
+    """Host-side W12 tensor: records, per-channel window base, escape index."""
+
+    def __init__(self, n, k, rec, base, esc_tile_off, esc):
+        self.n, self.k = n, k
+        self.rec, self.base, self.esc_tile_off, self.esc = rec, base, esc_tile_off, esc
+
+    @property
+    def n_escapes(self) -> int:
+        return int(self.esc.shape[0])
+
+    @property
+    def bytes(self) -> int:
+        return self.rec.nbytes + self.base.nbytes + self.esc_tile_off.nbytes + self.esc.nbytes
+
+
+def w12_pack(w: np.ndarray) -> Packed:
+    """Pack BF16 bits ``w[n][k]`` into W12 (window choice, records, escapes)."""
+    w = np.ascontiguousarray(w, dtype=np.uint16)
+    n, k = w.shape
+    L = lib()
+    base = np.empty(n, dtype=np.uint8)
+    ne = np.zeros(1, dtype=np.int64)
+    _check(L.orc_w12_layout(_ptr(w), n, k, _ptr(base), _ptr(ne)), "w12_layout")
+    tiles = (n // TILE_N) * (k // TILE_K)
+    rec = np.empty(tiles * REC_BYTES, dtype=np.uint8)
+    off = np.empty(tiles + 1, dtype=np.int32)
+    esc = np.empty(int(ne[0]), dtype=np.uint32)
+    _check(L.orc_w12_pack(_ptr(w), n, k, _ptr(base), _ptr(rec), _ptr(off), _ptr(esc) if esc.size else None),
+           "w12_pack")
+    return Packed(n, k, rec, base, off, esc)
+
+
+def w12_unpack(p: Packed, row0: int = 0, nrows: Optional[int] = None) -> np.ndarray:
+    """Decode rows ``[row0, row0 + nrows)`` back to BF16 bits."""
+    nrows = p.n - row0 if nrows is None else nrows
+    out = np.empty((nrows, p.k), dtype=np.uint16)
+    esc = p.esc if p.esc.size else np.zeros(1, dtype=np.uint32)
+    _check(lib().orc_w12_unpack_rows(_ptr(p.rec), _ptr(p.base), _ptr(p.esc_tile_off), _ptr(esc),
+                                     p.n, p.k, row0, nrows, _ptr(out)), "w12_unpack")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Verify GEMM and LM-head argmax (explainer "1.1", "2.1")
+# ---------------------------------------------------------------------------
+
+def gemm_f64(x: np.ndarray, w: np.ndarray, nthreads: int = 0) -> np.ndarray:
+    """``y = x . w^T`` with BF16 inputs and FP64 accumulation."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    w = np.ascontiguousarray(w, dtype=np.uint16)
+    R, k = x.shape
+    n = w.shape[0]
+    assert w.shape[1] == k
+    y = np.empty((R, n), dtype=np.float64)
+    _check(lib().orc_gemm_f64(_ptr(x), R, _ptr(w), n, k, _ptr(y), nthreads), "gemm_f64")
+    return y
+
+
+def head_argmax(h: np.ndarray, w_head: np.ndarray, bias: Optional[np.ndarray] = None,
+                nthreads: int = 0) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """Per row of ``h``: argmax over ``h . w_head^T`` (+ bias), the top-1 logit
+    and the top1 - top2 margin, all from FP64 logits."""
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    w_head = np.ascontiguousarray(w_head, dtype=np.uint16)
+    R, k = h.shape
+    V = w_head.shape[0]
+    am = np.empty(R, dtype=np.int32)
+    t1 = np.empty(R, dtype=np.float64)
+    mg = np.empty(R, dtype=np.float64)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float64)
+    _check(lib().orc_head_argmax(_ptr(h), R, _ptr(w_head), V, k, _ptr(b), _ptr(am), _ptr(t1), _ptr(mg),
+                                 nthreads), "head_argmax")
+    return am, t1, mg
+
+
+# ---------------------------------------------------------------------------
+# Best-first tree (explainer "4.2", "4.4") and acceptance ("1.1")
+# ---------------------------------------------------------------------------
+
+class Tree:
+    def __init__(self, R, parent, token, depth, req, score, rank, req_row_off):
+        self.R = R
+        self.parent, self.token, self.depth, self.req = parent, token, depth, req
+        self.score, self.rank, self.req_row_off = score, rank, req_row_off
+
+
+def tree_build(lat, budget: int) -> Tree:
+    """Best-first tree over a lattice (``synth.Lattice``) with a shared budget."""
+    n_req, p_max = lat.n_req, lat.p_max
+    out = dict(parent=np.empty(budget, np.int32), token=np.empty(budget, np.int32),
+               depth=np.empty(budget, np.uint8), req=np.empty(budget, np.int32),
+               score=np.empty(budget, np.float32), rank=np.empty(budget, np.uint8))
+    off = np.empty(n_req + 1, np.int32)
+    R = np.zeros(1, np.int32)
+    ct = np.ascontiguousarray(lat.cand_tok, np.int32)
+    cl = np.ascontiguousarray(lat.cand_logp, np.float32)
+    rc = lib().orc_tree_build(n_req, p_max, lat.n_cand, int(bool(lat.conditional)),
+                              _ptr(np.ascontiguousarray(lat.p_r, np.int32)),
+                              _ptr(np.ascontiguousarray(lat.root_tok, np.int32)), _ptr(ct), _ptr(cl), budget,
+                              _ptr(out["parent"]), _ptr(out["token"]), _ptr(out["depth"]), _ptr(out["req"]),
+                              _ptr(out["score"]), _ptr(out["rank"]), _ptr(off), _ptr(R))
+    _check(rc, "tree_build")
+    r = int(R[0])
+    return Tree(r, *(out[k][:r] for k in ("parent", "token", "depth", "req", "score", "rank")), off)
+
+
+def tree_accept(tree: Tree, argmax: np.ndarray, n_req: int, p_max: int):
+    """Greedy acceptance on every request's share of the tree."""
+    acc_tok = np.empty((n_req, p_max + 1), np.int32)
+    acc_len = np.empty(n_req, np.int32)
+    acc_node = np.empty(n_req, np.int32)
+    am = np.ascontiguousarray(argmax, np.int32)
+    _check(lib().orc_tree_accept(tree.R, _ptr(tree.parent), _ptr(tree.token), _ptr(tree.depth),
+                                 _ptr(tree.req_row_off), n_req, p_max, _ptr(am), _ptr(acc_tok),
+                                 _ptr(acc_len), _ptr(acc_node)), "tree_accept")
+    return acc_tok, acc_len, acc_node
