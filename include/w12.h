@@ -1,0 +1,263 @@
+/*
+ * w12.h -- C ABI of the W12 tree-verify library (GB300, sm_103a).
+ *
+ * The verify pass of tree-based speculative decoding over weights stored in
+ * the W12 12-bit lossless format:
+ *
+ *   lattice --w12_tree_build--> draft tree of R rows
+ *   rows    --w12_gemm (per linear)-------------------> Y = X . W^T
+ *   rows    --w12_lmhead_argmax--> target argmax per row
+ *   tree + argmax --w12_tree_accept--> accepted tokens + lengths
+ *
+ * Sources (SpecPilot explainer at jaehun.me, "SpecPilot: Autonomous Algorithm
+ * Discovery and Systems Optimization for Speculative Decoding"; the summary
+ * page at agihunt.info; the poot-llm speculative-decoding docs):
+ *   - W12: explainer section 4.1 "W12: a 12-bit lossless weight format".
+ *   - verify rows / greedy acceptance: explainer 1.1; poot-llm "What a round
+ *     guarantees".
+ *   - best-first tree / shared budget: explainer 4.2 and 4.4.
+ *   - typed refusal before anything runs: poot-llm "What is refused".
+ *
+ * Conventions for every entry point:
+ *   - Every argument is validated before any launch; a bad argument returns
+ *     a typed status and launches nothing.
+ *   - Device pointers are caller-owned (e.g. torch tensors).  The library
+ *     allocates no device memory and keeps no global state except cached
+ *     device properties and its driver entry point.
+ *   - Device work is asynchronous on the caller's stream unless stated.
+ *     Launch failures map to W12_E_CUDA.
+ *   - Conditions found on the device (a timed-out wait, bad lattice values)
+ *     are written to a status word in the workspace and read back with
+ *     w12_status_fetch(); no kernel traps.
+ *   - Limits: N % 128 == 0, K % 64 == 0, 1 <= R <= 256 rows, budget <= 512,
+ *     p_max <= 16, 16 candidates per position; anything else is
+ *     W12_E_UNSUPPORTED.
+ *   - There is no CPU fallback: every device step runs in this library's
+ *     CUDA kernels.
+ */
+#ifndef W12_H
+#define W12_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *w12_stream_t;
+
+typedef enum {
+    W12_OK = 0,
+    W12_E_INVAL = -1,        /* malformed argument (null pointer, bad size, ...) */
+    W12_E_UNSUPPORTED = -2,  /* well-formed but outside the limits above */
+    W12_E_MISMATCH = -3,     /* a bit-exact check failed (pack / load check) */
+    W12_E_CUDA = -4,         /* a CUDA call failed */
+    W12_E_TIMEOUT = -5,      /* a bounded device wait ran out */
+    W12_E_WORKSPACE = -6     /* workspace null, too small or misaligned */
+} w12_status;
+
+/* Human-readable name of a status code (static storage). */
+const char *w12_status_str(int status);
+
+/* ABI version of this header: major*100 + minor. */
+int w12_abi_version(void);
+
+/* ------------------------------------------------------------------------
+ * W12 packing (host memory, caller-owned)
+ *
+ * Format (explainer 4.1): for every output channel n a window base b_n (the
+ * BF16 biased exponent field of the window's lowest binade, 1..239) chosen
+ * to hold the most normal weights of the channel (ties: largest b_n).  A
+ * weight whose exponent field e lies in [b_n, b_n + 15] is stored in 12 bits:
+ * an 8-bit view byte [sign:1][e - b_n:4][mantissa bits 6..4] and a low nibble
+ * (mantissa bits 3..0).  Any other weight (zero, denormal, Inf, NaN, out of
+ * window) is stored as a zero code plus an exact 16-bit escape entry.
+ *
+ * Records: one 12288-byte record per 128x64 tile, tiles ordered n-tile major
+ * (t = n_tile * (K/64) + k_tile).  Bytes 0..8191 (the 8-bit view):
+ * four 16-K groups g, each 128 channels c x 16 bytes at (g*128 + c)*16, the
+ * weight kk of the group at byte pos(kk) = 4*((kk%8)/2) + 2*(kk/8) + kk%2.
+ * Bytes 8192..12287 (low nibbles): two 32-K groups h, each 128 channels x 16
+ * bytes at 8192 + (h*128 + c)*16; weight kk of the group's first 16 K is the
+ * low nibble of byte pos(kk), weight kk of the second 16 K the high nibble.
+ *
+ * Escapes: esc_tile_off[t] .. esc_tile_off[t+1] index the entries of record
+ * t in esc[], each u32 = n_local << 22 | k_local << 16 | bf16 bits, sorted
+ * by (n_local, k_local).
+ * ---------------------------------------------------------------------- */
+
+typedef struct {
+    int64_t n, k;            /* output channels, input features */
+    int64_t n_tiles, k_tiles;
+    int64_t n_escapes;
+    size_t rec_bytes;        /* n_tiles * k_tiles * 12288 */
+    size_t base_bytes;       /* n */
+    size_t esc_off_bytes;    /* (n_tiles * k_tiles + 1) * 4 */
+    size_t esc_bytes;        /* n_escapes * 4 */
+} w12_layout;
+
+/*
+ * Sizes of the packed buffers of a row-major BF16 tensor w_bf16[n][k].
+ * Reads the whole tensor (window choice and escape count).
+ * Errors: W12_E_INVAL (null pointer, n or k <= 0), W12_E_UNSUPPORTED
+ * (n % 128 or k % 64 nonzero).
+ */
+w12_status w12_pack_query(const uint16_t *w_bf16, int64_t n, int64_t k, w12_layout *out);
+
+/*
+ * Pack w_bf16[n][k] into caller buffers of the sizes w12_pack_query gave
+ * (esc may be NULL when n_escapes == 0).  The packer then decodes its own
+ * output on the host and compares it bit for bit with the source (the load
+ * check of explainer 4.1); any difference returns W12_E_MISMATCH.
+ * Runs on host threads; thread-safe for distinct outputs.
+ */
+w12_status w12_pack(const uint16_t *w_bf16, int64_t n, int64_t k, const w12_layout *layout,
+                    void *rec, uint8_t *base, int32_t *esc_tile_off, uint32_t *esc);
+
+/* ------------------------------------------------------------------------
+ * Device views.  All pointers below are device pointers owned by the caller.
+ * ---------------------------------------------------------------------- */
+
+typedef struct {
+    const void *rec;             /* records, 16-byte aligned */
+    const uint8_t *base;         /* [n] window bases */
+    const int32_t *esc_tile_off; /* [tiles + 1] */
+    const uint32_t *esc;         /* [n_escapes] (may be NULL if none) */
+    int64_t n, k;
+    int64_t n_escapes;
+} w12_weight;
+
+/*
+ * Workspace: one caller-owned device buffer, 256-byte aligned, at least
+ * w12_workspace_bytes(...) bytes for the largest call made with it, and set
+ * to zero once with w12_workspace_init before first use.  Calls that share
+ * a workspace must be ordered on one stream.
+ *   R       rows (<= 256), max_n: largest N of any weight, vocab: LM-head N,
+ *   n_req   requests of the tree (<= 512).
+ */
+size_t w12_workspace_bytes(int32_t R, int64_t max_n, int64_t vocab, int32_t n_req);
+w12_status w12_workspace_init(void *ws, size_t ws_bytes, w12_stream_t stream);
+
+/*
+ * Read and clear the device status word (synchronises the stream).
+ * Returns W12_OK or the first device-detected condition since the last
+ * fetch (W12_E_TIMEOUT, W12_E_INVAL for bad lattice values, ...).
+ */
+w12_status w12_status_fetch(void *ws, w12_stream_t stream);
+
+/*
+ * Decode a packed tensor to row-major BF16 dst[n][k] (device), escapes
+ * restored.  Errors: W12_E_INVAL, W12_E_UNSUPPORTED, W12_E_CUDA.
+ */
+w12_status w12_unpack(const w12_weight *w, uint16_t *dst_bf16, w12_stream_t stream);
+
+/*
+ * Load-time bit-exact check (explainer 4.1: "checks the restored tensors
+ * bit-for-bit against the checkpoint"): decodes w on the device and compares
+ * every weight with src_bf16[n][k] (device).  Synchronises the stream and
+ * writes the number of differing weights to *mismatches (host).
+ * Returns W12_OK if none differ, W12_E_MISMATCH otherwise.
+ */
+w12_status w12_load_check(const w12_weight *w, const uint16_t *src_bf16, int64_t *mismatches,
+                          void *ws, size_t ws_bytes, w12_stream_t stream);
+
+/*
+ * Verify GEMM (explainer 4.1 "W12 GEMM", 2.1): y[R][n] = x[R][k] . W^T with W
+ * decoded exactly from W12 inside the kernel, FP32 accumulation, BF16
+ * (round to nearest even) output.  x, y row-major BF16, 16-byte aligned
+ * rows (k % 64 == 0 already gives that).  Deterministic: the K-split points
+ * and the reduction order depend only on the shapes and the device.
+ */
+w12_status w12_gemm(const w12_weight *w, const uint16_t *x, int32_t R, uint16_t *y, void *ws,
+                    size_t ws_bytes, w12_stream_t stream);
+
+/*
+ * LM head + argmax: logits = h[R][k] . W_head^T in FP32 (never stored), then
+ * per row the index of the largest logit (lowest index on ties; NaN never
+ * wins) into argmax[R]; maxlogit[R] (nullable) gets the winning logit.
+ */
+w12_status w12_lmhead_argmax(const w12_weight *head, const uint16_t *h, int32_t R, int32_t *argmax,
+                             float *maxlogit, void *ws, size_t ws_bytes, w12_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Draft tree
+ * ---------------------------------------------------------------------- */
+
+typedef struct {
+    int32_t n_req;              /* requests */
+    int32_t p_max;              /* drafted positions per request (<= 16) */
+    int32_t n_cand;             /* candidates used per position (1 = chain, <= 16) */
+    int32_t conditional;        /* 0: logp[n_req][p_max][16]; 1: logp[n_req][p_max][16][16] */
+    const int32_t *p_r;         /* HOST [n_req]: positions drafted by request r (0..p_max) */
+    const int32_t *root_tok;    /* device [n_req]: last committed token */
+    const int32_t *cand_tok;    /* device [n_req][p_max][16] */
+    const float *cand_logp;     /* device, layout per `conditional`; finite and <= 0 */
+} w12_lattice;
+
+typedef struct {
+    int32_t R;                  /* rows, set by w12_tree_build */
+    int32_t *parent;            /* device [budget]: parent row, -1 for a root */
+    int32_t *token;             /* device [budget] */
+    uint8_t *depth;             /* device [budget] */
+    int32_t *req;               /* device [budget] */
+    float *score;               /* device [budget]: FP32 path log-probability */
+    uint8_t *rank;              /* device [budget]: candidate rank at its depth */
+    int32_t *req_row_off;       /* device [n_req + 1] */
+} w12_tree;
+
+/*
+ * Best-first tree under one shared node budget (explainer 4.2, 4.4): the
+ * rows are the `budget` nodes (roots included, score 0) ranked first by
+ * (path score desc, depth asc, request asc, candidate-rank path asc), where
+ * a child at depth d takes position d's candidates and its score is the
+ * FP32 sum of edge log-probabilities from the root.  The set is
+ * prefix-closed.  Rows are emitted grouped by request, best-first inside a
+ * request (so every parent precedes its children).  out->R is set on the
+ * host (min(budget, nodes available)) before anything runs.
+ * Device check: a used log-probability that is positive or not finite sets
+ * W12_E_INVAL in the status word.
+ */
+w12_status w12_tree_build(const w12_lattice *lat, int32_t budget, w12_tree *out, void *ws, size_t ws_bytes,
+                          w12_stream_t stream);
+
+/*
+ * Greedy acceptance (explainer 1.1): per request the root is accepted and a
+ * node is accepted iff its parent is and its token equals the argmax at the
+ * parent.  acc_tok[n_req][p_max + 1] gets the deepest accepted node's draft
+ * tokens followed by the bonus token (argmax at that node), padded with -1;
+ * acc_len[n_req] = tau = depth + 1; acc_node[n_req] (nullable) the row.
+ */
+w12_status w12_tree_accept(const w12_tree *tree, int32_t n_req, int32_t p_max, const int32_t *argmax,
+                           int32_t *acc_tok, int32_t *acc_len, int32_t *acc_node, w12_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * The verify step
+ * ---------------------------------------------------------------------- */
+
+typedef struct {
+    int32_t n_linear;
+    const w12_weight *lin;         /* HOST array [n_linear] */
+    const uint16_t *const *x;      /* HOST array [n_linear] of device x_l[R][lin[l].k] */
+    uint16_t *const *y;            /* HOST array [n_linear] of device y_l[R][lin[l].n] */
+    const w12_weight *head;
+    const uint16_t *h;             /* device h[R][head->k] */
+    int32_t *argmax;               /* device [R] */
+} w12_step;
+
+/*
+ * One verify pass over a built tree: every linear in order (each may start
+ * streaming its weights while the previous one finishes), then the LM head
+ * with per-row argmax, then greedy acceptance.  Same outputs as the
+ * individual calls.  rows = tree->R.
+ */
+w12_status w12_verify_step(const w12_step *step, const w12_tree *tree, int32_t n_req, int32_t p_max,
+                           int32_t *acc_tok, int32_t *acc_len, int32_t *acc_node, void *ws, size_t ws_bytes,
+                           w12_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W12_H */

@@ -1,0 +1,49 @@
+/*
+ * w12_debug.h -- test hooks of the W12 library (not for production use).
+ *
+ * These exist so that the failure paths of the kernels can be exercised
+ * without faulting the GPU: every wait inside the kernels is bounded, and a
+ * test can make one wait run out on purpose.
+ */
+#ifndef W12_DEBUG_H
+#define W12_DEBUG_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Process-wide debug settings applied to every later launch.
+ *   flags bit 0: in the next GEMM launches, CTA 0's producer announces its
+ *                first record but never copies it, so that CTA's consumers
+ *                time out; the kernel records W12_E_TIMEOUT in the workspace
+ *                status word and every CTA returns with no copy in flight.
+ *   timeout_ns:  limit of every bounded wait inside the kernels
+ *                (0 restores the default of 2 seconds).
+ * Not thread-safe; meant to be set between launches by a test.
+ */
+void w12_debug_set(int32_t flags, uint64_t timeout_ns);
+
+/*
+ * Per-launch timing of w12_verify_step for benchmarks.  While enabled, the
+ * step records a CUDA event before its first launch and after every launch
+ * (which also serialises the launches, so steps timed this way lose the
+ * overlap between consecutive kernels).  w12_debug_profile_read synchronises
+ * on the last event and writes the elapsed milliseconds of each launch of the
+ * most recent step (GEMM launches in order, then the argmax reduction, then
+ * acceptance) to ms[0..max); it returns the number of launches, or a
+ * negative status.
+ */
+void w12_debug_profile(int32_t enable);
+int32_t w12_debug_profile_read(float *ms, int32_t max);
+
+/* Number of SMs the kernels size their persistent grids for (current device). */
+int32_t w12_debug_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W12_DEBUG_H */

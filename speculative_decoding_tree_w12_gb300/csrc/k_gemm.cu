@@ -1,0 +1,592 @@
+// Stream-K W12 verify GEMM and fused LM-head tile argmax (sm_103a).
+//
+// SpecPilot explainer, section 4.1 "W12 GEMM": 12 KB records (128x64 weights)
+// are restored in registers and fed to the tensor cores; a stream-K split of
+// the reduction loop in a fixed order keeps the GEMM deterministic.  That
+// kernel was written for H100 (wgmma register operands); this one is built
+// for GB300:
+//   * one persistent CTA per SM; each CTA owns a contiguous run of records in
+//     (n-tile, k-tile) order, i.e. a contiguous slice of the packed buffer;
+//   * a producer warp streams records with 1-D bulk copies (cp.async.bulk,
+//     L2 evict-first) and the matching activation block with a 2-D TMA load
+//     (128-byte swizzle, out-of-range rows zero-filled) into an mbarrier ring;
+//   * consumer warps decode the records in registers straight into mma.sync
+//     A fragments (output channels are M, tree rows are N), patch escapes,
+//     and accumulate in FP32;
+//   * a tile split between CTAs is reduced by the last CTA to arrive, reading
+//     the partial sums in CTA order (no waiting, deterministic);
+//   * the LM-head epilogue reduces each 128-token tile to (max, index) per row.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+
+#include "w12_device.cuh"
+
+using namespace w12d;
+
+namespace {
+
+constexpr int kWarpsN = 4;            // consumer warps across the 128 channels (32 each)
+
+struct KParams {
+    const uint8_t *rec;
+    const uint8_t *base;
+    const int32_t *esc_off;
+    const uint32_t *esc;
+    int32_t n_tiles, k_tiles, R, mode;
+    uint16_t *y;
+    int64_t ldy;
+    float *s1_val;
+    int32_t *s1_idx;
+    float *partial;
+    int32_t *counters;
+    int32_t *status;
+    uint32_t mul16;
+    int32_t debug_flags;
+    uint64_t timeout_ns;
+    int32_t stages;
+    int32_t max_recs;       // records of the largest CTA share
+    int32_t esc_cap;        // escape entries that fit the shared cache
+    int32_t base_tiles;     // n-tiles whose window bases fit the shared cache
+};
+
+template <int NB8, int WK>
+struct Cfg {
+    static constexpr int kRows = NB8 * 8;                     // rows per activation block
+    static constexpr int kXBytes = kRows * 128;               // activation block: rows x 64 BF16
+    static constexpr int kConsumerWarps = kWarpsN * WK;
+    static constexpr int kConsumers = kConsumerWarps * 32;
+    static constexpr int kThreads = kConsumers + 32;          // + producer warp
+    static constexpr int kKgPerWarp = 4 / WK;                 // 16-K groups per consumer warp
+    static constexpr int kRedStride = 132;                    // padded row stride of the reduction tile
+    static constexpr int kRedBytes = WK * kRows * kRedStride * 4;
+};
+
+struct SmemPlan {
+    int rec_off, x_off, red_off, bar_off, flag_off, escoff_off, esc_off, base_off, total;
+};
+
+template <int NB8, int WK>
+__host__ __device__ inline SmemPlan smem_plan(int stages, int max_recs, int esc_cap, int base_tiles)
+{
+    using C = Cfg<NB8, WK>;
+    SmemPlan s;
+    int o = 0;
+    s.rec_off = o;
+    o += stages * w12i::kRecBytes;
+    s.x_off = o;
+    o += stages * C::kXBytes;
+    s.red_off = o;
+    o += C::kRedBytes;
+    s.bar_off = o;
+    o += 2 * stages * 8 + 8;
+    s.flag_off = o;
+    o += 16;
+    s.escoff_off = o;
+    o += ((max_recs + 1) * 4 + 15) / 16 * 16;
+    s.esc_off = o;
+    o += esc_cap * 4;
+    s.base_off = o;
+    o += base_tiles * w12i::kTileN;
+    s.total = o + 1024;   // slack to align the window to 1024 bytes at run time
+    return s;
+}
+
+__device__ __forceinline__ int cta_of_record(int64_t r, int G, int64_t T) { return (int)(((r + 1) * G - 1) / T); }
+__device__ __forceinline__ int64_t first_record(int c, int G, int64_t T) { return (int64_t)c * T / G; }
+
+template <int NB8, int WK>
+__global__ void __launch_bounds__(Cfg<NB8, WK>::kThreads, 1)
+    k_w12_gemm(const __grid_constant__ CUtensorMap xmap, const KParams p)
+{
+    using C = Cfg<NB8, WK>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // the 128-byte swizzle of the activation blocks needs 1024-byte alignment
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const SmemPlan sp = smem_plan<NB8, WK>(p.stages, p.max_recs, p.esc_cap, p.base_tiles);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = gridDim.x, cta = blockIdx.x;
+    const int KT = p.k_tiles;
+    const int64_t T = (int64_t)p.n_tiles * KT;
+    const int64_t rec_begin = first_record(cta, G, T), rec_end = first_record(cta + 1, G, T);
+    const int nrec = (int)(rec_end - rec_begin);
+    const int S = p.stages;
+
+    const uint32_t rec_s = smem_u32(smem + sp.rec_off);
+    const uint32_t x_s = smem_u32(smem + sp.x_off);
+    float *red = reinterpret_cast<float *>(smem + sp.red_off);
+    const uint32_t bar_full = smem_u32(smem + sp.bar_off);
+    const uint32_t bar_empty = bar_full + 8 * S;
+    const uint32_t bar_cons = bar_empty + 8 * S;
+    volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(smem + sp.flag_off);
+    int32_t *last_flag = reinterpret_cast<int32_t *>(smem + sp.flag_off + 4);
+    int32_t *esc_off_s = reinterpret_cast<int32_t *>(smem + sp.escoff_off);
+    uint32_t *esc_s = reinterpret_cast<uint32_t *>(smem + sp.esc_off);
+    uint8_t *base_s = smem + sp.base_off;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, C::kConsumerWarps);
+        }
+        mbar_init(bar_cons, C::kConsumers);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    if (warp == C::kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tmap(&xmap);
+            const uint64_t pol = policy_evict_first();
+            const uint32_t stage_bytes = w12i::kRecBytes + C::kXBytes;
+            const bool drop_first = (p.debug_flags & 1) && cta == 0;
+            const int pre = min(S, nrec);
+            // weights do not depend on earlier kernels: start them before the
+            // programmatic-dependency wait
+            for (int i = 0; i < pre; ++i) {
+                mbar_expect_tx(bar_full + 8 * i, stage_bytes);
+                if (!(drop_first && i == 0))
+                    bulk_g2s(rec_s + i * w12i::kRecBytes, p.rec + (rec_begin + i) * (int64_t)w12i::kRecBytes,
+                             w12i::kRecBytes, bar_full + 8 * i, pol);
+            }
+            pdl_wait();
+            for (int i = 0; i < pre; ++i)
+                if (!(drop_first && i == 0))
+                    tma_load_2d(x_s + i * C::kXBytes, &xmap, (int)((rec_begin + i) % KT) * w12i::kTileK, 0,
+                                bar_full + 8 * i);
+            int issued = pre;
+            for (int i = pre; i < nrec; ++i) {
+                const int s = i % S, u = i / S;
+                if (!mbar_wait(bar_empty + 8 * s, (u - 1) & 1, p.timeout_ns, p.status, abort_flag)) break;
+                mbar_expect_tx(bar_full + 8 * s, stage_bytes);
+                bulk_g2s(rec_s + s * w12i::kRecBytes, p.rec + (rec_begin + i) * (int64_t)w12i::kRecBytes,
+                         w12i::kRecBytes, bar_full + 8 * s, pol);
+                tma_load_2d(x_s + s * C::kXBytes, &xmap, (int)((rec_begin + i) % KT) * w12i::kTileK, 0,
+                            bar_full + 8 * s);
+                issued = i + 1;
+            }
+            if (*abort_flag) {
+                // leave no copy in flight: wait (bounded, ignoring the abort
+                // flag) for the last use of every stage that was issued
+                int32_t dummy_abort = 0;
+                for (int i = max(0, issued - S); i < issued; ++i) {
+                    if (drop_first && i == 0) continue;
+                    mbar_wait(bar_full + 8 * (i % S), (i / S) & 1, p.timeout_ns, p.status, &dummy_abort);
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int cw = warp;                 // consumer warp 0 .. kConsumerWarps-1
+    const int mw = cw % kWarpsN, wk = cw / kWarpsN;
+    const int g = lane >> 2, t = lane & 3;
+    const int ctid = threadIdx.x;        // 0 .. kConsumers-1
+
+    uint32_t cons_phase0 = 0;
+    auto cons_sync0 = [&]() -> bool {
+        mbar_arrive(bar_cons);
+        const bool ok = mbar_wait(bar_cons, cons_phase0, p.timeout_ns, p.status, abort_flag);
+        cons_phase0 ^= 1u;
+        return ok;
+    };
+    // shared caches: escape offsets/entries of this CTA's records, window bases
+    const int64_t nt_first = rec_begin / KT;
+    const int nt_span = (int)((rec_end - 1) / KT - nt_first + 1);
+    const bool base_cached = nt_span <= p.base_tiles;
+    for (int i = ctid; i <= nrec; i += C::kConsumers) esc_off_s[i] = __ldg(p.esc_off + rec_begin + i);
+    if (base_cached)
+        for (int i = ctid; i < nt_span * w12i::kTileN; i += C::kConsumers)
+            base_s[i] = __ldg(p.base + nt_first * w12i::kTileN + i);
+    if (!cons_sync0()) return;
+    const int32_t e_lo = esc_off_s[0];
+    const bool esc_cached = (esc_off_s[nrec] - e_lo) <= p.esc_cap;
+    if (esc_cached)
+        for (int i = ctid; i < esc_off_s[nrec] - e_lo; i += C::kConsumers) esc_s[i] = __ldg(p.esc + e_lo + i);
+    if (!cons_sync0()) return;
+
+    float acc[2][NB8][4];
+    ChanConst cc[2][2];
+    int64_t cur_nt = -1;
+    uint32_t cons_phase = cons_phase0;
+    // barrier over the consumer threads with a bounded wait; false = aborted
+    auto cons_sync = [&]() -> bool {
+        mbar_arrive(bar_cons);
+        const bool ok = mbar_wait(bar_cons, cons_phase, p.timeout_ns, p.status, abort_flag);
+        cons_phase ^= 1u;
+        return ok;
+    };
+
+    auto load_consts = [&](int64_t nt) {
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+            for (int hi = 0; hi < 2; ++hi) {
+                const int ch = mw * 32 + mb * 16 + hi * 8 + g;
+                const uint32_t b = base_cached ? base_s[(nt - nt_first) * w12i::kTileN + ch]
+                                               : __ldg(p.base + nt * w12i::kTileN + ch);
+                cc[mb][hi] = chan_const(b);
+            }
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+            for (int nb = 0; nb < NB8; ++nb)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[mb][nb][q] = 0.f;
+    };
+
+    // finish tile nt: combine the K-slices, then write (owned tile) or publish
+    // a partial and let the last contributor finish it
+    auto flush = [&](int64_t nt) -> bool {
+        if (*abort_flag) return false;
+        // 1. every consumer warp drops its accumulators into red[wk][row][ch]
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+            for (int nb = 0; nb < NB8; ++nb) {
+                const int ch = mw * 32 + mb * 16 + g;
+                const int row = nb * 8 + 2 * t;
+                float *rb = red + (wk * C::kRows) * C::kRedStride;
+                rb[row * C::kRedStride + ch] = acc[mb][nb][0];
+                rb[(row + 1) * C::kRedStride + ch] = acc[mb][nb][1];
+                rb[row * C::kRedStride + ch + 8] = acc[mb][nb][2];
+                rb[(row + 1) * C::kRedStride + ch + 8] = acc[mb][nb][3];
+            }
+        if (!cons_sync()) return false;
+        // 2. sum the K-slices in order into red[0]
+        const int R = p.R;
+        const int rows = min(R, C::kRows);
+        for (int e = ctid; e < rows * 32; e += C::kConsumers) {
+            const int row = e >> 5, c4 = (e & 31) * 4;
+            float4 v = *reinterpret_cast<float4 *>(red + row * C::kRedStride + c4);
+#pragma unroll
+            for (int s = 1; s < WK; ++s) {
+                const float4 w = *reinterpret_cast<float4 *>(red + (s * C::kRows + row) * C::kRedStride + c4);
+                v.x += w.x, v.y += w.y, v.z += w.z, v.w += w.w;
+            }
+            *reinterpret_cast<float4 *>(red + row * C::kRedStride + c4) = v;
+        }
+        if (!cons_sync()) return false;
+
+        const int64_t t0 = nt * KT, t1 = t0 + KT;
+        const bool owned = rec_begin <= t0 && rec_end >= t1;
+        bool finish = owned;
+        if (!owned) {
+            // 3. publish this CTA's partial (slot 0 for its first tile, 1 for its last)
+            const int slot = (nt == nt_first) ? 0 : 1;
+            float *mine = p.partial + ((int64_t)(cta * 2 + slot) * C::kRows) * w12i::kTileN;
+            for (int e = ctid; e < rows * 32; e += C::kConsumers) {
+                const int row = e >> 5, c4 = (e & 31) * 4;
+                __stcg(reinterpret_cast<float4 *>(mine + row * w12i::kTileN + c4),
+                       *reinterpret_cast<float4 *>(red + row * C::kRedStride + c4));
+            }
+            __threadfence();
+            if (!cons_sync()) return false;
+            const int c_first = cta_of_record(t0, G, T), c_last = cta_of_record(t1 - 1, G, T);
+            if (ctid == 0) {
+                const int old = atomicAdd(p.counters + nt, 1);
+                *last_flag = (old == c_last - c_first);
+            }
+            if (!cons_sync()) return false;
+            finish = *last_flag != 0;
+            if (finish) {
+                __threadfence();
+                // 4. the last contributor sums every partial in CTA order
+                for (int e = ctid; e < rows * 32; e += C::kConsumers) {
+                    const int row = e >> 5, c4 = (e & 31) * 4;
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int c = c_first; c <= c_last; ++c) {
+                        const int sl = (nt == first_record(c, G, T) / KT) ? 0 : 1;
+                        const float *src = p.partial + ((int64_t)(c * 2 + sl) * C::kRows) * w12i::kTileN;
+                        const float4 w = __ldcg(reinterpret_cast<const float4 *>(src + row * w12i::kTileN + c4));
+                        v.x += w.x, v.y += w.y, v.z += w.z, v.w += w.w;
+                    }
+                    *reinterpret_cast<float4 *>(red + row * C::kRedStride + c4) = v;
+                }
+                if (ctid == 0) p.counters[nt] = 0;   // ready for the next launch using this slot
+                if (!cons_sync()) return false;
+            }
+        }
+        if (finish) {
+            if (p.mode == w12i::kModeLinear) {
+                // 5a. BF16 (round to nearest even) rows of 128 channels
+                for (int e = ctid; e < rows * 32; e += C::kConsumers) {
+                    const int row = e >> 5, c4 = (e & 31) * 4;
+                    const float4 v = *reinterpret_cast<float4 *>(red + row * C::kRedStride + c4);
+                    uint2 packed;
+                    packed.x = pack_bf16x2(v.x, v.y);
+                    packed.y = pack_bf16x2(v.z, v.w);
+                    *reinterpret_cast<uint2 *>(p.y + row * p.ldy + nt * w12i::kTileN + c4) = packed;
+                }
+            } else {
+                // 5b. per row: (max, lowest index) over the tile's 128 tokens
+                for (int row = cw; row < rows; row += C::kConsumerWarps) {
+                    float bv = __int_as_float(0x7fc00000);
+                    int32_t bi = 0x7fffffff;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int ch = lane * 4 + q;
+                        const float v = red[row * C::kRedStride + ch];
+                        if (beats(v, ch, bv, bi)) bv = v, bi = ch;
+                    }
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) {
+                        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+                        const int32_t oi = __shfl_xor_sync(0xffffffffu, bi, off);
+                        if (beats(ov, oi, bv, bi)) bv = ov, bi = oi;
+                    }
+                    if (lane == 0) {
+                        p.s1_val[(int64_t)row * p.n_tiles + nt] = bv;
+                        p.s1_idx[(int64_t)row * p.n_tiles + nt] =
+                            (bi == 0x7fffffff) ? (int32_t)(nt * w12i::kTileN) : (int32_t)(nt * w12i::kTileN + bi);
+                    }
+                }
+            }
+        }
+        return cons_sync();
+    };
+
+    uint32_t a[2][C::kKgPerWarp][4];
+    for (int i = 0; i < nrec; ++i) {
+        const int64_t r = rec_begin + i;
+        const int64_t nt = r / KT;
+        if (nt != cur_nt) {
+            if (cur_nt >= 0 && !flush(cur_nt)) return;
+            cur_nt = nt;
+            load_consts(nt);
+        }
+        const int s = i % S;
+        if (!mbar_wait(bar_full + 8 * s, (i / S) & 1, p.timeout_ns, p.status, abort_flag)) return;
+        const uint32_t rb = rec_s + s * w12i::kRecBytes;
+        const uint32_t xb = x_s + s * C::kXBytes;
+
+        // decode this warp's 32 channels x (16 * kKgPerWarp) K of the record
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb) {
+            const int ch_lo = mw * 32 + mb * 16 + g;
+            uint32_t nib_lo = 0, nib_hi = 0;
+#pragma unroll
+            for (int kgl = 0; kgl < C::kKgPerWarp; ++kgl) {
+                const int kg = wk * C::kKgPerWarp + kgl;
+                if (kgl == 0 || (kg & 1) == 0) {
+                    nib_lo = lds32(rb + w12i::kViewBytes + (((kg >> 1) * w12i::kTileN + ch_lo) * 16 + 4 * t));
+                    nib_hi = lds32(rb + w12i::kViewBytes + (((kg >> 1) * w12i::kTileN + ch_lo + 8) * 16 + 4 * t));
+                }
+                const uint32_t sh = (kg & 1) * 4;
+                const uint32_t v_lo = lds32(rb + ((kg * w12i::kTileN + ch_lo) * 16 + 4 * t));
+                const uint32_t v_hi = lds32(rb + ((kg * w12i::kTileN + ch_lo + 8) * 16 + 4 * t));
+                decode_word(v_lo, nib_lo >> sh, cc[mb][0], p.mul16, a[mb][kgl][0], a[mb][kgl][2]);
+                decode_word(v_hi, nib_hi >> sh, cc[mb][1], p.mul16, a[mb][kgl][1], a[mb][kgl][3]);
+            }
+        }
+        // escaped slots: the owning lane replaces the filler by the exact value
+        {
+            const int32_t e0 = esc_off_s[i] - e_lo, e1 = esc_off_s[i + 1] - e_lo;
+            for (int e = e0; e < e1; ++e) {
+                const uint32_t en = esc_cached ? esc_s[e] : __ldg(p.esc + e_lo + e);
+                const int nl = (en >> 22) & 0x7F, kl = (en >> 16) & 0x3F;
+                const int kg = kl >> 4;
+                if ((nl >> 5) != mw || (kg / C::kKgPerWarp) != wk) continue;
+                const int kk = kl & 15;
+                if (lane != ((nl & 7) * 4 + ((kk & 7) >> 1))) continue;
+                const int mb_e = (nl >> 4) & 1, kgl_e = kg % C::kKgPerWarp;
+                const int j_e = (kk >> 3) * 2 + ((nl >> 3) & 1);
+                const uint32_t val = en & 0xFFFFu;
+                const bool upper = kk & 1;
+#pragma unroll
+                for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+                    for (int kgl = 0; kgl < C::kKgPerWarp; ++kgl)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (mb == mb_e && kgl == kgl_e && j == j_e)
+                                a[mb][kgl][j] = upper ? ((a[mb][kgl][j] & 0x0000FFFFu) | (val << 16))
+                                                      : ((a[mb][kgl][j] & 0xFFFF0000u) | val);
+            }
+        }
+        // activations (B operand) from the swizzled TMA block, then MMA
+#pragma unroll
+        for (int kgl = 0; kgl < C::kKgPerWarp; ++kgl) {
+            const int kg = wk * C::kKgPerWarp + kgl;
+            if constexpr (NB8 == 1) {
+                const int row = lane & 7, chunk = 2 * kg + ((lane >> 3) & 1);
+                uint32_t b0, b1;
+                ldsm_x2(xb + row * 128 + ((chunk ^ (row & 7)) << 4), b0, b1);
+#pragma unroll
+                for (int mb = 0; mb < 2; ++mb) mma_bf16_16816(acc[mb][0], a[mb][kgl], b0, b1);
+            } else {
+#pragma unroll
+                for (int nb = 0; nb < NB8; nb += 2) {
+                    const int q = lane >> 3;
+                    const int row = (nb + (q >> 1)) * 8 + (lane & 7), chunk = 2 * kg + (q & 1);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(xb + row * 128 + ((chunk ^ (row & 7)) << 4), b0, b1, b2, b3);
+#pragma unroll
+                    for (int mb = 0; mb < 2; ++mb) {
+                        mma_bf16_16816(acc[mb][nb], a[mb][kgl], b0, b1);
+                        mma_bf16_16816(acc[mb][nb + 1], a[mb][kgl], b2, b3);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+    }
+    if (cur_nt >= 0) flush(cur_nt);
+}
+
+// second stage of the LM-head argmax: one CTA per row, fixed-order reduction
+__global__ void __launch_bounds__(256) k_argmax_stage2(const float *s1_val, const int32_t *s1_idx, int32_t n_tiles,
+                                                       int32_t *argmax, float *maxlogit)
+{
+    pdl_wait();
+    const int row = blockIdx.x;
+    float bv = __int_as_float(0x7fc00000);
+    int32_t bi = 0x7fffffff;
+    for (int i = threadIdx.x; i < n_tiles; i += blockDim.x) {
+        const float v = s1_val[(int64_t)row * n_tiles + i];
+        const int32_t ix = s1_idx[(int64_t)row * n_tiles + i];
+        if (beats(v, ix, bv, bi)) bv = v, bi = ix;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int32_t oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (beats(ov, oi, bv, bi)) bv = ov, bi = oi;
+    }
+    __shared__ float sv[8];
+    __shared__ int32_t si[8];
+    if ((threadIdx.x & 31) == 0) sv[threadIdx.x >> 5] = bv, si[threadIdx.x >> 5] = bi;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < (int)(blockDim.x >> 5); ++w)
+            if (beats(sv[w], si[w], bv, bi)) bv = sv[w], bi = si[w];
+        argmax[row] = (bi == 0x7fffffff) ? 0 : bi;
+        if (maxlogit) maxlogit[row] = bv;
+    }
+    pdl_launch_dependents();
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+template <int NB8, int WK>
+int launch_t(const w12i::GemmArgs &a, const CUtensorMap &xmap, cudaStream_t st)
+{
+    using C = Cfg<NB8, WK>;
+    const int64_t T = (int64_t)a.w.n_tiles * a.w.k_tiles;
+    const int G = (int)std::min<int64_t>(a.num_sms, T);
+    const int max_recs = (int)((T + G - 1) / G);
+    KParams p{};
+    p.rec = a.w.rec;
+    p.base = a.w.base;
+    p.esc_off = a.w.esc_off;
+    p.esc = a.w.esc;
+    p.n_tiles = a.w.n_tiles;
+    p.k_tiles = a.w.k_tiles;
+    p.R = a.R;
+    p.mode = a.mode;
+    p.y = a.y;
+    p.ldy = a.w.n;
+    p.s1_val = a.stage1_val;
+    p.s1_idx = a.stage1_idx;
+    p.partial = a.partial;
+    p.counters = a.counters;
+    p.status = a.status;
+    p.mul16 = 16u;
+    p.debug_flags = a.debug_flags;
+    p.timeout_ns = a.timeout_ns;
+    p.max_recs = max_recs;
+    p.esc_cap = 2048;
+    p.base_tiles = std::min<int>(64, (int)(max_recs / a.w.k_tiles + 2));
+    const int budget = 227 * 1024;
+    int stages = 8;
+    while (stages > 2 && smem_plan<NB8, WK>(stages, max_recs, p.esc_cap, p.base_tiles).total > budget) --stages;
+    p.stages = stages;
+    const int smem = smem_plan<NB8, WK>(stages, max_recs, p.esc_cap, p.base_tiles).total;
+    if (smem > budget) return (int)cudaErrorInvalidConfiguration;
+    cudaError_t e = cudaFuncSetAttribute(k_w12_gemm<NB8, WK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return (int)e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(G);
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.pdl ? 1 : 0;
+    return (int)cudaLaunchKernelEx(&cfg, k_w12_gemm<NB8, WK>, xmap, p);
+}
+
+}  // namespace
+
+namespace w12i {
+
+int launch_gemm(const GemmArgs &a, void *stream)
+{
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return (int)cudaErrorNotSupported;
+    int nb8 = (a.R + 7) / 8;
+    nb8 = nb8 <= 1 ? 1 : nb8 <= 2 ? 2 : nb8 <= 4 ? 4 : 8;
+    CUtensorMap xmap;
+    const cuuint64_t dims[2] = {(cuuint64_t)a.w.k, (cuuint64_t)a.R};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.w.k * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kTileK, (cuuint32_t)(nb8 * 8)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(a.x), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return (int)cudaErrorInvalidValue;
+    switch (nb8) {
+    case 1: return launch_t<1, 2>(a, xmap, st);
+    case 2: return launch_t<2, 2>(a, xmap, st);
+    case 4: return launch_t<4, 2>(a, xmap, st);
+    default: return launch_t<8, 2>(a, xmap, st);
+    }
+}
+
+int launch_argmax_stage2(const float *s1_val, const int32_t *s1_idx, int32_t R, int32_t n_tiles, int32_t *argmax,
+                         float *maxlogit, bool pdl, void *stream)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(R);
+    cfg.blockDim = dim3(256);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return (int)cudaLaunchKernelEx(&cfg, k_argmax_stage2, s1_val, s1_idx, n_tiles, argmax, maxlogit);
+}
+
+}  // namespace w12i

@@ -1,0 +1,421 @@
+// C ABI of the W12 tree-verify library: argument validation (before any
+// launch), workspace layout and the sequencing of the CUDA kernels.
+//
+// Typed refusal before anything runs follows the poot-llm speculative
+// decoding docs ("What is refused": a typed error before anything compiles or
+// uploads).  Everything that touches data on the device is a kernel of this
+// library; nothing here computes on the host.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "w12.h"
+#include "w12_debug.h"
+#include "w12_internal.h"
+
+using namespace w12i;
+
+namespace {
+
+int32_t g_debug_flags = 0;
+uint64_t g_timeout_ns = 2000000000ull;   // 2 s per bounded wait
+
+constexpr int kMaxCtas = 256;            // persistent grids never exceed this
+
+// benchmark timing hook (see w12_debug.h)
+bool g_profile = false;
+constexpr int kProfMax = 1024;
+cudaEvent_t g_prof_ev[kProfMax + 1];
+int g_prof_created = 0, g_prof_used = 0;
+
+int prof_mark(cudaStream_t st)
+{
+    if (!g_profile || g_prof_used > kProfMax) return 0;
+    if (g_prof_used >= g_prof_created) {
+        if (cudaEventCreate(&g_prof_ev[g_prof_created]) != cudaSuccess) return 1;
+        ++g_prof_created;
+    }
+    return (int)cudaEventRecord(g_prof_ev[g_prof_used++], st);
+}
+constexpr int kPartialRows = 64;         // rows per GEMM launch (larger R is sliced)
+
+int num_sms()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return kMaxCtas;
+    static int cached_dev = -1, cached = 0;
+    if (dev != cached_dev) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return kMaxCtas;
+        cached_dev = dev;
+        cached = std::min(n, kMaxCtas);
+    }
+    return cached;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+w12_status weight_ok(const w12_weight *w)
+{
+    if (!w || !w->rec || !w->base || !w->esc_tile_off) return W12_E_INVAL;
+    if (w->n <= 0 || w->k <= 0 || w->n_escapes < 0) return W12_E_INVAL;
+    if (w->n_escapes > 0 && !w->esc) return W12_E_INVAL;
+    if (w->n % kTileN || w->k % kTileK) return W12_E_UNSUPPORTED;
+    if (w->n / kTileN > INT32_MAX || w->k / kTileK > INT32_MAX) return W12_E_UNSUPPORTED;
+    if (!aligned(w->rec, 16)) return W12_E_INVAL;
+    return W12_OK;
+}
+
+DevWeight dev_weight(const w12_weight *w)
+{
+    DevWeight d;
+    d.rec = static_cast<const uint8_t *>(w->rec);
+    d.base = w->base;
+    d.esc_off = w->esc_tile_off;
+    d.esc = w->esc;
+    d.n_tiles = static_cast<int32_t>(w->n / kTileN);
+    d.k_tiles = static_cast<int32_t>(w->k / kTileK);
+    d.n = w->n;
+    d.k = w->k;
+    return d;
+}
+
+w12_status cuda_status(int e) { return e == 0 ? W12_OK : W12_E_CUDA; }
+
+struct Ws {
+    uint8_t *base;
+    WsLayout L;
+    int32_t *status() const { return reinterpret_cast<int32_t *>(base + L.status); }
+    int64_t *mismatch() const { return reinterpret_cast<int64_t *>(base + L.status + 64); }
+    int32_t *counters(int slot) const
+    {
+        return reinterpret_cast<int32_t *>(base + L.counters) + static_cast<size_t>(slot) * L.max_tiles_n;
+    }
+    float *partial(int slot) const
+    {
+        return reinterpret_cast<float *>(base + L.partial) +
+               static_cast<size_t>(slot) * kMaxCtas * 2 * kPartialRows * kTileN;
+    }
+    // arrival counters start at zero for every call (the kernels also reset
+    // each counter they finish with, so launches inside one call need no memset)
+    int clear_counters(cudaStream_t st) const
+    {
+        return (int)cudaMemsetAsync(base + L.counters, 0, static_cast<size_t>(kGemmSlots) * L.max_tiles_n * 4, st);
+    }
+    float *s1_val() const { return reinterpret_cast<float *>(base + L.stage1_val); }
+    int32_t *s1_idx() const { return reinterpret_cast<int32_t *>(base + L.stage1_idx); }
+    void *tree() const { return base + L.tree; }
+};
+
+// The layout depends only on the sizes, so a workspace sized for a call is
+// laid out identically by every call whose sizes it covers.
+WsLayout layout_for(int32_t R, int64_t max_n, int64_t vocab, int32_t n_req)
+{
+    WsLayout L{};
+    L.rows8 = (std::max<int32_t>(R, 1) + 7) / 8 * 8;
+    L.max_tiles_n = std::max<int64_t>(std::max<int64_t>(max_n, vocab), kTileN) / kTileN;
+    L.vocab_tiles = std::max<int64_t>(vocab, kTileN) / kTileN;
+    L.max_ctas = kMaxCtas;
+    size_t o = 0;
+    L.status = o;
+    o += 256;
+    L.counters = o;
+    o = align256(o + static_cast<size_t>(kGemmSlots) * L.max_tiles_n * 4);
+    L.partial = o;
+    o = align256(o + static_cast<size_t>(kGemmSlots) * kMaxCtas * 2 * kPartialRows * kTileN * 4);
+    L.stage1_val = o;
+    o = align256(o + static_cast<size_t>(L.rows8) * L.vocab_tiles * 4);
+    L.stage1_idx = o;
+    o = align256(o + static_cast<size_t>(L.rows8) * L.vocab_tiles * 4);
+    L.tree = o;
+    o = align256(o + tree_ws_bytes(n_req));
+    L.total = o;
+    return L;
+}
+
+w12_status ws_check(void *ws, size_t ws_bytes, const WsLayout &L)
+{
+    if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return W12_E_WORKSPACE;
+    return W12_OK;
+}
+
+int gemm_slices(const DevWeight &dw, const uint16_t *x, int32_t R, int mode, uint16_t *y, const Ws &ws, int &slot,
+                bool pdl, cudaStream_t st)
+{
+    for (int32_t r0 = 0; r0 < R; r0 += kPartialRows) {
+        GemmArgs a{};
+        a.w = dw;
+        a.x = x + static_cast<int64_t>(r0) * dw.k;
+        a.R = std::min<int32_t>(kPartialRows, R - r0);
+        a.mode = mode;
+        a.y = y ? y + static_cast<int64_t>(r0) * dw.n : nullptr;
+        a.stage1_val = ws.s1_val() + static_cast<int64_t>(r0) * dw.n_tiles;
+        a.stage1_idx = ws.s1_idx() + static_cast<int64_t>(r0) * dw.n_tiles;
+        a.partial = ws.partial(slot);
+        a.counters = ws.counters(slot);
+        a.status = ws.status();
+        a.num_sms = num_sms();
+        a.pdl = pdl;
+        a.debug_flags = g_debug_flags;
+        a.timeout_ns = g_timeout_ns;
+        const int e = launch_gemm(a, st);
+        if (e) return e;
+        if (int pe = prof_mark(st)) return pe;
+        slot = (slot + 1) % kGemmSlots;
+        pdl = true;
+    }
+    return 0;
+}
+
+w12_status tree_ok(const w12_tree *t, bool need_rows)
+{
+    if (!t || !t->parent || !t->token || !t->depth || !t->req_row_off) return W12_E_INVAL;
+    if (need_rows && (t->R < 1 || t->R > kMaxBudget)) return t->R < 1 ? W12_E_INVAL : W12_E_UNSUPPORTED;
+    return W12_OK;
+}
+
+}  // namespace
+
+namespace w12i {
+WsLayout ws_layout(int32_t R, int64_t max_n, int64_t vocab, int32_t n_req, int)
+{
+    return layout_for(R, max_n, vocab, n_req);
+}
+}  // namespace w12i
+
+extern "C" {
+
+const char *w12_status_str(int status)
+{
+    switch (status) {
+    case W12_OK: return "W12_OK";
+    case W12_E_INVAL: return "W12_E_INVAL";
+    case W12_E_UNSUPPORTED: return "W12_E_UNSUPPORTED";
+    case W12_E_MISMATCH: return "W12_E_MISMATCH";
+    case W12_E_CUDA: return "W12_E_CUDA";
+    case W12_E_TIMEOUT: return "W12_E_TIMEOUT";
+    case W12_E_WORKSPACE: return "W12_E_WORKSPACE";
+    default: return "W12_E_UNKNOWN";
+    }
+}
+
+int w12_abi_version(void) { return 100; }
+
+void w12_debug_set(int32_t flags, uint64_t timeout_ns)
+{
+    g_debug_flags = flags;
+    g_timeout_ns = timeout_ns ? timeout_ns : 2000000000ull;
+}
+
+int32_t w12_debug_num_sms(void) { return num_sms(); }
+
+void w12_debug_profile(int32_t enable)
+{
+    g_profile = enable != 0;
+    g_prof_used = 0;
+}
+
+int32_t w12_debug_profile_read(float *ms, int32_t max)
+{
+    if (!ms || max < 0) return W12_E_INVAL;
+    if (g_prof_used < 2) return 0;
+    if (cudaEventSynchronize(g_prof_ev[g_prof_used - 1]) != cudaSuccess) return W12_E_CUDA;
+    const int n = std::min(g_prof_used - 1, max);
+    for (int i = 0; i < n; ++i)
+        if (cudaEventElapsedTime(&ms[i], g_prof_ev[i], g_prof_ev[i + 1]) != cudaSuccess) return W12_E_CUDA;
+    return g_prof_used - 1;
+}
+
+size_t w12_workspace_bytes(int32_t R, int64_t max_n, int64_t vocab, int32_t n_req)
+{
+    if (R < 1 || R > kMaxRows || max_n < 0 || vocab < 0 || n_req < 0 || n_req > kMaxBudget) return 0;
+    return layout_for(R, max_n, vocab, n_req).total;
+}
+
+w12_status w12_workspace_init(void *ws, size_t ws_bytes, w12_stream_t stream)
+{
+    if (!ws || !aligned(ws, 256) || ws_bytes < 256) return W12_E_WORKSPACE;
+    return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w12_status w12_status_fetch(void *ws, w12_stream_t stream)
+{
+    if (!ws || !aligned(ws, 256)) return W12_E_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, ws, sizeof v, cudaMemcpyDeviceToHost, st) != cudaSuccess) return W12_E_CUDA;
+    if (cudaMemsetAsync(ws, 0, sizeof v, st) != cudaSuccess) return W12_E_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return W12_E_CUDA;
+    return static_cast<w12_status>(v);
+}
+
+w12_status w12_unpack(const w12_weight *w, uint16_t *dst_bf16, w12_stream_t stream)
+{
+    w12_status s = weight_ok(w);
+    if (s != W12_OK) return s;
+    if (!dst_bf16 || !aligned(dst_bf16, 16)) return W12_E_INVAL;
+    return cuda_status(launch_unpack(dev_weight(w), dst_bf16, nullptr, nullptr, nullptr, stream));
+}
+
+w12_status w12_load_check(const w12_weight *w, const uint16_t *src_bf16, int64_t *mismatches, void *ws,
+                          size_t ws_bytes, w12_stream_t stream)
+{
+    w12_status s = weight_ok(w);
+    if (s != W12_OK) return s;
+    if (!src_bf16 || !mismatches || !aligned(src_bf16, 16)) return W12_E_INVAL;
+    if (!ws || !aligned(ws, 256) || ws_bytes < 256) return W12_E_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int64_t *dev_count = reinterpret_cast<int64_t *>(static_cast<uint8_t *>(ws) + 64);
+    if (cudaMemsetAsync(dev_count, 0, sizeof(int64_t), st) != cudaSuccess) return W12_E_CUDA;
+    if (launch_unpack(dev_weight(w), nullptr, src_bf16, dev_count, nullptr, stream)) return W12_E_CUDA;
+    int64_t host = 0;
+    if (cudaMemcpyAsync(&host, dev_count, sizeof host, cudaMemcpyDeviceToHost, st) != cudaSuccess) return W12_E_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return W12_E_CUDA;
+    *mismatches = host;
+    return host == 0 ? W12_OK : W12_E_MISMATCH;
+}
+
+w12_status w12_gemm(const w12_weight *w, const uint16_t *x, int32_t R, uint16_t *y, void *ws, size_t ws_bytes,
+                    w12_stream_t stream)
+{
+    w12_status s = weight_ok(w);
+    if (s != W12_OK) return s;
+    if (!x || !y || !aligned(x, 16) || !aligned(y, 16)) return W12_E_INVAL;
+    if (R < 1) return W12_E_INVAL;
+    if (R > kMaxRows) return W12_E_UNSUPPORTED;
+    const WsLayout L = layout_for(R, w->n, 0, 0);
+    if ((s = ws_check(ws, ws_bytes, L)) != W12_OK) return s;
+    Ws W{static_cast<uint8_t *>(ws), L};
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (W.clear_counters(st)) return W12_E_CUDA;
+    int slot = 0;
+    return cuda_status(gemm_slices(dev_weight(w), x, R, kModeLinear, y, W, slot, false, st));
+}
+
+w12_status w12_lmhead_argmax(const w12_weight *head, const uint16_t *h, int32_t R, int32_t *argmax, float *maxlogit,
+                             void *ws, size_t ws_bytes, w12_stream_t stream)
+{
+    w12_status s = weight_ok(head);
+    if (s != W12_OK) return s;
+    if (!h || !argmax || !aligned(h, 16)) return W12_E_INVAL;
+    if (R < 1) return W12_E_INVAL;
+    if (R > kMaxRows) return W12_E_UNSUPPORTED;
+    const WsLayout L = layout_for(R, 0, head->n, 0);
+    if ((s = ws_check(ws, ws_bytes, L)) != W12_OK) return s;
+    Ws W{static_cast<uint8_t *>(ws), L};
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (W.clear_counters(st)) return W12_E_CUDA;
+    int slot = 0;
+    const DevWeight dw = dev_weight(head);
+    if (int e = gemm_slices(dw, h, R, kModeHead, nullptr, W, slot, false, st)) return cuda_status(e);
+    return cuda_status(launch_argmax_stage2(W.s1_val(), W.s1_idx(), R, dw.n_tiles, argmax, maxlogit, true, st));
+}
+
+w12_status w12_tree_build(const w12_lattice *lat, int32_t budget, w12_tree *out, void *ws, size_t ws_bytes,
+                          w12_stream_t stream)
+{
+    if (!lat || !out || !lat->p_r || !lat->root_tok) return W12_E_INVAL;
+    if (lat->n_req < 1 || lat->p_max < 0 || lat->n_cand < 1 || budget < 1) return W12_E_INVAL;
+    if (lat->p_max > 0 && (!lat->cand_tok || !lat->cand_logp)) return W12_E_INVAL;
+    if (lat->n_req > kMaxBudget || lat->p_max > kMaxPositions || lat->n_cand > kCands || budget > kMaxBudget)
+        return W12_E_UNSUPPORTED;
+    if (budget < lat->n_req) return W12_E_INVAL;
+    if (!out->parent || !out->token || !out->depth || !out->req || !out->score || !out->rank || !out->req_row_off)
+        return W12_E_INVAL;
+    // rows = min(budget, nodes the lattice can hold), known before any launch
+    int64_t nodes = 0;
+    for (int32_t r = 0; r < lat->n_req; ++r) {
+        const int32_t pr = lat->p_r[r];
+        if (pr < 0 || pr > lat->p_max) return W12_E_INVAL;
+        int64_t level = 1, sum = 1;
+        for (int32_t d = 1; d <= pr && sum < budget; ++d) {
+            level = std::min<int64_t>(level * lat->n_cand, budget);
+            sum += level;
+        }
+        nodes = std::min<int64_t>(nodes + sum, budget);
+    }
+    const WsLayout L = layout_for(1, 0, 0, lat->n_req);
+    w12_status s = ws_check(ws, ws_bytes, L);
+    if (s != W12_OK) return s;
+    Ws W{static_cast<uint8_t *>(ws), L};
+    out->R = static_cast<int32_t>(nodes);
+    TreeArgs a{};
+    a.n_req = lat->n_req;
+    a.p_max = lat->p_max;
+    a.n_cand = lat->n_cand;
+    a.conditional = lat->conditional ? 1 : 0;
+    a.budget = budget;
+    a.R = out->R;
+    a.p_r_host = lat->p_r;
+    a.root_tok = lat->root_tok;
+    a.cand_tok = lat->cand_tok;
+    a.cand_logp = lat->cand_logp;
+    a.parent = out->parent;
+    a.token = out->token;
+    a.req = out->req;
+    a.req_row_off = out->req_row_off;
+    a.depth = out->depth;
+    a.rank = out->rank;
+    a.score = out->score;
+    a.scratch = W.tree();
+    a.status = W.status();
+    return cuda_status(launch_tree_build(a, stream));
+}
+
+w12_status w12_tree_accept(const w12_tree *tree, int32_t n_req, int32_t p_max, const int32_t *argmax, int32_t *acc_tok,
+                           int32_t *acc_len, int32_t *acc_node, w12_stream_t stream)
+{
+    w12_status s = tree_ok(tree, true);
+    if (s != W12_OK) return s;
+    if (!argmax || !acc_tok || !acc_len) return W12_E_INVAL;
+    if (n_req < 1 || p_max < 0) return W12_E_INVAL;
+    if (n_req > kMaxBudget || p_max > kMaxPositions) return W12_E_UNSUPPORTED;
+    return cuda_status(launch_tree_accept(tree->parent, tree->token, tree->depth, tree->req_row_off, tree->R, n_req,
+                                          p_max, argmax, acc_tok, acc_len, acc_node, false, stream));
+}
+
+w12_status w12_verify_step(const w12_step *step, const w12_tree *tree, int32_t n_req, int32_t p_max, int32_t *acc_tok,
+                           int32_t *acc_len, int32_t *acc_node, void *ws, size_t ws_bytes, w12_stream_t stream)
+{
+    if (!step || step->n_linear < 0 || (step->n_linear > 0 && (!step->lin || !step->x || !step->y)))
+        return W12_E_INVAL;
+    w12_status s = tree_ok(tree, true);
+    if (s != W12_OK) return s;
+    if (!acc_tok || !acc_len || !step->h || !step->argmax || !aligned(step->h, 16)) return W12_E_INVAL;
+    if (n_req < 1 || p_max < 0) return W12_E_INVAL;
+    if (n_req > kMaxBudget || p_max > kMaxPositions) return W12_E_UNSUPPORTED;
+    const int32_t R = tree->R;
+    if (R > kMaxRows) return W12_E_UNSUPPORTED;
+    if ((s = weight_ok(step->head)) != W12_OK) return s;
+    int64_t max_n = 0;
+    for (int32_t l = 0; l < step->n_linear; ++l) {
+        if ((s = weight_ok(&step->lin[l])) != W12_OK) return s;
+        if (!step->x[l] || !step->y[l] || !aligned(step->x[l], 16) || !aligned(step->y[l], 16)) return W12_E_INVAL;
+        max_n = std::max<int64_t>(max_n, step->lin[l].n);
+    }
+    const WsLayout L = layout_for(R, max_n, step->head->n, n_req);
+    if ((s = ws_check(ws, ws_bytes, L)) != W12_OK) return s;
+    Ws W{static_cast<uint8_t *>(ws), L};
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (W.clear_counters(st)) return W12_E_CUDA;
+    g_prof_used = 0;
+    if (prof_mark(st)) return W12_E_CUDA;
+    int slot = 0;
+    for (int32_t l = 0; l < step->n_linear; ++l)
+        if (int e = gemm_slices(dev_weight(&step->lin[l]), step->x[l], R, kModeLinear, step->y[l], W, slot, true, st))
+            return cuda_status(e);
+    const DevWeight hw = dev_weight(step->head);
+    if (int e = gemm_slices(hw, step->h, R, kModeHead, nullptr, W, slot, true, st)) return cuda_status(e);
+    if (int e = launch_argmax_stage2(W.s1_val(), W.s1_idx(), R, hw.n_tiles, step->argmax, nullptr, true, st))
+        return cuda_status(e);
+    if (prof_mark(st)) return W12_E_CUDA;
+    if (int e = launch_tree_accept(tree->parent, tree->token, tree->depth, tree->req_row_off, R, n_req, p_max,
+                                   step->argmax, acc_tok, acc_len, acc_node, true, stream))
+        return cuda_status(e);
+    return prof_mark(st) ? W12_E_CUDA : W12_OK;
+}
+
+}  // extern "C"

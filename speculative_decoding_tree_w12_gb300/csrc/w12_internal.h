@@ -1,0 +1,96 @@
+// Internal declarations shared by the host ABI layer and the CUDA kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "w12.h"
+
+namespace w12i {
+
+constexpr int kTileN = 128;          // output channels per W12 record
+constexpr int kTileK = 64;           // input features per W12 record
+constexpr int kRecBytes = 12288;     // one record: 8 KB view plane + 4 KB low nibbles
+constexpr int kViewBytes = 8192;
+constexpr int kMaxRows = 256;
+constexpr int kMaxBudget = 512;
+constexpr int kMaxPositions = 16;
+constexpr int kCands = 16;
+constexpr int kGemmSlots = 2;        // consecutive GEMMs alternate workspace slots
+
+// Device status word values (first condition wins).
+constexpr int32_t kDevOk = 0;
+
+// Byte layout of the caller's workspace.  Every region is 256-byte aligned.
+struct WsLayout {
+    size_t status;        // int32[64]: [0] status, [1] detail, [8] mismatch count (int64)
+    size_t counters;      // int32[kGemmSlots][max_tiles_n]: split-tile arrival counters
+    size_t partial;       // float[kGemmSlots][max_ctas][2][rows8][128]
+    size_t stage1_val;    // float[rows][vocab_tiles]
+    size_t stage1_idx;    // int32[rows][vocab_tiles]
+    size_t tree;          // tree-build scratch
+    size_t total;
+    int64_t max_tiles_n, max_ctas, rows8, vocab_tiles;
+};
+
+WsLayout ws_layout(int32_t R, int64_t max_n, int64_t vocab, int32_t n_req, int num_sms);
+size_t tree_ws_bytes(int32_t n_req);
+
+// ---------------------------------------------------------------------------
+// kernel launchers (defined in the .cu files); all return cudaError_t as int
+// ---------------------------------------------------------------------------
+
+struct DevWeight {
+    const uint8_t *rec;
+    const uint8_t *base;
+    const int32_t *esc_off;
+    const uint32_t *esc;
+    int32_t n_tiles, k_tiles;
+    int64_t n, k;
+};
+
+int launch_unpack(const DevWeight &w, uint16_t *dst, const uint16_t *cmp, int64_t *mismatch, int32_t *status,
+                  void *stream);
+
+enum GemmMode : int32_t { kModeLinear = 0, kModeHead = 1 };
+
+struct GemmArgs {
+    DevWeight w;
+    const uint16_t *x;       // [R][k] row-major BF16
+    int32_t R;
+    int32_t mode;
+    uint16_t *y;             // linear: [R][n]
+    float *stage1_val;       // head: [R][n_tiles]
+    int32_t *stage1_idx;
+    float *partial;          // this call's slot
+    int32_t *counters;       // this call's slot
+    int32_t *status;
+    int num_sms;
+    bool pdl;                // launched as a programmatic dependent of the previous kernel
+    int32_t debug_flags;
+    uint64_t timeout_ns;
+};
+
+int launch_gemm(const GemmArgs &a, void *stream);
+int launch_argmax_stage2(const float *s1_val, const int32_t *s1_idx, int32_t R, int32_t n_tiles, int32_t *argmax,
+                         float *maxlogit, bool pdl, void *stream);
+
+struct TreeArgs {
+    int32_t n_req, p_max, n_cand, conditional, budget, R;
+    const int32_t *p_r_host;     // [n_req], host memory (copied into the launch parameters)
+    const int32_t *root_tok;
+    const int32_t *cand_tok;
+    const float *cand_logp;
+    int32_t *parent, *token, *req, *req_row_off;
+    uint8_t *depth, *rank;
+    float *score;
+    void *scratch;
+    int32_t *status;
+};
+
+int launch_tree_build(const TreeArgs &a, void *stream);
+int launch_tree_accept(const int32_t *parent, const int32_t *token, const uint8_t *depth,
+                       const int32_t *req_row_off, int32_t R, int32_t n_req, int32_t p_max, const int32_t *argmax,
+                       int32_t *acc_tok, int32_t *acc_len, int32_t *acc_node, bool pdl, void *stream);
+
+}  // namespace w12i

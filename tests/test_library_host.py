@@ -1,0 +1,138 @@
+"""Host-side checks of the C-ABI library (no GPU needed): it loads, exports
+every symbol the headers declare, its packer writes exactly the bytes of the
+oracle's packer (two independent implementations of one written format), and
+malformed calls are refused with a typed status before anything launches."""
+from __future__ import annotations
+
+import ctypes as C
+import glob
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from speculative_decoding_tree_w12_gb300 import synth
+import speculative_decoding_tree_w12_gb300 as w12
+from speculative_decoding_tree_w12_gb300 import build as w12build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    w12build.build()
+    return w12.lib()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(w12_\w+)\s*\(", src, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared_functions()
+    assert {"w12_pack", "w12_gemm", "w12_verify_step", "w12_tree_build", "w12_tree_accept",
+            "w12_lmhead_argmax", "w12_load_check", "w12_unpack"} <= names
+    for n in sorted(names):
+        assert hasattr(L, n), n
+
+
+def _lib_pack(w):
+    return w12.w12_pack(w)
+
+
+@pytest.mark.parametrize("case", ["tiny", "specials", "exhaustive", "zeros", "wide"])
+def test_host_packer_bytes_equal_oracle(L, case):
+    if case == "tiny":
+        w = synth.weights(1024, 512, 0, synth.STREAM_LINEAR, 0.01, 0.01)
+    elif case == "specials":
+        w = synth.weights(256, 384, 4, 1)
+        g = np.random.default_rng(0)
+        idx = g.choice(w.size, 3000, replace=False)
+        w.reshape(-1)[idx] = g.integers(0, 65536, size=3000).astype(np.uint16)
+    elif case == "exhaustive":
+        g = np.random.default_rng(1)
+        w = g.permutation(np.arange(65536, dtype=np.uint32).astype(np.uint16)).reshape(512, 128)
+    elif case == "zeros":
+        w = np.zeros((128, 64), np.uint16)
+    else:
+        w = synth.weights(384, 2048, 9, 2, 0.002, 0.0)
+    a = _lib_pack(w)
+    b = oracle.w12_pack(w)
+    assert np.array_equal(a.base, b.base)
+    assert np.array_equal(a.esc_tile_off, b.esc_tile_off)
+    assert np.array_equal(a.esc, b.esc)
+    assert np.array_equal(a.rec, b.rec)
+    # and the oracle decodes the library's bytes back to the source
+    assert np.array_equal(oracle.w12_unpack(oracle.Packed(a.n, a.k, a.rec, a.base, a.esc_tile_off, a.esc)), w)
+
+
+def test_pack_refuses_bad_shapes(L):
+    w = np.zeros((100, 64), np.uint16)
+    lay = w12.Layout()
+    assert L.w12_pack_query(w.ctypes.data_as(C.c_void_p), 100, 64, C.byref(lay)) == w12.W12_E_UNSUPPORTED
+    assert L.w12_pack_query(None, 128, 64, C.byref(lay)) == w12.W12_E_INVAL
+    assert L.w12_pack_query(w.ctypes.data_as(C.c_void_p), 0, 64, C.byref(lay)) == w12.W12_E_INVAL
+
+
+def _stream_k_bounds(T, G):
+    return [c * T // G for c in range(G + 1)]
+
+
+@pytest.mark.parametrize("T,G", [(64, 64), (3200, 152), (94960, 152), (4480, 152), (21760, 152), (7, 3),
+                                 (152 * 80 + 5, 152), (1000003, 148)])
+def test_stream_k_owner_formula(T, G):
+    """The kernel finds the CTA owning record r as ((r+1)*G - 1) // T; check
+    it against the CTA ranges [c*T//G, (c+1)*T//G)."""
+    b = _stream_k_bounds(T, G)
+    rs = np.unique(np.concatenate([np.arange(min(T, 5000)), np.asarray(b[1:-1]) - 1, np.asarray(b[1:-1]),
+                                   [T - 1]]))
+    for r in rs:
+        c = ((int(r) + 1) * G - 1) // T
+        assert b[c] <= r < b[c + 1], (r, c)
+
+
+def test_refusals_before_launch(L):
+    """Malformed calls return a typed status and launch nothing (these run
+    without a GPU because validation precedes every CUDA call)."""
+    fake = C.c_void_p(0x1000)   # never dereferenced: validation fails first
+    wt = w12.Weight(0x1000, 0x1000, 0x1000, None, 128, 64, 0)
+    ws = C.c_void_p(0x100000)
+    # null weight / null x
+    assert L.w12_gemm(None, fake, 4, fake, ws, 1 << 30, None) == w12.W12_E_INVAL
+    assert L.w12_gemm(C.byref(wt), None, 4, fake, ws, 1 << 30, None) == w12.W12_E_INVAL
+    # rows out of range
+    assert L.w12_gemm(C.byref(wt), fake, 0, fake, ws, 1 << 30, None) == w12.W12_E_INVAL
+    assert L.w12_gemm(C.byref(wt), fake, 257, fake, ws, 1 << 30, None) == w12.W12_E_UNSUPPORTED
+    # unsupported shape
+    bad = w12.Weight(0x1000, 0x1000, 0x1000, None, 100, 64, 0)
+    assert L.w12_gemm(C.byref(bad), fake, 4, fake, ws, 1 << 30, None) == w12.W12_E_UNSUPPORTED
+    # escapes announced but no list
+    noesc = w12.Weight(0x1000, 0x1000, 0x1000, None, 128, 64, 5)
+    assert L.w12_gemm(C.byref(noesc), fake, 4, fake, ws, 1 << 30, None) == w12.W12_E_INVAL
+    # workspace too small / misaligned
+    assert L.w12_gemm(C.byref(wt), fake, 4, fake, ws, 16, None) == w12.W12_E_WORKSPACE
+    assert L.w12_gemm(C.byref(wt), fake, 4, fake, C.c_void_p(0x100010), 1 << 30, None) == w12.W12_E_WORKSPACE
+    # tree: budget below the number of requests, too many positions
+    pr = np.asarray([4, 4], np.int32)
+    lat = w12.LatticeC(2, 4, 16, 0, pr.ctypes.data, 0x1000, 0x1000, 0x1000)
+    tr = w12.TreeC(0, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000)
+    assert L.w12_tree_build(C.byref(lat), 1, C.byref(tr), ws, 1 << 30, None) == w12.W12_E_INVAL
+    lat17 = w12.LatticeC(2, 17, 16, 0, pr.ctypes.data, 0x1000, 0x1000, 0x1000)
+    assert L.w12_tree_build(C.byref(lat17), 8, C.byref(tr), ws, 1 << 30, None) == w12.W12_E_UNSUPPORTED
+    prbad = np.asarray([5, 1], np.int32)
+    latb = w12.LatticeC(2, 4, 16, 0, prbad.ctypes.data, 0x1000, 0x1000, 0x1000)
+    assert L.w12_tree_build(C.byref(latb), 8, C.byref(tr), ws, 1 << 30, None) == w12.W12_E_INVAL
+    assert L.w12_tree_build(C.byref(lat), 600, C.byref(tr), ws, 1 << 30, None) == w12.W12_E_UNSUPPORTED
+    # accept with a tree of zero rows
+    assert L.w12_tree_accept(C.byref(tr), 2, 4, fake, fake, fake, None, None) == w12.W12_E_INVAL
+    assert L.w12_workspace_bytes(0, 128, 0, 1) == 0
+    assert L.w12_workspace_bytes(257, 128, 0, 1) == 0
+    assert w12.status_str(w12.W12_E_TIMEOUT) == "W12_E_TIMEOUT"
