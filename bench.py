@@ -1,0 +1,592 @@
+#!/usr/bin/env python
+"""Benchmark of the W12 tree-verify pass on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+best-first tree build from a drafter lattice, every W12 linear of the layer,
+the W12 LM head with per-row argmax, and greedy acceptance.  The headline
+metric is the effective W12 weight-stream bandwidth of the step (W12 bytes
+read per step / step time, GB/s), reported with the step time in
+microseconds and as a fraction of the HBM roofline.
+
+Default workload: one 27B-like decoder layer (QKV 5120->7168, O 5120->5120,
+gate/up 5120->34816, down 17408->5120) + LM head 5120x151936 in W12
+(1.66 GB), one request, a 32-row tree from a top-16 x 16-position lattice.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--rows R] [--impl reference]
+
+Multi-GPU (torchrun): the pass has no exchange step at this scope, so N GPUs
+run N independent replicas (weak scaling); value = all ranks' bytes / the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify-step µs and W12 weight-stream HBM GB/s (% of GB300 peak) vs tree rows"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+DESCRIPTIONS = {
+    "tiny": "1 linear 512->1024 + head 512x4096 (1% x64 outliers, 1% zeros), 8-row chain over 8 positions",
+    "single_27b": "one 27B-like layer (QKV 5120->7168, O 5120->5120, gate/up 5120->34816, down 17408->5120) "
+                  "+ LM head 5120x151936, W12; 1 request, 32-node tree from top-16 x 16 positions",
+    "batched_27b": "same shapes; 24 requests sharing a 192-node budget, 16/12/8 positions",
+    "b4_tree": "4B-like layer (2560->3584, 2560->2560, 2560->19456, 9728->2560) + head 2560x151936; "
+               "32 requests, 256-node budget, trees",
+    "b4_chain": "4B-like layer + head; 32 requests, 256-node budget, chains",
+    "full_depth_27b": "64 stacked 27B-like layers + LM head (32.9 GB W12 resident)",
+}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("k_gemm.cu", "w12_device.cuh"):
+        with open(os.path.join(ROOT, "speculative_decoding_tree_w12_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload):
+    """DRAM bytes per GEMM launch from a committed ncu summary, if it was taken
+    on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "w12_gemm_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        if d.get("kernel_source_hash") != kernel_source_hash():
+            return None
+        return d.get("per_step_bytes", {}).get(workload)
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = tempfile.mktemp(prefix="w12clk", suffix=".csv")
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------
+
+class Workload:
+    def __init__(self, name, rows, device, seed=0):
+        import torch
+        import speculative_decoding_tree_w12_gb300 as w12
+        from speculative_decoding_tree_w12_gb300 import synth
+
+        self.w12, self.torch, self.synth = w12, torch, synth
+        w = synth.WORKLOADS[name]
+        if rows:
+            w = synth.scaled(w, budget=int(rows))
+        self.wl, self.name, self.device = w, name, device
+        t0 = time.time()
+        self.lat = synth.lattice(w, seed)
+        # weights: generate, pack on the host (library packer, self-checked), upload
+        self.lin_bits, self.lin = [], []
+        distinct = {}
+        for layer in range(w.layers):
+            for i, (n, k) in enumerate(w.linears):
+                # stacked layers reuse 4 distinct weight sets (each layer still
+                # streams its own copy from HBM)
+                key = (layer % 4, i)
+                if key not in distinct:
+                    bits = synth.weights(n, k, seed, synth.STREAM_LINEAR + 100 * (layer % 4) + i,
+                                         w.outlier_frac, w.zero_frac)
+                    distinct[key] = (bits, w12.w12_pack(bits))
+                    if layer == 0:
+                        self.lin_bits.append(bits)
+                bits, hp = distinct[key]
+                self.lin.append(w12.DeviceWeight(hp, device))
+        self.head_bits = synth.weights(w.vocab, w.hidden, seed, synth.STREAM_HEAD, w.outlier_frac, w.zero_frac)
+        self.head_hp = w12.w12_pack(self.head_bits)
+        self.head = w12.DeviceWeight(self.head_hp, device)
+        self.lin_hp = [distinct[(0, i)][1] for i in range(len(w.linears))]
+        log(f"[bench] weights generated and packed in {time.time() - t0:.1f}s")
+        # tree (GPU), then the toy target's hidden rows for that tree
+        self.dlat = w12.DeviceLattice(self.lat, device)
+        max_n = max(n for n, _ in w.linears)
+        self.ws = w12.Workspace(min(w.budget, 256), max_n, w.vocab, w.n_req, device)
+        self.tree = w12.w12_tree_build(self.dlat, w.budget, self.ws)
+        torch.cuda.synchronize()
+        self.R = self.tree.R
+        th = self.tree.host()
+        self.h_bits = synth.hidden_rows(th["req"], th["parent"], th["token"], self.lat.truth, self.head_bits, seed)
+        self.x_bits = [synth.activations(self.R, k, seed, synth.STREAM_X + i) for i, (n, k) in enumerate(w.linears)]
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+        self.h = dev(self.h_bits)
+        xs_layer = [dev(x) for x in self.x_bits]
+        self.xs = [xs_layer[j % len(w.linears)] for j in range(len(self.lin))]
+        self.ys = [torch.empty((self.R, dw.n), dtype=torch.bfloat16, device=device) for dw in self.lin]
+        self.argmax = torch.empty(self.R, dtype=torch.int32, device=device)
+        self.acc_tok = torch.empty((w.n_req, w.p_max + 1), dtype=torch.int32, device=device)
+        self.acc_len = torch.empty(w.n_req, dtype=torch.int32, device=device)
+        self.step_args = w12.VerifyStep(self.lin, self.xs, self.ys, self.head, self.h, self.argmax)
+
+    # bytes ---------------------------------------------------------------
+    def w12_bytes(self):
+        return sum(d.nbytes for d in self.lin) + self.head.nbytes
+
+    def launch_bytes(self):
+        """Algorithmic bytes of each GEMM launch of a step, in launch order:
+        W12 record/base/escape bytes + activations in + outputs out."""
+        R = self.R
+        out = []
+        slices = (R + 63) // 64
+        for d in self.lin:
+            for s in range(slices):
+                r = min(64, R - 64 * s)
+                out.append(d.nbytes + r * d.k * 2 + r * d.n * 2)
+        for s in range(slices):
+            r = min(64, R - 64 * s)
+            out.append(self.head.nbytes + r * self.head.k * 2 + r * (self.head.n // 128) * 8)
+        return out
+
+    def gpu_launches_per_step(self):
+        slices = (self.R + 63) // 64
+        return 1 + slices * (len(self.lin) + 1) + 2
+
+    # the step ------------------------------------------------------------
+    def step(self):
+        w, w12 = self.wl, self.w12
+        w12.w12_tree_build(self.dlat, w.budget, self.ws, self.tree)
+        w12.w12_verify_step(self.step_args, self.tree, w.n_req, w.p_max, self.ws, self.acc_tok, self.acc_len)
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle, as it stands, on a bounded sample
+# ---------------------------------------------------------------------------
+
+def oracle_sample_runner(wk: Workload, frac: float):
+    """A callable that runs the oracle over the first `frac` of every weight's
+    output channels (multiples of 128, all rows): W12 decode (oracle unpack),
+    FP64 GEMM for the linears, FP64 logits + argmax for the head, then the
+    tree build and acceptance.  Returns (callable, sampled W12 bytes, text)."""
+    import oracle
+    jobs = []
+    total = 0
+    w = wk.wl
+    for bits, x in zip(wk.lin_bits, wk.x_bits):
+        n = max(128, int(bits.shape[0] * frac) // 128 * 128)
+        p = oracle.w12_pack(bits[:n])
+        jobs.append(("lin", p, x))
+        total += p.bytes
+    nh = max(128, int(wk.head_bits.shape[0] * frac) // 128 * 128)
+    ph = oracle.w12_pack(wk.head_bits[:nh])
+    jobs.append(("head", ph, wk.h_bits))
+    total += ph.bytes
+
+    def run():
+        for kind, p, x in jobs:
+            wdec = oracle.w12_unpack(p)
+            if kind == "lin":
+                oracle.gemm_f64(x, wdec)
+            else:
+                am, _, _ = oracle.head_argmax(x, wdec)
+        t = oracle.tree_build(wk.lat, w.budget)
+        oracle.tree_accept(t, np.resize(am, t.R), w.n_req, w.p_max)
+
+    text = (f"first {frac:.4f} of the output channels of every linear and of the LM head "
+            f"({total / 1e6:.1f} MB of W12), all {wk.R} rows; decode + FP64 GEMM/argmax + tree build + accept")
+    return run, total, text
+
+
+def cpu_baseline(wk: Workload, target_s=10.0):
+    import oracle
+    oracle.build()
+    run, b0, _ = oracle_sample_runner(wk, 1.0 / 64)
+    t = time.time()
+    run()
+    dt = max(time.time() - t, 1e-3)
+    frac = min(1.0, (1.0 / 64) * target_s / dt)
+    run, b, text = oracle_sample_runner(wk, frac)
+    t = time.time()
+    run()
+    dt = time.time() - t
+    cores = os.cpu_count() or 1
+    return {"value": b / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": text,
+            "seconds": round(dt, 2)}
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the oracle timed as it stands
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from speculative_decoding_tree_w12_gb300 import synth
+    import oracle
+    oracle.build()
+
+    class HostOnly:
+        pass
+
+    w = synth.WORKLOADS[args.workload]
+    if args.rows:
+        w = synth.scaled(w, budget=args.rows)
+    wk = HostOnly()
+    wk.wl = w
+    wk.lat = synth.lattice(w, 0)
+    frac = 1.0 / 32
+    # sampled weights only (the reference arm never touches the GPU)
+    wk.lin_bits = []
+    for i, (n, k) in enumerate(w.linears):
+        nn = max(128, int(n * frac) // 128 * 128)
+        wk.lin_bits.append(synth.weights(n, k, 0, synth.STREAM_LINEAR + i, w.outlier_frac, w.zero_frac)[:nn])
+    t = oracle.tree_build(wk.lat, w.budget)
+    wk.R = t.R
+    wk.head_bits = synth.weights(w.vocab, w.hidden, 0, synth.STREAM_HEAD, w.outlier_frac, w.zero_frac)
+    wk.h_bits = synth.hidden_rows(t.req, t.parent, t.token, wk.lat.truth, wk.head_bits, 0)
+    nh = max(128, int(w.vocab * frac) // 128 * 128)
+    wk.head_bits = wk.head_bits[:nh]
+    wk.x_bits = [synth.activations(t.R, k, 0, synth.STREAM_X + i) for i, (n, k) in enumerate(w.linears)]
+    run, nbytes, text = oracle_sample_runner(wk, 1.0)
+    for _ in range(args.warmup):
+        run()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.time()
+        run()
+        times.append(time.time() - t0)
+    total = sum(times)
+    value = nbytes * args.steps / total / 1e9
+    cores = os.cpu_count() or 1
+    text = text.replace("first 1.0000 of the output channels", f"first {frac:.4f} of the output channels")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {DESCRIPTIONS.get(args.workload, '')}", "rows": int(t.R)},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": text},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="w12", choices=["w12", "reference"])
+    ap.add_argument("--workload", default="single_27b")
+    ap.add_argument("--rows", type=int, default=0, help="override the node budget (tree rows)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cublas", action="store_true")
+    ap.add_argument("--no-graph", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        log("[bench] warmup raised to 3")
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+
+    from speculative_decoding_tree_w12_gb300 import build as w12build
+    if rank == 0 or world == 1:
+        w12build.build()
+    if dist:
+        dist.barrier()
+    import speculative_decoding_tree_w12_gb300 as w12
+
+    wk = Workload(args.workload, args.rows, device)
+    W, K = args.warmup, args.steps
+    for _ in range(W):
+        wk.step()
+    torch.cuda.synchronize()
+    st = wk.ws.status()
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {w12.status_str(st)}")
+    ref_tok = wk.acc_tok.clone()
+    ref_len = wk.acc_len.clone()
+
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            wk.step()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph):
+            wk.step()
+        for _ in range(W):
+            graph.replay()
+        torch.cuda.synchronize()
+
+    run = graph.replay if graph is not None else wk.step
+
+    # ------------------------------------------------------------ timed region
+    clk = ClockSampler(local)
+    clk.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = clk.stop()
+    ms = e0.elapsed_time(e1) / K
+    if dist:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    st = wk.ws.status()
+    if st != 0 or not torch.equal(wk.acc_tok, ref_tok) or not torch.equal(wk.acc_len, ref_len):
+        raise RuntimeError(f"timed steps diverged from the warm-up result (status {w12.status_str(st)})")
+
+    w12_bytes = wk.w12_bytes()
+    value = world * w12_bytes / (ms * 1e-3) / 1e9
+
+    # ------------------------------------------------ per-launch roofline pass
+    w12.profile(True)
+    per_launch = None
+    tb_ms = []
+    for _ in range(K):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        w12.w12_tree_build(wk.dlat, wk.wl.budget, wk.ws, wk.tree)
+        b.record()
+        w12.w12_verify_step(wk.step_args, wk.tree, wk.wl.n_req, wk.wl.p_max, wk.ws, wk.acc_tok, wk.acc_len)
+        lt = np.asarray(w12.profile_read())
+        torch.cuda.synchronize()
+        tb_ms.append(a.elapsed_time(b))
+        per_launch = lt if per_launch is None else per_launch + lt
+    w12.profile(False)
+    per_launch = per_launch / K
+    lb = wk.launch_bytes()
+    n_gemm = len(lb)
+    gemm_ms = per_launch[:n_gemm]
+    gemm_bytes = float(sum(lb))
+    achieved = gemm_bytes / (float(gemm_ms.sum()) * 1e-3) / 1e9
+    peak, peak_kind = load_peaks()
+    traffic = committed_traffic(args.workload)
+    kernels = {
+        "tree_build_us": 1e3 * float(np.mean(tb_ms)),
+        "w12_gemm_us": [round(1e3 * float(v), 2) for v in gemm_ms],
+        "w12_gemm_gbs": [round(b / (float(v) * 1e-3) / 1e9, 1) for b, v in zip(lb, gemm_ms)],
+        "argmax_stage2_us": 1e3 * float(per_launch[n_gemm]),
+        "accept_us": 1e3 * float(per_launch[n_gemm + 1]),
+    }
+
+    # ------------------------------------------------------------ end to end
+    e2e = None
+    try:
+        e2e = measure_e2e(wk, K, w12_bytes)
+    except Exception as ex:  # reported, never hidden
+        e2e = {"value": None, "unit": "GB/s", "error": str(ex)[:200]}
+
+    # ------------------------------------------------------- cuBLAS context
+    cublas = None
+    if not args.no_cublas and rank == 0:
+        try:
+            cublas = cublas_reference_us(wk, K)
+        except Exception as ex:
+            cublas = {"error": str(ex)[:200]}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wk)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {DESCRIPTIONS.get(args.workload, '')}", "rows": wk.R,
+                       "requests": wk.wl.n_req, "w12_bytes_per_step": w12_bytes,
+                       "l2": "inputs larger than L2 (W12 bytes per step vs 129 MB L2); no flush",
+                       "timing": "CUDA-graph replays of the whole step, CUDA events" if graph else "eager launches",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "step_us": round(1e3 * ms, 2),
+            "pct_of_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+            "pct_of_measured_hbm": round(100 * value / world / peak, 2),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": "k_w12_gemm",
+                         "peak_kind": peak_kind,
+                         "note": "all W12 GEMM launches of a step (linears + LM head), serialised, "
+                                 "algorithmic bytes (W12 + activations + outputs) / summed launch time"},
+            "kernels": kernels,
+            "e2e": e2e,
+            "cublas_bf16": cublas,
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "gpu_launches": K * wk.gpu_launches_per_step(),
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_e2e(wk: Workload, K: int, w12_bytes: int):
+    """Through the public API with host buffers: per step, copy the lattice,
+    activations and hidden rows in from pinned host memory, run the pass, read
+    the accepted tokens and lengths back."""
+    import torch
+    w12 = wk.w12
+    pin = lambda t: t.cpu().pin_memory()
+    host_in = [(pin(wk.dlat.root_tok), wk.dlat.root_tok), (pin(wk.dlat.cand_tok), wk.dlat.cand_tok),
+               (pin(wk.dlat.cand_logp), wk.dlat.cand_logp), (pin(wk.h), wk.h)]
+    seen = set()
+    for x in wk.xs:
+        if x.data_ptr() not in seen:
+            seen.add(x.data_ptr())
+            host_in.append((pin(x), x))
+    out_tok = torch.empty_like(wk.acc_tok, device="cpu").pin_memory()
+    out_len = torch.empty_like(wk.acc_len, device="cpu").pin_memory()
+    h2d = sum(h.numel() * h.element_size() for h, _ in host_in)
+    d2h = out_tok.numel() * 4 + out_len.numel() * 4
+
+    def one():
+        for h, d in host_in:
+            d.copy_(h, non_blocking=True)
+        wk.step()
+        out_tok.copy_(wk.acc_tok, non_blocking=True)
+        out_len.copy_(wk.acc_len, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    return {"value": round(w12_bytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "ms_per_step": round(ms, 5),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def cublas_reference_us(wk: Workload, K: int):
+    """torch.matmul (cuBLAS) BF16 with dense weights of the same shapes, for
+    context: the same rows through the same linears and the head (logits
+    only, no argmax)."""
+    import torch
+    shapes = [(d.n, d.k) for d in wk.lin[:len(wk.wl.linears)]] + [(wk.head.n, wk.head.k)]
+    ws = [torch.randn((n, k), dtype=torch.bfloat16, device=wk.device) * 0.02 for n, k in shapes]
+    xs = [torch.randn((wk.R, k), dtype=torch.bfloat16, device=wk.device) for _, k in shapes]
+    for _ in range(3):
+        for x, w in zip(xs, ws):
+            torch.matmul(x, w.t())
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        for x, w in zip(xs, ws):
+            torch.matmul(x, w.t())
+    e1.record()
+    torch.cuda.synchronize()
+    us = 1e3 * e0.elapsed_time(e1) / K
+    dense = sum(2 * n * k for n, k in shapes)
+    del ws, xs
+    torch.cuda.empty_cache()
+    return {"us_per_step": round(us, 2), "bf16_bytes": dense, "gbs": round(dense / (us * 1e-6) / 1e9, 1),
+            "layers_per_step": wk.wl.layers}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -69,11 +69,18 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
 def weights(n: int, k: int, seed: int, stream: int, outlier_frac: float = 0.0,
             zero_frac: float = 0.0, chunk_rows: int = 4096) -> np.ndarray:
     """BF16 bits ``[n][k]``: N(0, 0.02) * U[0.5, 2] per row, plus optional
-    x64 outliers and exact zeros (each a fraction of all entries)."""
-    g = rng(seed, stream)
+    x64 outliers and exact zeros (each a fraction of all entries).
+
+    Rows are drawn in chunks of ``chunk_rows``, chunk i from the child stream
+    SeedSequence([seed, stream, i]); chunks are filled on a thread pool."""
+    import concurrent.futures as cf
+    import os
+
     out = np.empty((n, k), dtype=np.uint16)
-    for r0 in range(0, n, chunk_rows):
-        r1 = min(n, r0 + chunk_rows)
+
+    def fill(i):
+        r0, r1 = i * chunk_rows, min(n, (i + 1) * chunk_rows)
+        g = np.random.default_rng(np.random.SeedSequence([int(seed), int(stream), i]))
         w = g.standard_normal((r1 - r0, k), dtype=np.float32)
         w *= np.float32(0.02)
         w *= g.uniform(0.5, 2.0, size=(r1 - r0, 1)).astype(np.float32)
@@ -84,6 +91,13 @@ def weights(n: int, k: int, seed: int, stream: int, outlier_frac: float = 0.0,
             m = g.random((r1 - r0, k)) < zero_frac
             w[m] = 0.0
         out[r0:r1] = f32_to_bf16_bits(w)
+
+    chunks = (n + chunk_rows - 1) // chunk_rows
+    if chunks == 1:
+        fill(0)
+    else:
+        with cf.ThreadPoolExecutor(max_workers=min(chunks, os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, range(chunks)))
     return out
 
 
