@@ -23,7 +23,8 @@
  *     a typed status and launches nothing.
  *   - Device pointers are caller-owned (e.g. torch tensors).  The library
  *     allocates no device memory and keeps no global state except cached
- *     device properties and its driver entry point.
+ *     device properties, its driver entry point and the fixed scratch array
+ *     of w12_gemm_static_scratch.
  *   - Device work is asynchronous on the caller's stream unless stated.
  *     Launch failures map to W12_E_CUDA.
  *   - Conditions found on the device (a timed-out wait, bad lattice values)
@@ -172,6 +173,32 @@ w12_status w12_load_check(const w12_weight *w, const uint16_t *src_bf16, int64_t
  */
 w12_status w12_gemm(const w12_weight *w, const uint16_t *x, int32_t R, uint16_t *y, void *ws,
                     size_t ws_bytes, w12_stream_t stream);
+
+/*
+ * w12_gemm without a workspace, for callers that cannot allocate device
+ * memory where they call it: code running inside a CUDA stream capture
+ * (where cudaMalloc may be refused), plugin hosts that give kernels no
+ * device allocations, and processes that must keep a fixed footprint.  The
+ * paper has no counterpart to this entry point; it computes exactly what
+ * w12_gemm computes, with the same kernel.
+ *   - Scratch (split-tile partial sums, tile arrival counters, a status word)
+ *     is a file-scope device array of about 4.1 MiB that every GPU loading
+ *     the library holds until the process exits.  The call allocates and
+ *     frees nothing.
+ *   - Limits: 1 <= R <= 16 rows and n <= 16384 * 128 output channels; larger
+ *     sizes return W12_E_UNSUPPORTED before anything runs.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call on a device shares the array and leaves its contents
+ *     behind; each call zeroes the counters and status word it uses.  Calls
+ *     whose kernels overlap on the GPU (different streams, no ordering)
+ *     race on the array: order them on one stream.
+ *   - Device-detected conditions (a timed-out wait) are recorded only in the
+ *     array's status word, which this entry point does not report.
+ * Arguments, layout and errors otherwise as w12_gemm.
+ */
+w12_status w12_gemm_static_scratch(const w12_weight *w, const uint16_t *x, int32_t R, uint16_t *y,
+                                   w12_stream_t stream);
 
 /*
  * LM head + argmax: logits = h[R][k] . W_head^T in FP32 (never stored), then

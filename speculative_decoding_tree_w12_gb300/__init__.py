@@ -86,6 +86,7 @@ def lib():
             "w12_unpack": ([p, p, p], C.c_int),
             "w12_load_check": ([p, p, p, p, sz, p], C.c_int),
             "w12_gemm": ([p, p, i32, p, p, sz, p], C.c_int),
+            "w12_gemm_static_scratch": ([p, p, i32, p, p], C.c_int),
             "w12_lmhead_argmax": ([p, p, i32, p, p, p, sz, p], C.c_int),
             "w12_tree_build": ([p, i32, p, p, sz, p], C.c_int),
             "w12_tree_accept": ([p, i32, i32, p, p, p, p, p], C.c_int),

@@ -21,6 +21,7 @@
 
 #include <algorithm>
 #include <cstdio>
+#include <mutex>
 
 #include "w12_device.cuh"
 
@@ -572,6 +573,78 @@ int launch_gemm(const GemmArgs &a, void *stream)
     case 4: return launch_t<4, 2>(a, xmap, st);
     default: return launch_t<8, 2>(a, xmap, st);
     }
+}
+
+// ---------------------------------------------------------------------------
+// Scratch of the allocation-free GEMM entry point (w12_gemm_static_scratch).
+//
+// Some callers cannot allocate device memory at the point where they run the
+// GEMM (code inside a CUDA stream capture, hosts that hand out no device
+// allocations to plugins, processes that must keep a fixed footprint).  For
+// them the split-tile partial sums, the tile arrival counters and a status
+// word live in this file-scope array instead of a caller workspace.  Every
+// GPU that loads the library keeps it (about 4.1 MiB) until the process exits.
+// Limits: R <= kStaticMaxRows rows, at most kStaticMaxTiles output tiles of
+// 128 channels, at most kStaticMaxCtas CTAs.
+// ---------------------------------------------------------------------------
+constexpr int kStaticMaxRows = 16;
+constexpr int kStaticMaxCtas = 256;
+constexpr int kStaticMaxTiles = 16384;
+constexpr size_t kStaticStatusBytes = 256;
+constexpr size_t kStaticCounterBytes = (size_t)kStaticMaxTiles * 4;
+constexpr size_t kStaticPartialBytes = (size_t)kStaticMaxCtas * 2 * kStaticMaxRows * kTileN * 4;
+constexpr size_t kStaticScratchBytes = kStaticStatusBytes + kStaticCounterBytes + kStaticPartialBytes;
+
+}  // namespace w12i
+
+static __device__ __align__(256) unsigned char g_static_scratch[w12i::kStaticScratchBytes];
+
+namespace w12i {
+
+// Device address of g_static_scratch on the current device, looked up once per
+// device (with that device current) and cached.  A host-side name of a
+// __device__ array is not a device address, so it is never passed directly.
+static int static_scratch_on_current_device(unsigned char **out)
+{
+    static std::mutex mu;
+    static unsigned char *cache[128] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return (int)e;
+    if (dev < 0 || dev >= 128) return (int)cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return (int)e;
+        cache[dev] = static_cast<unsigned char *>(p);
+    }
+    *out = cache[dev];
+    return 0;
+}
+
+int static_scratch_limits(int32_t *max_rows, int32_t *max_tiles)
+{
+    *max_rows = kStaticMaxRows;
+    *max_tiles = kStaticMaxTiles;
+    return 0;
+}
+
+int launch_gemm_static_scratch(const GemmArgs &in, void *stream)
+{
+    if (in.R < 1 || in.R > kStaticMaxRows || in.w.n_tiles > kStaticMaxTiles || in.num_sms > kStaticMaxCtas)
+        return (int)cudaErrorInvalidValue;
+    unsigned char *base = nullptr;
+    if (int e = static_scratch_on_current_device(&base)) return e;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    GemmArgs a = in;
+    a.status = reinterpret_cast<int32_t *>(base);
+    a.counters = reinterpret_cast<int32_t *>(base + kStaticStatusBytes);
+    a.partial = reinterpret_cast<float *>(base + kStaticStatusBytes + kStaticCounterBytes);
+    // the status word and the arrival counters of this call start at zero
+    cudaError_t e = cudaMemsetAsync(base, 0, kStaticStatusBytes + (size_t)a.w.n_tiles * 4, st);
+    if (e != cudaSuccess) return (int)e;
+    return launch_gemm(a, stream);
 }
 
 int launch_argmax_stage2(const float *s1_val, const int32_t *s1_idx, int32_t R, int32_t n_tiles, int32_t *argmax,

@@ -295,6 +295,29 @@ w12_status w12_gemm(const w12_weight *w, const uint16_t *x, int32_t R, uint16_t 
     return cuda_status(gemm_slices(dev_weight(w), x, R, kModeLinear, y, W, slot, false, st));
 }
 
+w12_status w12_gemm_static_scratch(const w12_weight *w, const uint16_t *x, int32_t R, uint16_t *y,
+                                   w12_stream_t stream)
+{
+    w12_status s = weight_ok(w);
+    if (s != W12_OK) return s;
+    if (!x || !y || !aligned(x, 16) || !aligned(y, 16)) return W12_E_INVAL;
+    if (R < 1) return W12_E_INVAL;
+    int32_t max_rows = 0, max_tiles = 0;
+    static_scratch_limits(&max_rows, &max_tiles);
+    if (R > max_rows || w->n / kTileN > max_tiles) return W12_E_UNSUPPORTED;
+    GemmArgs a{};
+    a.w = dev_weight(w);
+    a.x = x;
+    a.R = R;
+    a.mode = kModeLinear;
+    a.y = y;
+    a.num_sms = num_sms();
+    a.pdl = false;
+    a.debug_flags = 0;
+    a.timeout_ns = g_timeout_ns;
+    return cuda_status(launch_gemm_static_scratch(a, stream));
+}
+
 w12_status w12_lmhead_argmax(const w12_weight *head, const uint16_t *h, int32_t R, int32_t *argmax, float *maxlogit,
                              void *ws, size_t ws_bytes, w12_stream_t stream)
 {

@@ -72,6 +72,9 @@ struct GemmArgs {
 };
 
 int launch_gemm(const GemmArgs &a, void *stream);
+// same kernel, scratch in a file-scope device array (no workspace argument)
+int launch_gemm_static_scratch(const GemmArgs &a, void *stream);
+int static_scratch_limits(int32_t *max_rows, int32_t *max_tiles);
 int launch_argmax_stage2(const float *s1_val, const int32_t *s1_idx, int32_t R, int32_t n_tiles, int32_t *argmax,
                          float *maxlogit, bool pdl, void *stream);
 
