@@ -39,6 +39,12 @@ void w12_debug_set(int32_t flags, uint64_t timeout_ns);
 void w12_debug_profile(int32_t enable);
 int32_t w12_debug_profile_read(float *ms, int32_t max);
 
+/*
+ * The CUDA error behind the most recent W12_E_CUDA returned by this library
+ * (0 if none): its code, and its name copied into buf (len bytes, may be NULL).
+ */
+int32_t w12_debug_last_cuda_error(char *buf, int32_t len);
+
 /* Number of SMs the kernels size their persistent grids for (current device). */
 int32_t w12_debug_num_sms(void);
 

@@ -30,7 +30,12 @@ TILE_N, TILE_K, REC_BYTES = 128, 64, 12288
 class W12Error(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what}: {status_str(status)} ({status})")
+        detail = ""
+        if status == W12_E_CUDA:
+            buf = C.create_string_buffer(96)
+            code = lib().w12_debug_last_cuda_error(buf, 96)
+            detail = f" [{buf.value.decode()} = {code}]"
+        super().__init__(f"{what}: {status_str(status)} ({status}){detail}")
 
 
 # ---------------------------------------------------------------------------
@@ -94,6 +99,7 @@ def lib():
             "w12_debug_set": ([i32, C.c_uint64], None),
             "w12_debug_num_sms": ([], i32),
             "w12_debug_profile": ([i32], None),
+            "w12_debug_last_cuda_error": ([p, i32], i32),
             "w12_debug_profile_read": ([p, i32], i32),
         }
         for name, (args, res) in sigs.items():

@@ -162,15 +162,18 @@ __global__ void __launch_bounds__(Cfg<NB8, WK>::kThreads, 1)
                     tma_load_2d(x_s + i * C::kXBytes, &xmap, (int)((rec_begin + i) % KT) * w12i::kTileK, 0,
                                 bar_full + 8 * i);
             int issued = pre;
+            int s = pre % S;
+            uint32_t use = pre / S;                 // how many times stage s has been filled
+            int kt = (int)((rec_begin + pre) % KT);
             for (int i = pre; i < nrec; ++i) {
-                const int s = i % S, u = i / S;
-                if (!mbar_wait(bar_empty + 8 * s, (u - 1) & 1, p.timeout_ns, p.status, abort_flag)) break;
+                if (!mbar_wait(bar_empty + 8 * s, (use - 1) & 1, p.timeout_ns, p.status, abort_flag)) break;
                 mbar_expect_tx(bar_full + 8 * s, stage_bytes);
                 bulk_g2s(rec_s + s * w12i::kRecBytes, p.rec + (rec_begin + i) * (int64_t)w12i::kRecBytes,
                          w12i::kRecBytes, bar_full + 8 * s, pol);
-                tma_load_2d(x_s + s * C::kXBytes, &xmap, (int)((rec_begin + i) % KT) * w12i::kTileK, 0,
-                            bar_full + 8 * s);
+                tma_load_2d(x_s + s * C::kXBytes, &xmap, kt * w12i::kTileK, 0, bar_full + 8 * s);
                 issued = i + 1;
+                if (++s == S) s = 0, ++use;
+                if (++kt == KT) kt = 0;
             }
             if (*abort_flag) {
                 // leave no copy in flight: wait (bounded, ignoring the abort
@@ -355,34 +358,53 @@ __global__ void __launch_bounds__(Cfg<NB8, WK>::kThreads, 1)
     };
 
     uint32_t a[2][C::kKgPerWarp][4];
+    int64_t nt = nt_first;
+    int kt = (int)(rec_begin - nt_first * KT);
+    int s = 0;
+    uint32_t full_phase = 0;
+    // Per-thread parts of every shared-memory address, hoisted out of the
+    // record loop; what varies inside it is a compile-time offset.
+    //   view word (kg, mb, hi): thread base + kg*2048 + mb*256 + hi*128
+    //   nibble word:            thread base + 8192 + (kg/2)*2048 + mb*256 + hi*128
+    const uint8_t *rec_thread = smem + sp.rec_off + (mw * 32 + g) * 16 + 4 * t;
+    uint32_t x_thread[C::kKgPerWarp];
+#pragma unroll
+    for (int kgl = 0; kgl < C::kKgPerWarp; ++kgl) {
+        const int kg = wk * C::kKgPerWarp + kgl;
+        if constexpr (NB8 == 1) {
+            const int chunk = 2 * kg + ((lane >> 3) & 1);
+            x_thread[kgl] = (lane & 7) * 128 + ((chunk ^ (lane & 7)) << 4);
+        } else {
+            const int q = lane >> 3, chunk = 2 * kg + (q & 1);
+            x_thread[kgl] = ((q >> 1) * 8 + (lane & 7)) * 128 + ((chunk ^ (lane & 7)) << 4);
+        }
+    }
     for (int i = 0; i < nrec; ++i) {
-        const int64_t r = rec_begin + i;
-        const int64_t nt = r / KT;
         if (nt != cur_nt) {
             if (cur_nt >= 0 && !flush(cur_nt)) return;
             cur_nt = nt;
             load_consts(nt);
         }
-        const int s = i % S;
-        if (!mbar_wait(bar_full + 8 * s, (i / S) & 1, p.timeout_ns, p.status, abort_flag)) return;
-        const uint32_t rb = rec_s + s * w12i::kRecBytes;
+        if (!mbar_try_wait(bar_full + 8 * s, full_phase) &&
+            !mbar_wait(bar_full + 8 * s, full_phase, p.timeout_ns, p.status, abort_flag))
+            return;
+        const uint32_t *rw = reinterpret_cast<const uint32_t *>(rec_thread + s * w12i::kRecBytes);
         const uint32_t xb = x_s + s * C::kXBytes;
 
         // decode this warp's 32 channels x (16 * kKgPerWarp) K of the record
 #pragma unroll
         for (int mb = 0; mb < 2; ++mb) {
-            const int ch_lo = mw * 32 + mb * 16 + g;
             uint32_t nib_lo = 0, nib_hi = 0;
 #pragma unroll
             for (int kgl = 0; kgl < C::kKgPerWarp; ++kgl) {
                 const int kg = wk * C::kKgPerWarp + kgl;
                 if (kgl == 0 || (kg & 1) == 0) {
-                    nib_lo = lds32(rb + w12i::kViewBytes + (((kg >> 1) * w12i::kTileN + ch_lo) * 16 + 4 * t));
-                    nib_hi = lds32(rb + w12i::kViewBytes + (((kg >> 1) * w12i::kTileN + ch_lo + 8) * 16 + 4 * t));
+                    nib_lo = rw[(w12i::kViewBytes + (kg >> 1) * 2048 + mb * 256) / 4];
+                    nib_hi = rw[(w12i::kViewBytes + (kg >> 1) * 2048 + mb * 256 + 128) / 4];
                 }
                 const uint32_t sh = (kg & 1) * 4;
-                const uint32_t v_lo = lds32(rb + ((kg * w12i::kTileN + ch_lo) * 16 + 4 * t));
-                const uint32_t v_hi = lds32(rb + ((kg * w12i::kTileN + ch_lo + 8) * 16 + 4 * t));
+                const uint32_t v_lo = rw[(kg * 2048 + mb * 256) / 4];
+                const uint32_t v_hi = rw[(kg * 2048 + mb * 256 + 128) / 4];
                 decode_word(v_lo, nib_lo >> sh, cc[mb][0], p.mul16, a[mb][kgl][0], a[mb][kgl][2]);
                 decode_word(v_hi, nib_hi >> sh, cc[mb][1], p.mul16, a[mb][kgl][1], a[mb][kgl][3]);
             }
@@ -415,30 +437,30 @@ __global__ void __launch_bounds__(Cfg<NB8, WK>::kThreads, 1)
         // activations (B operand) from the swizzled TMA block, then MMA
 #pragma unroll
         for (int kgl = 0; kgl < C::kKgPerWarp; ++kgl) {
-            const int kg = wk * C::kKgPerWarp + kgl;
+            const uint32_t xa = xb + x_thread[kgl];
             if constexpr (NB8 == 1) {
-                const int row = lane & 7, chunk = 2 * kg + ((lane >> 3) & 1);
                 uint32_t b0, b1;
-                ldsm_x2(xb + row * 128 + ((chunk ^ (row & 7)) << 4), b0, b1);
+                ldsm_x2(xa, b0, b1);
 #pragma unroll
                 for (int mb = 0; mb < 2; ++mb) mma_bf16_16816(acc[mb][0], a[mb][kgl], b0, b1);
             } else {
-#pragma unroll
-                for (int nb = 0; nb < NB8; nb += 2) {
-                    const int q = lane >> 3;
-                    const int row = (nb + (q >> 1)) * 8 + (lane & 7), chunk = 2 * kg + (q & 1);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(xb + row * 128 + ((chunk ^ (row & 7)) << 4), b0, b1, b2, b3);
-#pragma unroll
-                    for (int mb = 0; mb < 2; ++mb) {
-                        mma_bf16_16816(acc[mb][nb], a[mb][kgl], b0, b1);
-                        mma_bf16_16816(acc[mb][nb + 1], a[mb][kgl], b2, b3);
-                    }
+                uint32_t b[NB8][2];
+                ldsm_x4_off<0>(xa, b[0][0], b[0][1], b[1][0], b[1][1]);
+                if constexpr (NB8 >= 4) ldsm_x4_off<2048>(xa, b[2][0], b[2][1], b[3][0], b[3][1]);
+                if constexpr (NB8 >= 8) {
+                    ldsm_x4_off<4096>(xa, b[4][0], b[4][1], b[5][0], b[5][1]);
+                    ldsm_x4_off<6144>(xa, b[6][0], b[6][1], b[7][0], b[7][1]);
                 }
+#pragma unroll
+                for (int nb = 0; nb < NB8; ++nb)
+#pragma unroll
+                    for (int mb = 0; mb < 2; ++mb) mma_bf16_16816(acc[mb][nb], a[mb][kgl], b[nb][0], b[nb][1]);
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+        if (++s == S) s = 0, full_phase ^= 1u;
+        if (++kt == KT) kt = 0, ++nt;
     }
     if (cur_nt >= 0) flush(cur_nt);
 }
@@ -534,6 +556,10 @@ int launch_t(const w12i::GemmArgs &a, const CUtensorMap &xmap, cudaStream_t st)
     if (smem > budget) return (int)cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(k_w12_gemm<NB8, WK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return (int)e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, k_w12_gemm<NB8, WK>);
+    if (e != cudaSuccess) return (int)e;
+    if (fa.maxThreadsPerBlock < C::kThreads) return (int)cudaErrorLaunchOutOfResources;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(G);
     cfg.blockDim = dim3(C::kThreads);
@@ -567,10 +593,11 @@ int launch_gemm(const GemmArgs &a, void *stream)
                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return (int)cudaErrorInvalidValue;
+    // up to 32 rows: 16 consumer warps, one 16-K group each; 64 rows: 8 warps
     switch (nb8) {
-    case 1: return launch_t<1, 2>(a, xmap, st);
-    case 2: return launch_t<2, 2>(a, xmap, st);
-    case 4: return launch_t<4, 2>(a, xmap, st);
+    case 1: return launch_t<1, 4>(a, xmap, st);
+    case 2: return launch_t<2, 4>(a, xmap, st);
+    case 4: return launch_t<4, 4>(a, xmap, st);
     default: return launch_t<8, 2>(a, xmap, st);
     }
 }

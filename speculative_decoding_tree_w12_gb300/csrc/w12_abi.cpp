@@ -83,7 +83,14 @@ DevWeight dev_weight(const w12_weight *w)
     return d;
 }
 
-w12_status cuda_status(int e) { return e == 0 ? W12_OK : W12_E_CUDA; }
+int g_last_cuda_error = 0;
+
+w12_status cuda_status(int e)
+{
+    if (e == 0) return W12_OK;
+    g_last_cuda_error = e;
+    return W12_E_CUDA;
+}
 
 struct Ws {
     uint8_t *base;
@@ -212,6 +219,16 @@ void w12_debug_set(int32_t flags, uint64_t timeout_ns)
 
 int32_t w12_debug_num_sms(void) { return num_sms(); }
 
+int32_t w12_debug_last_cuda_error(char *buf, int32_t len)
+{
+    if (buf && len > 0) {
+        const char *name = g_last_cuda_error ? cudaGetErrorName(static_cast<cudaError_t>(g_last_cuda_error)) : "";
+        std::strncpy(buf, name, static_cast<size_t>(len - 1));
+        buf[len - 1] = 0;
+    }
+    return g_last_cuda_error;
+}
+
 void w12_debug_profile(int32_t enable)
 {
     g_profile = enable != 0;
@@ -290,7 +307,7 @@ w12_status w12_gemm(const w12_weight *w, const uint16_t *x, int32_t R, uint16_t 
     if ((s = ws_check(ws, ws_bytes, L)) != W12_OK) return s;
     Ws W{static_cast<uint8_t *>(ws), L};
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (W.clear_counters(st)) return W12_E_CUDA;
+    if (int ce = W.clear_counters(st)) return cuda_status(ce);
     int slot = 0;
     return cuda_status(gemm_slices(dev_weight(w), x, R, kModeLinear, y, W, slot, false, st));
 }
@@ -330,7 +347,7 @@ w12_status w12_lmhead_argmax(const w12_weight *head, const uint16_t *h, int32_t 
     if ((s = ws_check(ws, ws_bytes, L)) != W12_OK) return s;
     Ws W{static_cast<uint8_t *>(ws), L};
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (W.clear_counters(st)) return W12_E_CUDA;
+    if (int ce = W.clear_counters(st)) return cuda_status(ce);
     int slot = 0;
     const DevWeight dw = dev_weight(head);
     if (int e = gemm_slices(dw, h, R, kModeHead, nullptr, W, slot, false, st)) return cuda_status(e);
@@ -423,7 +440,7 @@ w12_status w12_verify_step(const w12_step *step, const w12_tree *tree, int32_t n
     if ((s = ws_check(ws, ws_bytes, L)) != W12_OK) return s;
     Ws W{static_cast<uint8_t *>(ws), L};
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (W.clear_counters(st)) return W12_E_CUDA;
+    if (int ce = W.clear_counters(st)) return cuda_status(ce);
     g_prof_used = 0;
     if (prof_mark(st)) return W12_E_CUDA;
     int slot = 0;
