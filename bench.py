@@ -204,24 +204,24 @@ class Workload:
     def w12_bytes(self):
         return sum(d.nbytes for d in self.lin) + self.head.nbytes
 
-    def launch_bytes(self):
+    def launch_bytes(self, launches_per_weight):
         """Algorithmic bytes of each GEMM launch of a step, in launch order:
-        W12 record/base/escape bytes + activations in + outputs out."""
+        W12 record/base/escape bytes + activations in + outputs out (a weight
+        split into row slices is streamed once per slice)."""
         R = self.R
         out = []
-        slices = (R + 63) // 64
+        slices = launches_per_weight
         for d in self.lin:
             for s in range(slices):
-                r = min(64, R - 64 * s)
+                r = R if slices == 1 else min(64, R - 64 * s)
                 out.append(d.nbytes + r * d.k * 2 + r * d.n * 2)
         for s in range(slices):
-            r = min(64, R - 64 * s)
+            r = R if slices == 1 else min(64, R - 64 * s)
             out.append(self.head.nbytes + r * self.head.k * 2 + r * (self.head.n // 128) * 8)
         return out
 
-    def gpu_launches_per_step(self):
-        slices = (self.R + 63) // 64
-        return 1 + slices * (len(self.lin) + 1) + 2
+    def gpu_launches_per_step(self, launches_per_weight):
+        return 1 + launches_per_weight * (len(self.lin) + 1) + 2
 
     # the step ------------------------------------------------------------
     def step(self):
@@ -357,6 +357,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cublas", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--gemm", default="auto", choices=["auto", "tcgen05", "warp_mma"],
+                    help="GEMM kernel: the library's choice by row count, or one forced")
     args = ap.parse_args()
     if args.warmup < 3:
         log("[bench] warmup raised to 3")
@@ -382,6 +384,7 @@ def main():
     if dist:
         dist.barrier()
     import speculative_decoding_tree_w12_gb300 as w12
+    w12.debug_set({"auto": 0, "tcgen05": 2, "warp_mma": 4}[args.gemm], 0)
 
     wk = Workload(args.workload, args.rows, device)
     W, K = args.warmup, args.steps
@@ -455,8 +458,9 @@ def main():
         per_launch = lt if per_launch is None else per_launch + lt
     w12.profile(False)
     per_launch = per_launch / K
-    lb = wk.launch_bytes()
-    n_gemm = len(lb)
+    n_gemm = len(per_launch) - 2                     # then the argmax reduction and acceptance
+    per_weight = n_gemm // (len(wk.lin) + 1)
+    lb = wk.launch_bytes(per_weight)
     gemm_ms = per_launch[:n_gemm]
     gemm_bytes = float(sum(lb))
     achieved = gemm_bytes / (float(gemm_ms.sum()) * 1e-3) / 1e9
@@ -498,7 +502,7 @@ def main():
                        "requests": wk.wl.n_req, "w12_bytes_per_step": w12_bytes,
                        "l2": "inputs larger than L2 (W12 bytes per step vs 129 MB L2); no flush",
                        "timing": "CUDA-graph replays of the whole step, CUDA events" if graph else "eager launches",
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
+                       "parallelism": "replicas" if world > 1 else "single GPU", "gemm_kernel": args.gemm},
             "step_us": round(1e3 * ms, 2),
             "pct_of_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
             "pct_of_measured_hbm": round(100 * value / world / peak, 2),
@@ -512,7 +516,7 @@ def main():
             "cublas_bf16": cublas,
             "cpu_baseline": cpu,
             "clocks": clocks,
-            "gpu_launches": K * wk.gpu_launches_per_step(),
+            "gpu_launches": K * wk.gpu_launches_per_step(per_weight),
         }
         print(json.dumps(line), flush=True)
     if dist:

@@ -20,6 +20,9 @@ extern "C" {
  *                first record but never copies it, so that CTA's consumers
  *                time out; the kernel records W12_E_TIMEOUT in the workspace
  *                status word and every CTA returns with no copy in flight.
+ *   flags bit 1: run every GEMM on the tensor-memory (tcgen05) kernel.
+ *   flags bit 2: run every GEMM on the warp-MMA kernel (64 rows per pass).
+ *                Without either bit the library picks by row count.
  *   timeout_ns:  limit of every bounded wait inside the kernels
  *                (0 restores the default of 2 seconds).
  * Not thread-safe; meant to be set between launches by a test.

@@ -53,8 +53,9 @@ struct KParams {
     int32_t base_tiles;     // n-tiles whose window bases fit the shared cache
 };
 
-template <int NB8, int WK>
+template <int NB8, int WK, int RPS>
 struct Cfg {
+    static constexpr int kRecsPerStage = RPS;                  // records per shared-memory stage
     static constexpr int kRows = NB8 * 8;                     // rows per activation block
     static constexpr int kXBytes = kRows * 128;               // activation block: rows x 64 BF16
     static constexpr int kConsumerWarps = kWarpsN * WK;
@@ -69,16 +70,16 @@ struct SmemPlan {
     int rec_off, x_off, red_off, bar_off, flag_off, escoff_off, esc_off, base_off, total;
 };
 
-template <int NB8, int WK>
+template <int NB8, int WK, int RPS>
 __host__ __device__ inline SmemPlan smem_plan(int stages, int max_recs, int esc_cap, int base_tiles)
 {
-    using C = Cfg<NB8, WK>;
+    using C = Cfg<NB8, WK, RPS>;
     SmemPlan s;
     int o = 0;
     s.rec_off = o;
-    o += stages * w12i::kRecBytes;
+    o += stages * RPS * w12i::kRecBytes;
     s.x_off = o;
-    o += stages * C::kXBytes;
+    o += stages * RPS * C::kXBytes;
     s.red_off = o;
     o += C::kRedBytes;
     s.bar_off = o;
@@ -98,15 +99,15 @@ __host__ __device__ inline SmemPlan smem_plan(int stages, int max_recs, int esc_
 __device__ __forceinline__ int cta_of_record(int64_t r, int G, int64_t T) { return (int)(((r + 1) * G - 1) / T); }
 __device__ __forceinline__ int64_t first_record(int c, int G, int64_t T) { return (int64_t)c * T / G; }
 
-template <int NB8, int WK>
-__global__ void __launch_bounds__(Cfg<NB8, WK>::kThreads, 1)
+template <int NB8, int WK, int RPS>
+__global__ void __launch_bounds__(Cfg<NB8, WK, RPS>::kThreads, 1)
     k_w12_gemm(const __grid_constant__ CUtensorMap xmap, const KParams p)
 {
-    using C = Cfg<NB8, WK>;
+    using C = Cfg<NB8, WK, RPS>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // the 128-byte swizzle of the activation blocks needs 1024-byte alignment
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const SmemPlan sp = smem_plan<NB8, WK>(p.stages, p.max_recs, p.esc_cap, p.base_tiles);
+    const SmemPlan sp = smem_plan<NB8, WK, RPS>(p.stages, p.max_recs, p.esc_cap, p.base_tiles);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, cta = blockIdx.x;
@@ -133,7 +134,7 @@ __global__ void __launch_bounds__(Cfg<NB8, WK>::kThreads, 1)
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, C::kConsumerWarps);
         }
-        mbar_init(bar_cons, C::kConsumers);
+        mbar_init(bar_cons, C::kConsumerWarps);   // one arrival per consumer warp
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -145,43 +146,45 @@ __global__ void __launch_bounds__(Cfg<NB8, WK>::kThreads, 1)
         if (lane == 0) {
             prefetch_tmap(&xmap);
             const uint64_t pol = policy_evict_first();
-            const uint32_t stage_bytes = w12i::kRecBytes + C::kXBytes;
             const bool drop_first = (p.debug_flags & 1) && cta == 0;
-            const int pre = min(S, nrec);
+            const int nst = (nrec + RPS - 1) / RPS;
+            auto recs_in = [&](int j) { return min(RPS, nrec - j * RPS); };
+            auto issue_w = [&](int j, int sl) {
+                const int n = recs_in(j);
+                mbar_expect_tx(bar_full + 8 * sl, (uint32_t)n * (w12i::kRecBytes + C::kXBytes));
+                if (!(drop_first && j == 0))
+                    bulk_g2s(rec_s + sl * RPS * w12i::kRecBytes, p.rec + (rec_begin + j * RPS) * (int64_t)w12i::kRecBytes,
+                             (uint32_t)n * w12i::kRecBytes, bar_full + 8 * sl, pol);
+            };
+            auto issue_x = [&](int j, int sl) {
+                if (drop_first && j == 0) return;
+                for (int r = 0; r < recs_in(j); ++r)
+                    tma_load_2d(x_s + (sl * RPS + r) * C::kXBytes, &xmap,
+                                (int)((rec_begin + j * RPS + r) % KT) * w12i::kTileK, 0, bar_full + 8 * sl);
+            };
+            const int pre = min(S, nst);
             // weights do not depend on earlier kernels: start them before the
             // programmatic-dependency wait
-            for (int i = 0; i < pre; ++i) {
-                mbar_expect_tx(bar_full + 8 * i, stage_bytes);
-                if (!(drop_first && i == 0))
-                    bulk_g2s(rec_s + i * w12i::kRecBytes, p.rec + (rec_begin + i) * (int64_t)w12i::kRecBytes,
-                             w12i::kRecBytes, bar_full + 8 * i, pol);
-            }
+            for (int j = 0; j < pre; ++j) issue_w(j, j);
             pdl_wait();
-            for (int i = 0; i < pre; ++i)
-                if (!(drop_first && i == 0))
-                    tma_load_2d(x_s + i * C::kXBytes, &xmap, (int)((rec_begin + i) % KT) * w12i::kTileK, 0,
-                                bar_full + 8 * i);
+            for (int j = 0; j < pre; ++j) issue_x(j, j);
             int issued = pre;
-            int s = pre % S;
-            uint32_t use = pre / S;                 // how many times stage s has been filled
-            int kt = (int)((rec_begin + pre) % KT);
-            for (int i = pre; i < nrec; ++i) {
-                if (!mbar_wait(bar_empty + 8 * s, (use - 1) & 1, p.timeout_ns, p.status, abort_flag)) break;
-                mbar_expect_tx(bar_full + 8 * s, stage_bytes);
-                bulk_g2s(rec_s + s * w12i::kRecBytes, p.rec + (rec_begin + i) * (int64_t)w12i::kRecBytes,
-                         w12i::kRecBytes, bar_full + 8 * s, pol);
-                tma_load_2d(x_s + s * C::kXBytes, &xmap, kt * w12i::kTileK, 0, bar_full + 8 * s);
-                issued = i + 1;
-                if (++s == S) s = 0, ++use;
-                if (++kt == KT) kt = 0;
+            int sl = pre % S;
+            uint32_t use = pre / S;                 // how many times stage sl has been filled
+            for (int j = pre; j < nst; ++j) {
+                if (!mbar_wait(bar_empty + 8 * sl, (use - 1) & 1, p.timeout_ns, p.status, abort_flag)) break;
+                issue_w(j, sl);
+                issue_x(j, sl);
+                issued = j + 1;
+                if (++sl == S) sl = 0, ++use;
             }
             if (*abort_flag) {
                 // leave no copy in flight: wait (bounded, ignoring the abort
                 // flag) for the last use of every stage that was issued
                 int32_t dummy_abort = 0;
-                for (int i = max(0, issued - S); i < issued; ++i) {
-                    if (drop_first && i == 0) continue;
-                    mbar_wait(bar_full + 8 * (i % S), (i / S) & 1, p.timeout_ns, p.status, &dummy_abort);
+                for (int j = max(0, issued - S); j < issued; ++j) {
+                    if (drop_first && j == 0) continue;
+                    mbar_wait(bar_full + 8 * (j % S), (j / S) & 1, p.timeout_ns, p.status, &dummy_abort);
                 }
             }
         }
@@ -196,7 +199,8 @@ __global__ void __launch_bounds__(Cfg<NB8, WK>::kThreads, 1)
 
     uint32_t cons_phase0 = 0;
     auto cons_sync0 = [&]() -> bool {
-        mbar_arrive(bar_cons);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_cons);
         const bool ok = mbar_wait(bar_cons, cons_phase0, p.timeout_ns, p.status, abort_flag);
         cons_phase0 ^= 1u;
         return ok;
@@ -222,7 +226,8 @@ __global__ void __launch_bounds__(Cfg<NB8, WK>::kThreads, 1)
     uint32_t cons_phase = cons_phase0;
     // barrier over the consumer threads with a bounded wait; false = aborted
     auto cons_sync = [&]() -> bool {
-        mbar_arrive(bar_cons);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_cons);
         const bool ok = mbar_wait(bar_cons, cons_phase, p.timeout_ns, p.status, abort_flag);
         cons_phase ^= 1u;
         return ok;
@@ -357,7 +362,6 @@ __global__ void __launch_bounds__(Cfg<NB8, WK>::kThreads, 1)
         return cons_sync();
     };
 
-    uint32_t a[2][C::kKgPerWarp][4];
     int64_t nt = nt_first;
     int kt = (int)(rec_begin - nt_first * KT);
     int s = 0;
@@ -379,19 +383,9 @@ __global__ void __launch_bounds__(Cfg<NB8, WK>::kThreads, 1)
             x_thread[kgl] = ((q >> 1) * 8 + (lane & 7)) * 128 + ((chunk ^ (lane & 7)) << 4);
         }
     }
-    for (int i = 0; i < nrec; ++i) {
-        if (nt != cur_nt) {
-            if (cur_nt >= 0 && !flush(cur_nt)) return;
-            cur_nt = nt;
-            load_consts(nt);
-        }
-        if (!mbar_try_wait(bar_full + 8 * s, full_phase) &&
-            !mbar_wait(bar_full + 8 * s, full_phase, p.timeout_ns, p.status, abort_flag))
-            return;
-        const uint32_t *rw = reinterpret_cast<const uint32_t *>(rec_thread + s * w12i::kRecBytes);
-        const uint32_t xb = x_s + s * C::kXBytes;
-
-        // decode this warp's 32 channels x (16 * kKgPerWarp) K of the record
+    using Frag = uint32_t[2][C::kKgPerWarp][4];
+    // decode this warp's 32 channels x (16 * kKgPerWarp) K of one record
+    auto decode_rec = [&](const uint32_t *rw, Frag &fa) {
 #pragma unroll
         for (int mb = 0; mb < 2; ++mb) {
             uint32_t nib_lo = 0, nib_hi = 0;
@@ -405,36 +399,38 @@ __global__ void __launch_bounds__(Cfg<NB8, WK>::kThreads, 1)
                 const uint32_t sh = (kg & 1) * 4;
                 const uint32_t v_lo = rw[(kg * 2048 + mb * 256) / 4];
                 const uint32_t v_hi = rw[(kg * 2048 + mb * 256 + 128) / 4];
-                decode_word(v_lo, nib_lo >> sh, cc[mb][0], p.mul16, a[mb][kgl][0], a[mb][kgl][2]);
-                decode_word(v_hi, nib_hi >> sh, cc[mb][1], p.mul16, a[mb][kgl][1], a[mb][kgl][3]);
+                decode_word(v_lo, nib_lo >> sh, cc[mb][0], p.mul16, fa[mb][kgl][0], fa[mb][kgl][2]);
+                decode_word(v_hi, nib_hi >> sh, cc[mb][1], p.mul16, fa[mb][kgl][1], fa[mb][kgl][3]);
             }
         }
-        // escaped slots: the owning lane replaces the filler by the exact value
-        {
-            const int32_t e0 = esc_off_s[i] - e_lo, e1 = esc_off_s[i + 1] - e_lo;
-            for (int e = e0; e < e1; ++e) {
-                const uint32_t en = esc_cached ? esc_s[e] : __ldg(p.esc + e_lo + e);
-                const int nl = (en >> 22) & 0x7F, kl = (en >> 16) & 0x3F;
-                const int kg = kl >> 4;
-                if ((nl >> 5) != mw || (kg / C::kKgPerWarp) != wk) continue;
-                const int kk = kl & 15;
-                if (lane != ((nl & 7) * 4 + ((kk & 7) >> 1))) continue;
-                const int mb_e = (nl >> 4) & 1, kgl_e = kg % C::kKgPerWarp;
-                const int j_e = (kk >> 3) * 2 + ((nl >> 3) & 1);
-                const uint32_t val = en & 0xFFFFu;
-                const bool upper = kk & 1;
+    };
+    // escaped slots of record i: the owning lane replaces the filler by the exact value
+    auto patch_rec = [&](int i, Frag &fa) {
+        const int32_t e0 = esc_off_s[i] - e_lo, e1 = esc_off_s[i + 1] - e_lo;
+        for (int e = e0; e < e1; ++e) {
+            const uint32_t en = esc_cached ? esc_s[e] : __ldg(p.esc + e_lo + e);
+            const int nl = (en >> 22) & 0x7F, kl = (en >> 16) & 0x3F;
+            const int kg = kl >> 4;
+            if ((nl >> 5) != mw || (kg / C::kKgPerWarp) != wk) continue;
+            const int kk = kl & 15;
+            if (lane != ((nl & 7) * 4 + ((kk & 7) >> 1))) continue;
+            const int mb_e = (nl >> 4) & 1, kgl_e = kg % C::kKgPerWarp;
+            const int j_e = (kk >> 3) * 2 + ((nl >> 3) & 1);
+            const uint32_t val = en & 0xFFFFu;
+            const bool upper = kk & 1;
 #pragma unroll
-                for (int mb = 0; mb < 2; ++mb)
+            for (int mb = 0; mb < 2; ++mb)
 #pragma unroll
-                    for (int kgl = 0; kgl < C::kKgPerWarp; ++kgl)
+                for (int kgl = 0; kgl < C::kKgPerWarp; ++kgl)
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            if (mb == mb_e && kgl == kgl_e && j == j_e)
-                                a[mb][kgl][j] = upper ? ((a[mb][kgl][j] & 0x0000FFFFu) | (val << 16))
-                                                      : ((a[mb][kgl][j] & 0xFFFF0000u) | val);
-            }
+                    for (int j = 0; j < 4; ++j)
+                        if (mb == mb_e && kgl == kgl_e && j == j_e)
+                            fa[mb][kgl][j] = upper ? ((fa[mb][kgl][j] & 0x0000FFFFu) | (val << 16))
+                                                   : ((fa[mb][kgl][j] & 0xFFFF0000u) | val);
         }
-        // activations (B operand) from the swizzled TMA block, then MMA
+    };
+    // activations (B operand) from the swizzled TMA block, then MMA
+    auto mma_rec = [&](uint32_t xb, const Frag &fa) {
 #pragma unroll
         for (int kgl = 0; kgl < C::kKgPerWarp; ++kgl) {
             const uint32_t xa = xb + x_thread[kgl];
@@ -442,7 +438,7 @@ __global__ void __launch_bounds__(Cfg<NB8, WK>::kThreads, 1)
                 uint32_t b0, b1;
                 ldsm_x2(xa, b0, b1);
 #pragma unroll
-                for (int mb = 0; mb < 2; ++mb) mma_bf16_16816(acc[mb][0], a[mb][kgl], b0, b1);
+                for (int mb = 0; mb < 2; ++mb) mma_bf16_16816(acc[mb][0], fa[mb][kgl], b0, b1);
             } else {
                 uint32_t b[NB8][2];
                 ldsm_x4_off<0>(xa, b[0][0], b[0][1], b[1][0], b[1][1]);
@@ -454,13 +450,49 @@ __global__ void __launch_bounds__(Cfg<NB8, WK>::kThreads, 1)
 #pragma unroll
                 for (int nb = 0; nb < NB8; ++nb)
 #pragma unroll
-                    for (int mb = 0; mb < 2; ++mb) mma_bf16_16816(acc[mb][nb], a[mb][kgl], b[nb][0], b[nb][1]);
+                    for (int mb = 0; mb < 2; ++mb) mma_bf16_16816(acc[mb][nb], fa[mb][kgl], b[nb][0], b[nb][1]);
+            }
+        }
+    };
+    auto rec_words = [&](int q) {
+        return reinterpret_cast<const uint32_t *>(rec_thread + (s * RPS + q) * w12i::kRecBytes);
+    };
+    auto rec_x = [&](int q) { return x_s + (s * RPS + q) * C::kXBytes; };
+
+    for (int i = 0; i < nrec;) {
+        if (!mbar_try_wait(bar_full + 8 * s, full_phase) &&
+            !mbar_wait(bar_full + 8 * s, full_phase, p.timeout_ns, p.status, abort_flag))
+            return;
+        int q = 0;
+        while (q < RPS && i < nrec) {
+            if (nt != cur_nt) {
+                if (cur_nt >= 0 && !flush(cur_nt)) return;
+                cur_nt = nt;
+                load_consts(nt);
+            }
+            if (RPS == 2 && q == 0 && i + 1 < nrec && kt + 1 < KT) {
+                // both records of the stage belong to this tile: interleave them
+                Frag f0, f1;
+                decode_rec(rec_words(0), f0);
+                decode_rec(rec_words(1), f1);
+                patch_rec(i, f0);
+                patch_rec(i + 1, f1);
+                mma_rec(rec_x(0), f0);
+                mma_rec(rec_x(1), f1);
+                q += 2, i += 2, kt += 2;
+                if (kt == KT) kt = 0, ++nt;
+            } else {
+                Frag f0;
+                decode_rec(rec_words(q), f0);
+                patch_rec(i, f0);
+                mma_rec(rec_x(q), f0);
+                ++q, ++i;
+                if (++kt == KT) kt = 0, ++nt;
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + 8 * s);
         if (++s == S) s = 0, full_phase ^= 1u;
-        if (++kt == KT) kt = 0, ++nt;
     }
     if (cur_nt >= 0) flush(cur_nt);
 }
@@ -519,10 +551,10 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-template <int NB8, int WK>
+template <int NB8, int WK, int RPS>
 int launch_t(const w12i::GemmArgs &a, const CUtensorMap &xmap, cudaStream_t st)
 {
-    using C = Cfg<NB8, WK>;
+    using C = Cfg<NB8, WK, RPS>;
     const int64_t T = (int64_t)a.w.n_tiles * a.w.k_tiles;
     const int G = (int)std::min<int64_t>(a.num_sms, T);
     const int max_recs = (int)((T + G - 1) / G);
@@ -550,14 +582,14 @@ int launch_t(const w12i::GemmArgs &a, const CUtensorMap &xmap, cudaStream_t st)
     p.base_tiles = std::min<int>(64, (int)(max_recs / a.w.k_tiles + 2));
     const int budget = 227 * 1024;
     int stages = 8;
-    while (stages > 2 && smem_plan<NB8, WK>(stages, max_recs, p.esc_cap, p.base_tiles).total > budget) --stages;
+    while (stages > 2 && smem_plan<NB8, WK, RPS>(stages, max_recs, p.esc_cap, p.base_tiles).total > budget) --stages;
     p.stages = stages;
-    const int smem = smem_plan<NB8, WK>(stages, max_recs, p.esc_cap, p.base_tiles).total;
+    const int smem = smem_plan<NB8, WK, RPS>(stages, max_recs, p.esc_cap, p.base_tiles).total;
     if (smem > budget) return (int)cudaErrorInvalidConfiguration;
-    cudaError_t e = cudaFuncSetAttribute(k_w12_gemm<NB8, WK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(k_w12_gemm<NB8, WK, RPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return (int)e;
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, k_w12_gemm<NB8, WK>);
+    e = cudaFuncGetAttributes(&fa, k_w12_gemm<NB8, WK, RPS>);
     if (e != cudaSuccess) return (int)e;
     if (fa.maxThreadsPerBlock < C::kThreads) return (int)cudaErrorLaunchOutOfResources;
     cudaLaunchConfig_t cfg{};
@@ -570,7 +602,7 @@ int launch_t(const w12i::GemmArgs &a, const CUtensorMap &xmap, cudaStream_t st)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 1 : 0;
-    return (int)cudaLaunchKernelEx(&cfg, k_w12_gemm<NB8, WK>, xmap, p);
+    return (int)cudaLaunchKernelEx(&cfg, k_w12_gemm<NB8, WK, RPS>, xmap, p);
 }
 
 }  // namespace
@@ -593,12 +625,13 @@ int launch_gemm(const GemmArgs &a, void *stream)
                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return (int)cudaErrorInvalidValue;
-    // up to 32 rows: 16 consumer warps, one 16-K group each; 64 rows: 8 warps
+    // 8 consumer warps (two 16-K groups each); two records per stage up to 32
+    // rows (one wait and one release per 24 KB), one record per stage at 64 rows
     switch (nb8) {
-    case 1: return launch_t<1, 4>(a, xmap, st);
-    case 2: return launch_t<2, 4>(a, xmap, st);
-    case 4: return launch_t<4, 4>(a, xmap, st);
-    default: return launch_t<8, 2>(a, xmap, st);
+    case 1: return launch_t<1, 2, 2>(a, xmap, st);
+    case 2: return launch_t<2, 2, 2>(a, xmap, st);
+    case 4: return launch_t<4, 2, 2>(a, xmap, st);
+    default: return launch_t<8, 2, 1>(a, xmap, st);
     }
 }
 

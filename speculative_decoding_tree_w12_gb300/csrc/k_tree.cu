@@ -45,6 +45,7 @@ struct TreeParams {
 };
 
 struct Hdr {
+    uint8_t p_r[w12i::kMaxBudget];
     uint32_t hist[256];
     int32_t red[kWarps];
     int32_t bcast[2];
@@ -104,10 +105,17 @@ __device__ void radix_select(const uint32_t *keys, int n, int K, uint32_t &tau, 
 {
     uint32_t prefix = 0, mask = 0;
     int krem = K;
+    const int rounds = (n + kThreads - 1) / kThreads;   // uniform trip count: whole warps vote
     for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = threadIdx.x; i < n; i += kThreads) {
-            const uint32_t k = keys[i];
-            if ((k & mask) == prefix) atomicAdd(&h.hist[(k >> shift) & 255u], 1u);
+        for (int it = 0; it < rounds; ++it) {
+            const int i = it * kThreads + threadIdx.x;
+            const uint32_t k = i < n ? keys[i] : 0u;
+            const bool counted = i < n && (k & mask) == prefix;
+            const uint32_t bin = counted ? ((k >> shift) & 255u) : 256u;
+            // one atomic per distinct bin per warp: scores of one depth share
+            // their top bits, so per-key atomics would serialise on one bin
+            const unsigned peers = __match_any_sync(0xffffffffu, bin);
+            if (counted && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h.hist[bin], (uint32_t)__popc(peers));
         }
         __syncthreads();
         if (threadIdx.x < 32) {
@@ -197,6 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tree_build(const TreeParams p)
 
     pdl_wait();
     for (int i = tid; i < 256; i += kThreads) h.hist[i] = 0;
+    for (int r = tid; r < p.n_req; r += kThreads) h.p_r[r] = p.p_r[r];
     if (p.stage_lattice) {
         const int n = p.n_req * p.p_max * 16;
         for (int i = tid; i < n; i += kThreads) {
@@ -247,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tree_build(const TreeParams p)
             const int par = pb + pl;
             const int r = u_req[par];
             uint32_t key = kInvalid;
-            if (d <= p.p_r[r]) {
+            if (d <= h.p_r[r]) {
                 const float e = edge(r, d, u_meta[par] & 0xFF, j);
                 if (!(e <= 0.f) || isinf(e)) bad_input = true;
                 key = score_key(__fadd_rn(u_score[par], e));

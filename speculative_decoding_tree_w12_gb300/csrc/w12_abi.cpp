@@ -38,7 +38,21 @@ int prof_mark(cudaStream_t st)
     }
     return (int)cudaEventRecord(g_prof_ev[g_prof_used++], st);
 }
-constexpr int kPartialRows = 64;         // rows per GEMM launch (larger R is sliced)
+constexpr int kPartialRows = 64;         // rows per warp-MMA launch (larger R is sliced)
+
+// rows of one CTA's partial tile: the warp-MMA path pads to <= 64, the
+// tensor-memory path to a multiple of 32
+int partial_rows(int32_t R) { return std::max(kPartialRows, (R + 31) / 32 * 32); }
+
+// Path choice: the tensor-memory kernel streams the weights once for any
+// R <= 256; the warp-MMA kernel covers R <= 64 per pass.  Debug flag bit 1
+// forces the tensor-memory path, bit 2 the warp-MMA path.
+bool use_tc(int32_t R)
+{
+    if (g_debug_flags & 2) return true;
+    if (g_debug_flags & 4) return false;
+    return R > kPartialRows;
+}
 
 int num_sms()
 {
@@ -104,7 +118,7 @@ struct Ws {
     float *partial(int slot) const
     {
         return reinterpret_cast<float *>(base + L.partial) +
-               static_cast<size_t>(slot) * kMaxCtas * 2 * kPartialRows * kTileN;
+               static_cast<size_t>(slot) * kMaxCtas * 2 * partial_rows(L.rows) * kTileN;
     }
     // arrival counters start at zero for every call (the kernels also reset
     // each counter they finish with, so launches inside one call need no memset)
@@ -123,6 +137,7 @@ WsLayout layout_for(int32_t R, int64_t max_n, int64_t vocab, int32_t n_req)
 {
     WsLayout L{};
     L.rows8 = (std::max<int32_t>(R, 1) + 7) / 8 * 8;
+    L.rows = std::max<int32_t>(R, 1);
     L.max_tiles_n = std::max<int64_t>(std::max<int64_t>(max_n, vocab), kTileN) / kTileN;
     L.vocab_tiles = std::max<int64_t>(vocab, kTileN) / kTileN;
     L.max_ctas = kMaxCtas;
@@ -132,7 +147,7 @@ WsLayout layout_for(int32_t R, int64_t max_n, int64_t vocab, int32_t n_req)
     L.counters = o;
     o = align256(o + static_cast<size_t>(kGemmSlots) * L.max_tiles_n * 4);
     L.partial = o;
-    o = align256(o + static_cast<size_t>(kGemmSlots) * kMaxCtas * 2 * kPartialRows * kTileN * 4);
+    o = align256(o + static_cast<size_t>(kGemmSlots) * kMaxCtas * 2 * partial_rows(L.rows) * kTileN * 4);
     L.stage1_val = o;
     o = align256(o + static_cast<size_t>(L.rows8) * L.vocab_tiles * 4);
     L.stage1_idx = o;
@@ -152,11 +167,13 @@ w12_status ws_check(void *ws, size_t ws_bytes, const WsLayout &L)
 int gemm_slices(const DevWeight &dw, const uint16_t *x, int32_t R, int mode, uint16_t *y, const Ws &ws, int &slot,
                 bool pdl, cudaStream_t st)
 {
-    for (int32_t r0 = 0; r0 < R; r0 += kPartialRows) {
+    const bool tc = use_tc(R);
+    const int32_t step = tc ? R : kPartialRows;
+    for (int32_t r0 = 0; r0 < R; r0 += step) {
         GemmArgs a{};
         a.w = dw;
         a.x = x + static_cast<int64_t>(r0) * dw.k;
-        a.R = std::min<int32_t>(kPartialRows, R - r0);
+        a.R = std::min<int32_t>(step, R - r0);
         a.mode = mode;
         a.y = y ? y + static_cast<int64_t>(r0) * dw.n : nullptr;
         a.stage1_val = ws.s1_val() + static_cast<int64_t>(r0) * dw.n_tiles;
@@ -168,7 +185,7 @@ int gemm_slices(const DevWeight &dw, const uint16_t *x, int32_t R, int mode, uin
         a.pdl = pdl;
         a.debug_flags = g_debug_flags;
         a.timeout_ns = g_timeout_ns;
-        const int e = launch_gemm(a, st);
+        const int e = tc ? launch_gemm_tc(a, st) : launch_gemm(a, st);
         if (e) return e;
         if (int pe = prof_mark(st)) return pe;
         slot = (slot + 1) % kGemmSlots;

@@ -31,6 +31,7 @@ struct WsLayout {
     size_t tree;          // tree-build scratch
     size_t total;
     int64_t max_tiles_n, max_ctas, rows8, vocab_tiles;
+    int32_t rows;
 };
 
 WsLayout ws_layout(int32_t R, int64_t max_n, int64_t vocab, int32_t n_req, int num_sms);
@@ -71,7 +72,8 @@ struct GemmArgs {
     uint64_t timeout_ns;
 };
 
-int launch_gemm(const GemmArgs &a, void *stream);
+int launch_gemm(const GemmArgs &a, void *stream);      // warp-MMA path, R <= 64 per launch
+int launch_gemm_tc(const GemmArgs &a, void *stream);   // tensor-memory path, R <= 256
 // same kernel, scratch in a file-scope device array (no workspace argument)
 int launch_gemm_static_scratch(const GemmArgs &a, void *stream);
 int static_scratch_limits(int32_t *max_rows, int32_t *max_tiles);

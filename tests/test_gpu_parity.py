@@ -22,6 +22,15 @@ def w12():
     return m
 
 
+@pytest.fixture(params=["warp_mma", "tcgen05"])
+def path(request, w12):
+    """Run the test on one GEMM kernel: the warp-MMA kernel (flag 4) or the
+    tensor-memory kernel (flag 2)."""
+    w12.debug_set(4 if request.param == "warp_mma" else 2, 0)
+    yield request.param
+    w12.debug_set(0, 0)
+
+
 def _dev_bf16(bits: np.ndarray):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
 
@@ -96,7 +105,7 @@ GEMM_CASES = [
 
 
 @pytest.mark.parametrize("n,k,R,outl,zero", GEMM_CASES)
-def test_gemm_matches_oracle(w12, n, k, R, outl, zero):
+def test_gemm_matches_oracle(w12, path, n, k, R, outl, zero):
     w = synth.weights(n, k, n + k + R, 11, outl, zero)
     x = synth.activations(R, k, n + k + R, 12)
     dw = _packed(w12, w)
@@ -114,7 +123,7 @@ def test_gemm_matches_oracle(w12, n, k, R, outl, zero):
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
 
 
-def test_gemm_exact_integer_case(w12):
+def test_gemm_exact_integer_case(w12, path):
     """Products and sums exact in FP32 -> the BF16 output is the BF16 rounding
     of the exact integer result."""
     g = np.random.default_rng(7)
@@ -135,7 +144,7 @@ def test_gemm_exact_integer_case(w12):
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("V,K,R", [(4096, 512, 8), (8192, 1024, 33), (1280, 2560, 70), (2048, 384, 256)])
-def test_lmhead_argmax_matches_oracle(w12, V, K, R):
+def test_lmhead_argmax_matches_oracle(w12, path, V, K, R):
     wh = synth.weights(V, K, V + R, 2000, 0.005, 0.005)
     h = synth.activations(R, K, V + R, 5)
     dw = _packed(w12, wh)
@@ -233,7 +242,7 @@ def _oracle_step(w: synth.Workload, lat, wh, n2, seed=0):
     ("b4_tree", dict(vocab=4096, hidden=256, linears=((768, 256), (256, 768)))),
     ("b4_chain", dict(vocab=4096, hidden=256, linears=((256, 256),))),
 ])
-def test_verify_step_matches_oracle(w12, name, kw):
+def test_verify_step_matches_oracle(w12, path, name, kw):
     """Whole pass through the C ABI: tree -> linears -> head argmax -> accept,
     against the oracle (accepted tokens bit-exact on margin-passing requests)."""
     w = synth.scaled(synth.WORKLOADS[name], **kw)
@@ -277,14 +286,15 @@ def test_verify_step_matches_oracle(w12, name, kw):
     assert np.all(acc_len.cpu().numpy() >= 1)
 
 
-def test_bounded_wait_times_out_cleanly(w12):
+@pytest.mark.parametrize("kernel_flag", [4, 2])
+def test_bounded_wait_times_out_cleanly(w12, kernel_flag):
     """A GEMM whose first record is never copied (test hook) records
     W12_E_TIMEOUT and returns; the context stays usable."""
     w = synth.weights(1024, 512, 1, 1)
     x = synth.activations(8, 512, 1, 2)
     dw = _packed(w12, w)
     ws = w12.Workspace(8, 1024)
-    w12.debug_set(1, 50_000_000)      # 50 ms limit
+    w12.debug_set(1 | kernel_flag, 50_000_000)      # 50 ms limit
     try:
         w12.w12_gemm(dw, _dev_bf16(x), ws)
         torch.cuda.synchronize()
