@@ -3,26 +3,30 @@
 // Same contract as the stream-K kernel in k_gemm.cu (SpecPilot explainer,
 // section 4.1 "W12 GEMM": records restored in registers and fed to the tensor
 // cores, a fixed-order stream-K split), laid out for Blackwell's tensor
-// memory instead of warp-level MMA fragments:
+// memory:
 //
-//   producer warp   bulk copy of each 12 KB record + 2-D TMA of the matching
-//                   activation block (128-byte swizzle) into a shared ring
-//   decode warps    two groups of four, alternating records; thread = output
-//                   channel: six 16-byte shared loads, in-register decode of
-//                   its 64 weights, escape patch, one tcgen05.st of 32
-//                   columns into a tensor-memory A buffer (4 buffers)
-//   MMA thread      per record four tcgen05.mma (M=128 channels, N = rows
-//                   rounded up to 32, K=16) with A from tensor memory and the
-//                   activations from shared memory, FP32 accumulator in
-//                   tensor memory (two accumulators while N <= 192)
-//   epilogue warps  tcgen05.ld of a finished tile; BF16 rows, or the tile's
-//                   (max, index) per row for the LM head; a tile split between
-//                   CTAs is published as a partial and finished by the last
-//                   contributor in CTA order (deterministic, no waiting)
+//   producer warp    bulk copy of each 12 KB record + 2-D TMA of the matching
+//                    activation block (128-byte swizzle) into a shared ring
+//   decode groups    one or two groups of four warps (one per tensor-memory
+//                    lane quarter); a group takes every G-th record of the
+//                    CTA.  Thread = output channel: six 16-byte shared loads,
+//                    in-register decode of its 64 weights, escape patch, one
+//                    tcgen05.st of 32 columns into the group's A buffer.  The
+//                    group then meets at a named barrier and one of its
+//                    threads issues the record's four MMAs (M = 128 channels,
+//                    N = rows rounded up to 32, K = 16) into the group's own
+//                    FP32 accumulator, followed by one commit that frees both
+//                    the shared-memory stage and the A buffer.  No warp waits
+//                    on a signal from another role while records are in flight.
+//   epilogue warps   tcgen05.ld of each group's accumulator for a finished
+//                    tile, summed in group order (deterministic); BF16 rows,
+//                    or the tile's (max, index) per row for the LM head; a
+//                    tile split between CTAs is published as a partial and
+//                    finished by the last contributor in CTA order.
 //
 // Every wait is bounded: on a timeout the kernel records W12_E_TIMEOUT, all
-// roles stop, the MMA thread waits for its issued work, and tensor memory is
-// released before the CTA exits.
+// roles stop together (group exits are agreed at the named barrier), issued
+// MMAs are waited for, and tensor memory is released before the CTA exits.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -34,16 +38,15 @@ using namespace w12d;
 
 namespace {
 
-constexpr int kProducerWarp = 0;
-constexpr int kMmaWarp = 1;
-constexpr int kDecodeWarp0 = 2;   // warps 2..9: group 0 = 2..5, group 1 = 6..9
-constexpr int kEpiWarp0 = 10;     // warps 10..13
-constexpr int kThreads = 14 * 32;
-constexpr int kMaxABufs = 8;      // tensor-memory A buffers of 32 columns (8 while N <= 128, else 4)
+constexpr int kProducerWarp = 0;   // also allocates tensor memory
+constexpr int kGroupWarp0 = 1;     // decode group g = warps 1 + 4g .. 4 + 4g
+constexpr int kMaxGroups = 2;
+constexpr int kEpiWarp0 = 1 + 4 * kMaxGroups;   // warps 9..12
+constexpr int kThreads = (kEpiWarp0 + 4) * 32;
 constexpr int kACols = 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kRecsPerStage = 1;  // records per shared-memory stage
-constexpr int kBatch = 4;         // records per MMA batch: one wait round, 16 MMAs, two commits
+constexpr int kBarCaches = 1;      // named barrier: decode threads after filling the shared caches
+constexpr int kBarGroup0 = 2;      // named barrier per decode group (2, 3)
 
 struct TcParams {
     const uint8_t *rec;
@@ -52,8 +55,9 @@ struct TcParams {
     const uint32_t *esc;
     int32_t n_tiles, k_tiles, R, mode;
     int32_t nr;          // MMA N: rows rounded up to 32
-    int32_t d_bufs;      // accumulators in tensor memory (1 or 2)
-    int32_t a_bufs;      // A buffers in tensor memory (4 or 8); accumulators start after them
+    int32_t groups;      // decode groups (1 or 2)
+    int32_t a_bufs;      // A buffers per group
+    int32_t d_bufs;      // accumulators per group (1 or 2)
     uint16_t *y;
     int64_t ldy;
     float *s1_val;
@@ -76,11 +80,11 @@ __host__ __device__ inline Plan plan(int stages, int nr, int max_recs, int esc_c
     Plan p;
     int o = 0;
     p.rec = o;
-    o += stages * kRecsPerStage * w12i::kRecBytes;
+    o += stages * w12i::kRecBytes;            // 12 KB per stage keeps the 1024-byte alignment
     p.x = o;
-    o += stages * kRecsPerStage * nr * 128;
+    o += stages * nr * 128;
     p.bars = o;
-    o += 8 * (2 * stages + 2 * kMaxABufs + 4 + 2);   // full + slot-empty, A ready + A free, acc, syncs
+    o += 8 * (2 * stages + 4 * kMaxGroups * 2 + 2);   // full, done; acc full/empty [g][d]; epilogue sync
     p.misc = o;
     o += 32;
     p.escoff = o;
@@ -98,11 +102,23 @@ __host__ __device__ inline Plan plan(int stages, int nr, int max_recs, int esc_c
 __device__ __forceinline__ int cta_of_record(int64_t r, int G, int64_t T) { return (int)(((r + 1) * G - 1) / T); }
 __device__ __forceinline__ int64_t first_record(int c, int G, int64_t T) { return (int64_t)c * T / G; }
 
+// AND of `pred` over the `threads` threads meeting at named barrier `id`
+__device__ __forceinline__ bool bar_and(int id, int threads, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(threads)
+        : "memory");
+    return r != 0;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_constant__ CUtensorMap xmap, const TcParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const int S = p.stages, NR = p.nr;
+    const int S = p.stages, NR = p.nr, GR = p.groups, NAG = p.a_bufs, DB = p.d_bufs;
     const Plan pl = plan(S, NR, p.max_recs, p.esc_cap, p.base_tiles);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, cta = blockIdx.x;
@@ -113,13 +129,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
     const int64_t nt_first = rec_begin / KT, nt_last = (rec_end - 1) / KT;
 
     const uint32_t rec_s = smem_u32(smem + pl.rec), x_s = smem_u32(smem + pl.x);
+    const uint32_t xb = (uint32_t)NR * 128;
     const uint32_t bar0 = smem_u32(smem + pl.bars);
-    const uint32_t bar_full = bar0, bar_empty = bar0 + 8 * S;
-    const uint32_t bar_afull = bar_empty + 8 * S, bar_afree = bar_afull + 8 * kMaxABufs;
-    const uint32_t bar_accfull = bar_afree + 8 * kMaxABufs, bar_accempty = bar_accfull + 16;
-    const int NA = p.a_bufs;
-    const int kDCol0 = NA * kACols;
-    const uint32_t bar_epi = bar_accempty + 16, bar_dec = bar_epi + 8;
+    const uint32_t bar_full = bar0, bar_done = bar0 + 8 * S;
+    const uint32_t bar_accfull = bar_done + 8 * S;                  // [g][d]
+    const uint32_t bar_accempty = bar_accfull + 8 * kMaxGroups * 2;  // [g][d]
+    const uint32_t bar_epi = bar_accempty + 8 * kMaxGroups * 2;
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(smem + pl.misc);
     int32_t *last_flag = reinterpret_cast<int32_t *>(smem + pl.misc + 4);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + pl.misc + 8);
@@ -129,236 +144,197 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, 4 * kBatch + 1);   // per slot of kBatch stages: 4 decode warps per record + 1 commit
+            mbar_init(bar_full + 8 * s, 1);   // the producer's expect_tx arrival (+ the copies' bytes)
+            mbar_init(bar_done + 8 * s, 1);   // one commit per record: its MMAs (and its reads) are done
         }
-        for (int b = 0; b < kMaxABufs; ++b) {
-            mbar_init(bar_afull + 8 * b, 4);    // per A buffer: the 4 decode warps that filled it
-            mbar_init(bar_afree + 8 * b, 1);    // per batch of A buffers: one MMA commit
+        for (int b = 0; b < kMaxGroups * 2; ++b) {
+            mbar_init(bar_accfull + 8 * b, 1);    // commit after a tile's last MMA of the group
+            mbar_init(bar_accempty + 8 * b, 4);   // the four epilogue warps have read the accumulator
         }
-        for (int d = 0; d < 2; ++d) {
-            mbar_init(bar_accfull + 8 * d, 1);
-            mbar_init(bar_accempty + 8 * d, 4);
-        }
-        mbar_init(bar_epi, 4);     // one arrival per epilogue warp
-        mbar_init(bar_dec, 8);     // one arrival per decode warp
+        mbar_init(bar_epi, 4);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == kMmaWarp) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    if (warp == kProducerWarp) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     pdl_launch_dependents();
 
+    const uint32_t d_col0 = (uint32_t)(GR * NAG * kACols);
+    auto a_col = [&](int g, int a) { return (uint32_t)((g * NAG + a) * kACols); };
+    auto d_col = [&](int g, int d) { return d_col0 + (uint32_t)((g * DB + d) * NR); };
+
     if (warp == kProducerWarp) {
         // -------------------------------------------------------------- producer
         if (lane == 0) {
             prefetch_tmap(&xmap);
             const uint64_t pol = policy_evict_first();
-            const uint32_t xb = (uint32_t)NR * 128;
             const bool drop_first = (p.debug_flags & 1) && cta == 0;
-            const int nst = (nrec + kRecsPerStage - 1) / kRecsPerStage;
-            auto recs_in = [&](int j) { return min(kRecsPerStage, nrec - j * kRecsPerStage); };
-            auto issue_w = [&](int j, int sl) {
-                const int n = recs_in(j);
-                mbar_expect_tx(bar_full + 8 * sl, (uint32_t)n * (w12i::kRecBytes + xb));
-                if (!(drop_first && j == 0))
-                    bulk_g2s(rec_s + sl * kRecsPerStage * w12i::kRecBytes,
-                             p.rec + (rec_begin + j * kRecsPerStage) * (int64_t)w12i::kRecBytes,
-                             (uint32_t)n * w12i::kRecBytes, bar_full + 8 * sl, pol);
+            auto issue_w = [&](int i, int s) {
+                mbar_expect_tx(bar_full + 8 * s, (uint32_t)w12i::kRecBytes + xb);
+                if (!(drop_first && i == 0))
+                    bulk_g2s(rec_s + s * w12i::kRecBytes, p.rec + (rec_begin + i) * (int64_t)w12i::kRecBytes,
+                             (uint32_t)w12i::kRecBytes, bar_full + 8 * s, pol);
             };
-            auto issue_x = [&](int j, int sl) {
-                if (drop_first && j == 0) return;
-                for (int r = 0; r < recs_in(j); ++r) {
-                    const int kt = (int)((rec_begin + j * kRecsPerStage + r) % KT);
-                    tma_load_2d(x_s + (sl * kRecsPerStage + r) * xb, &xmap, kt * w12i::kTileK, 0, bar_full + 8 * sl);
-                }
+            auto issue_x = [&](int i, int s) {
+                if (drop_first && i == 0) return;
+                const int kt = (int)((rec_begin + i) % KT);
+                tma_load_2d(x_s + s * xb, &xmap, kt * w12i::kTileK, 0, bar_full + 8 * s);
             };
-            const int pre = min(S, nst);
-            for (int j = 0; j < pre; ++j) issue_w(j, j);
+            const int pre = min(S, nrec);
+            // weights do not depend on earlier kernels: start them before the
+            // programmatic-dependency wait
+            for (int i = 0; i < pre; ++i) issue_w(i, i);
             pdl_wait();
-            for (int j = 0; j < pre; ++j) issue_x(j, j);
+            for (int i = 0; i < pre; ++i) issue_x(i, i);
             int issued = pre;
-            for (int j = pre; j < nst; ++j) {
-                const int sl = j % S;
-                // the first stage of a slot waits until the whole slot is released
-                if (sl % kBatch == 0 &&
-                    !mbar_wait(bar_empty + 8 * (sl / kBatch), ((j / S) - 1) & 1, p.timeout_ns, p.status, abort_flag))
-                    break;
-                issue_w(j, sl);
-                issue_x(j, sl);
-                issued = j + 1;
+            for (int i = pre; i < nrec; ++i) {
+                const int s = i % S;
+                // stage s was last used by record i - S: wait for its MMAs
+                if (!mbar_wait(bar_done + 8 * s, ((i / S) - 1) & 1, p.timeout_ns, p.status, abort_flag)) break;
+                issue_w(i, s);
+                issue_x(i, s);
+                issued = i + 1;
             }
             if (*abort_flag) {
+                // leave no copy in flight
                 int32_t no_abort = 0;
-                for (int j = max(0, issued - S); j < issued; ++j) {
-                    if (drop_first && j == 0) continue;
-                    mbar_wait(bar_full + 8 * (j % S), (j / S) & 1, p.timeout_ns, p.status, &no_abort);
+                for (int i = max(0, issued - S); i < issued; ++i) {
+                    if (drop_first && i == 0) continue;
+                    mbar_wait(bar_full + 8 * (i % S), (i / S) & 1, p.timeout_ns, p.status, &no_abort);
                 }
             }
-        }
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------- MMA issue
-        const uint32_t idesc = idesc_bf16_f32(128, NR);
-        int kt = (int)(rec_begin - nt_first * KT);
-        int dbuf = 0;
-        uint32_t duse[2] = {0, 0};
-        int last_i = -1;
-        for (int i0 = 0; i0 < nrec; i0 += kBatch) {
-            // lanes wait in parallel: lane l < kBatch on record i0+l's A buffer,
-            // lane kBatch+l on its shared-memory stage
-            bool ok = true;
-            if (lane < 2 * kBatch) {
-                const int i = i0 + (lane % kBatch);
-                if (i < nrec) {
-                    if (lane < kBatch)
-                        ok = mbar_wait(bar_afull + 8 * (i % NA), (i / NA) & 1, p.timeout_ns, p.status, abort_flag);
-                    else
-                        ok = mbar_wait(bar_full + 8 * (i % S), (i / S) & 1, p.timeout_ns, p.status, abort_flag);
-                }
-            }
-            if (__any_sync(0xffffffffu, !ok)) break;
-            if (lane == 0) {
-                tc_fence_after();
-                const int n = min(kBatch, nrec - i0);
-                bool stop = false;
-                for (int r = 0; r < n && !stop; ++r) {
-                    const int i = i0 + r;
-                    const bool first = (i == 0) || kt == 0;
-                    const bool last = (i == nrec - 1) || kt == KT - 1;
-                    if (first && duse[dbuf] > 0) {
-                        if (!mbar_wait(bar_accempty + 8 * dbuf, (duse[dbuf] - 1) & 1, p.timeout_ns, p.status,
-                                       abort_flag)) {
-                            stop = true;
-                            break;
-                        }
-                        tc_fence_after();
-                    }
-                    const uint32_t d_t = tmem + kDCol0 + dbuf * NR;
-                    const uint32_t a_t = tmem + (i % NA) * kACols;
-                    const uint64_t bd = smem_desc_sw128(x_s + (i % S) * NR * 128);
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        tc_mma_ts(d_t, a_t + ks * 8, bd + (uint64_t)(ks * 2), idesc, (first && ks == 0) ? 0u : 1u);
-                    if (last) {
-                        tc_commit(bar_accfull + 8 * dbuf);
-                        ++duse[dbuf];
-                        if (p.d_bufs == 2) dbuf ^= 1;
-                    }
-                    last_i = i;
-                    if (++kt == KT) kt = 0;
-                }
-                // one commit frees the batch's A buffers, one its shared-memory slot
-                tc_commit(bar_afree + 8 * ((i0 / kBatch) % (NA / kBatch)));
-                tc_commit(bar_empty + 8 * ((i0 % S) / kBatch));
-                if (stop) *abort_flag = 1;
-            }
-            __syncwarp();
-            if (*abort_flag) break;
-        }
-        // tensor memory is released only after every issued MMA has finished
-        if (lane == 0 && last_i >= 0) {
-            int32_t no_abort = 0;
-            mbar_wait(bar_afree + 8 * ((last_i / kBatch) % (NA / kBatch)), (last_i / NA) & 1, p.timeout_ns, p.status,
-                      &no_abort);
         }
     } else if (warp < kEpiWarp0) {
         // --------------------------------------------------------------- decode
-        const int dw = warp - kDecodeWarp0;
-        const int grp = dw >> 2;
-        const int quarter = warp & 3;          // tensor-memory lanes this warp may touch
-        const int c = quarter * 32 + lane;     // output channel of this thread
-        const int dtid = dw * 32 + lane;       // 0..255
-        // shared caches: escape offsets/entries of the CTA's records, window bases
-        const int nt_span = (int)(nt_last - nt_first + 1);
-        const bool base_cached = nt_span <= p.base_tiles;
-        for (int i = dtid; i <= nrec; i += 256) esc_off_s[i] = __ldg(p.esc_off + rec_begin + i);
-        if (base_cached)
-            for (int i = dtid; i < nt_span * w12i::kTileN; i += 256)
-                base_s[i] = __ldg(p.base + nt_first * w12i::kTileN + i);
-        uint32_t dph = 0;
-        auto dec_sync = [&]() -> bool {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_dec);
-            const bool ok = mbar_wait(bar_dec, dph, p.timeout_ns, p.status, abort_flag);
-            dph ^= 1u;
-            return ok;
-        };
-        bool ok = dec_sync();
-        const int32_t e_lo = esc_off_s[0];
-        const bool esc_cached = (esc_off_s[nrec] - e_lo) <= p.esc_cap;
-        if (ok && esc_cached)
-            for (int i = dtid; i < esc_off_s[nrec] - e_lo; i += 256) esc_s[i] = __ldg(p.esc + e_lo + i);
-        ok = ok && dec_sync();
+        const int g = (warp - kGroupWarp0) >> 2;
+        const int wq = (warp - kGroupWarp0) & 3;     // warp within the group
+        const int quarter = warp & 3;                // tensor-memory lanes this warp may touch
+        const int c = quarter * 32 + lane;           // output channel of this thread
+        if (g < GR) {
+            const int dtid = g * 128 + wq * 32 + lane;
+            const int ndec = GR * 128;
+            // shared caches: escape offsets/entries of the CTA's records, window bases
+            const int nt_span = (int)(nt_last - nt_first + 1);
+            const bool base_cached = nt_span <= p.base_tiles;
+            for (int i = dtid; i <= nrec; i += ndec) esc_off_s[i] = __ldg(p.esc_off + rec_begin + i);
+            if (base_cached)
+                for (int i = dtid; i < nt_span * w12i::kTileN; i += ndec)
+                    base_s[i] = __ldg(p.base + nt_first * w12i::kTileN + i);
+            named_bar(kBarCaches, ndec);
+            const int32_t e_lo = esc_off_s[0];
+            const bool esc_cached = (esc_off_s[nrec] - e_lo) <= p.esc_cap;
+            if (esc_cached)
+                for (int i = dtid; i < esc_off_s[nrec] - e_lo; i += ndec) esc_s[i] = __ldg(p.esc + e_lo + i);
+            named_bar(kBarCaches, ndec);
 
-        int64_t nt = -1;
-        ChanConst cc{0, 0};
-        int kt = (int)(rec_begin - nt_first * KT) + grp;
-        int64_t ntc = nt_first;
-        while (kt >= KT) kt -= KT, ++ntc;
-        for (int i = grp; ok && i < nrec; i += 2) {
-            if (ntc != nt) {
-                nt = ntc;
-                const uint32_t b = base_cached ? base_s[(nt - nt_first) * w12i::kTileN + c]
-                                               : __ldg(p.base + nt * w12i::kTileN + c);
-                cc = chan_const(b);
+            const bool issuer = (wq == 0 && lane == 0);
+            const uint32_t idesc = idesc_bf16_f32(128, NR);
+            int64_t nt_cur = -1;
+            ChanConst cc{0, 0};
+            int tiles_g = 0, dcur = 0, last_i = -1;
+            for (int j = 0;; ++j) {
+                const int i = g + j * GR;
+                if (i >= nrec) break;
+                const int s = i % S;
+                const int64_t r = rec_begin + i;
+                const int64_t nt = r / KT;
+                const int kt = (int)(r - nt * KT);
+                const int ab = j % NAG;
+                bool ok = mbar_wait(bar_full + 8 * s, (i / S) & 1, p.timeout_ns, p.status, abort_flag);
+                if (ok && j >= NAG) {
+                    // the A buffer's previous record (i - GR * NAG) must have finished its MMAs
+                    const int ip = i - GR * NAG;
+                    ok = mbar_wait(bar_done + 8 * (ip % S), (ip / S) & 1, p.timeout_ns, p.status, abort_flag);
+                }
+                ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+                if (ok) {
+                    if (nt != nt_cur) {
+                        nt_cur = nt;
+                        const uint32_t b = base_cached ? base_s[(nt - nt_first) * w12i::kTileN + c]
+                                                       : __ldg(p.base + nt * w12i::kTileN + c);
+                        cc = chan_const(b);
+                    }
+                    const uint8_t *rb = smem + pl.rec + s * w12i::kRecBytes;
+                    uint4 v[4], nb[2];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) v[q] = *reinterpret_cast<const uint4 *>(rb + (q * 128 + c) * 16);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        nb[h] = *reinterpret_cast<const uint4 *>(rb + w12i::kViewBytes + (h * 128 + c) * 16);
+                    uint32_t a[32];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t vw[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+                        const uint4 n4 = nb[q >> 1];
+                        const uint32_t nw[4] = {n4.x, n4.y, n4.z, n4.w};
+#pragma unroll
+                        for (int w = 0; w < 4; ++w)
+                            decode_word(vw[w], nw[w] >> ((q & 1) * 4), cc, p.mul16, a[8 * q + w], a[8 * q + 4 + w]);
+                    }
+                    // escaped slots of this channel: the exact value replaces the filler
+                    const int32_t e0 = esc_off_s[i] - e_lo, e1 = esc_off_s[i + 1] - e_lo;
+                    for (int e = e0; e < e1; ++e) {
+                        const uint32_t en = esc_cached ? esc_s[e] : __ldg(p.esc + e_lo + e);
+                        const int nl = (en >> 22) & 0x7F;
+                        if ((nl >> 5) != quarter) continue;   // warp-uniform skip
+                        const int kl = (en >> 16) & 0x3F, col = kl >> 1;
+                        const uint32_t val = en & 0xFFFFu;
+                        const bool mine = nl == c, upper = kl & 1;
+#pragma unroll
+                        for (int w = 0; w < 32; ++w)
+                            if (mine && w == col)
+                                a[w] = upper ? ((a[w] & 0x0000FFFFu) | (val << 16)) : ((a[w] & 0xFFFF0000u) | val);
+                    }
+                    tmem_st_x32(tmem + ((uint32_t)(quarter * 32) << 16) + a_col(g, ab), a);
+                    tmem_st_wait();
+                    tc_fence_before();
+                }
+                // the group agrees to go on (all four quarters are in the A buffer) or to stop
+                if (!bar_and(kBarGroup0 + g, 128, ok)) break;
+                if (issuer) {
+                    tc_fence_after();
+                    const bool first = (i < GR) || (kt < GR);
+                    const bool last = (i + GR >= nrec) || (kt + GR >= KT);
+                    bool go = true;
+                    if (first) {
+                        dcur = tiles_g % DB;
+                        if (tiles_g >= DB)
+                            go = mbar_wait(bar_accempty + 8 * (g * 2 + dcur), ((tiles_g / DB) - 1) & 1, p.timeout_ns,
+                                           p.status, abort_flag);
+                        tc_fence_after();
+                    }
+                    if (go) {
+                        const uint32_t d_t = tmem + d_col(g, dcur), a_t = tmem + a_col(g, ab);
+                        const uint64_t bd = smem_desc_sw128(x_s + s * xb);
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            tc_mma_ts(d_t, a_t + ks * 8, bd + (uint64_t)(ks * 2), idesc, (first && ks == 0) ? 0u : 1u);
+                        tc_commit(bar_done + 8 * s);
+                        last_i = i;
+                        if (last) {
+                            tc_commit(bar_accfull + 8 * (g * 2 + dcur));
+                            ++tiles_g;
+                        }
+                    } else {
+                        *abort_flag = 1;
+                    }
+                }
             }
-            const int j = i / kRecsPerStage, ab = i % NA;
-            const int s = j % S;
-            if (!mbar_wait(bar_full + 8 * s, (j / S) & 1, p.timeout_ns, p.status, abort_flag)) break;
-            if (i >= NA && !mbar_wait(bar_afree + 8 * ((i / kBatch) % (NA / kBatch)), ((i / NA) - 1) & 1, p.timeout_ns,
-                                      p.status, abort_flag))
-                break;
-            const uint8_t *rb = smem + pl.rec + (s * kRecsPerStage + i % kRecsPerStage) * w12i::kRecBytes;
-            uint4 v[4], nb[2];
-#pragma unroll
-            for (int g = 0; g < 4; ++g) v[g] = *reinterpret_cast<const uint4 *>(rb + (g * 128 + c) * 16);
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-                nb[h] = *reinterpret_cast<const uint4 *>(rb + w12i::kViewBytes + (h * 128 + c) * 16);
-            uint32_t a[32];
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                const uint32_t vw[4] = {v[g].x, v[g].y, v[g].z, v[g].w};
-                const uint4 n4 = nb[g >> 1];
-                const uint32_t nw[4] = {n4.x, n4.y, n4.z, n4.w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    decode_word(vw[q], nw[q] >> ((g & 1) * 4), cc, p.mul16, a[8 * g + q], a[8 * g + 4 + q]);
+            // tensor memory is released only after this group's issued MMAs finished
+            if (issuer && last_i >= 0) {
+                int32_t no_abort = 0;
+                mbar_wait(bar_done + 8 * (last_i % S), (last_i / S) & 1, p.timeout_ns, p.status, &no_abort);
             }
-            // escaped slots of this channel: the exact value replaces the filler
-            const int32_t e0 = esc_off_s[i] - e_lo, e1 = esc_off_s[i + 1] - e_lo;
-            for (int e = e0; e < e1; ++e) {
-                const uint32_t en = esc_cached ? esc_s[e] : __ldg(p.esc + e_lo + e);
-                const int nl = (en >> 22) & 0x7F;
-                if ((nl >> 5) != quarter) continue;              // warp-uniform skip
-                const int kl = (en >> 16) & 0x3F, col = kl >> 1;
-                const uint32_t val = en & 0xFFFFu;
-                const bool mine = nl == c, upper = kl & 1;
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (mine && j == col)
-                        a[j] = upper ? ((a[j] & 0x0000FFFFu) | (val << 16)) : ((a[j] & 0xFFFF0000u) | val);
-            }
-            tmem_st_x32(tmem + ((uint32_t)(quarter * 32) << 16) + ab * kACols, a);
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(bar_afull + 8 * ab);
-                mbar_arrive(bar_empty + 8 * (s / kBatch));
-            }
-            kt += 2;
-            while (kt >= KT) kt -= KT, ++ntc;
         }
     } else {
         // ------------------------------------------------------------- epilogue
         const int quarter = warp & 3;
         const int c = quarter * 32 + lane;
-        const int etid = (warp - kEpiWarp0) * 32 + lane;   // 0..127
         const int ew = warp - kEpiWarp0;
+        const int etid = ew * 32 + lane;   // 0..127
         const int rows = p.R;
         float *red_v = reinterpret_cast<float *>(smem + pl.red);
         int32_t *red_i = reinterpret_cast<int32_t *>(smem + pl.red + 4 * NR * 4);
@@ -368,10 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
             if (lane == 0) mbar_arrive(bar_epi);
             const bool ok = mbar_wait(bar_epi, eph, p.timeout_ns, p.status, abort_flag);
             eph ^= 1u;
-            return ok;
+            return __all_sync(0xffffffffu, ok);
         };
-        int dbuf = 0;
-        uint32_t duse[2] = {0, 0};
+        int tg[kMaxGroups] = {0, 0};
         // write (or reduce, for the LM head) 32 rows r0..r0+31 of this channel
         auto emit_rows = [&](int64_t nt, int r0, const float (&v)[32]) {
             if (p.mode == w12i::kModeLinear) {
@@ -411,20 +386,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
             return epi_sync();
         };
         for (int64_t nt = nt_first; nt <= nt_last; ++nt) {
-            if (!mbar_wait(bar_accfull + 8 * dbuf, duse[dbuf] & 1, p.timeout_ns, p.status, abort_flag)) break;
-            tc_fence_after();
             const int64_t t0 = nt * KT, t1 = t0 + KT;
+            // this CTA's records of the tile, [ia, ib) in CTA-local numbering
+            const int ia = (int)((rec_begin > t0 ? rec_begin : t0) - rec_begin);
+            const int ib = (int)((rec_end < t1 ? rec_end : t1) - rec_begin);
+            bool part[kMaxGroups];
+            int dsel[kMaxGroups];
+            bool ok = true;
+#pragma unroll
+            for (int g = 0; g < kMaxGroups; ++g) {
+                part[g] = g < GR && (ib - ia >= GR || ia % GR == g);
+                dsel[g] = tg[g] % DB;
+                if (part[g] && ok)
+                    ok = mbar_wait(bar_accfull + 8 * (g * 2 + dsel[g]), (tg[g] / DB) & 1, p.timeout_ns, p.status,
+                                   abort_flag);
+            }
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
             const bool owned = rec_begin <= t0 && rec_end >= t1;
             const int slot = (nt == nt_first) ? 0 : 1;
             float *mine = p.partial + ((int64_t)(cta * 2 + slot) * NR) * w12i::kTileN;
-            const uint32_t d_t = tmem + ((uint32_t)(quarter * 32) << 16) + kDCol0 + dbuf * NR;
+            const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
             for (int r0 = 0; r0 < NR; r0 += 32) {
-                uint32_t raw[32];
-                tmem_ld_x32(d_t + r0, raw);
-                tmem_ld_wait();
                 float v[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]);
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+#pragma unroll
+                for (int g = 0; g < kMaxGroups; ++g) {
+                    if (!part[g]) continue;
+                    uint32_t raw[32];
+                    tmem_ld_x32(lane_base + d_col(g, dsel[g]) + r0, raw);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] += __uint_as_float(raw[j]);
+                }
                 if (owned) {
                     emit_rows(nt, r0, v);
                 } else {
@@ -435,9 +430,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_accempty + 8 * dbuf);
-            ++duse[dbuf];
-            if (p.d_bufs == 2) dbuf ^= 1;
+#pragma unroll
+            for (int g = 0; g < kMaxGroups; ++g)
+                if (part[g]) {
+                    if (lane == 0) mbar_arrive(bar_accempty + 8 * (g * 2 + dsel[g]));
+                    ++tg[g];
+                }
             if (owned) {
                 if (!head_finish(nt)) break;
                 continue;
@@ -472,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+    if (warp == kProducerWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -496,6 +494,21 @@ EncodeTiledFn encode_fn_tc()
 }  // namespace
 
 namespace w12i {
+
+// Tensor-memory plan for MMA width nr: groups x A buffers x 32 columns, then
+// groups x accumulators x nr columns, within 512 columns.  More groups and
+// more buffers first.
+bool tc_tmem_plan(int nr, int *groups, int *a_bufs, int *d_bufs)
+{
+    static const int cand[][3] = {{2, 4, 2}, {2, 2, 2}, {2, 2, 1}, {1, 4, 2}, {1, 4, 1}, {1, 2, 1}};
+    for (const auto &c : cand) {
+        if (c[0] * c[1] * 32 + c[0] * c[2] * nr <= (int)kTmemCols) {
+            *groups = c[0], *a_bufs = c[1], *d_bufs = c[2];
+            return true;
+        }
+    }
+    return false;
+}
 
 int launch_gemm_tc(const GemmArgs &a, void *stream)
 {
@@ -524,10 +537,7 @@ int launch_gemm_tc(const GemmArgs &a, void *stream)
     p.R = a.R;
     p.mode = a.mode;
     p.nr = nr;
-    // 8 A buffers (four records of slack per decode group) while the two
-    // accumulators still fit next to them; otherwise 4
-    p.a_bufs = (8 * kACols + 2 * nr <= (int)kTmemCols) ? 8 : 4;
-    p.d_bufs = (p.a_bufs * kACols + 2 * nr <= (int)kTmemCols) ? 2 : 1;
+    if (!tc_tmem_plan(nr, &p.groups, &p.a_bufs, &p.d_bufs)) return (int)cudaErrorInvalidValue;
     p.y = a.y;
     p.ldy = a.w.n;
     p.s1_val = a.stage1_val;
@@ -542,8 +552,14 @@ int launch_gemm_tc(const GemmArgs &a, void *stream)
     p.esc_cap = 2048;
     p.base_tiles = std::min<int>(64, (int)(p.max_recs / a.w.k_tiles + 2));
     const int budget = 227 * 1024;
-    int stages = 16;   // a multiple of kBatch, as many as fit
-    while (stages > kBatch && plan(stages, nr, p.max_recs, p.esc_cap, p.base_tiles).total > budget) stages -= kBatch;
+    // stages: as many as fit (at most 16), a multiple of the group count and
+    // never fewer than the A buffers in flight.  Then record i - S of a stage
+    // belongs to the same group as record i, so a group never sees the shared
+    // "done" barrier of a stage run more than one phase ahead of its wait.
+    int stages = 16;
+    while (stages - p.groups >= p.groups * p.a_bufs &&
+           plan(stages, nr, p.max_recs, p.esc_cap, p.base_tiles).total > budget)
+        stages -= p.groups;
     p.stages = stages;
     const int smem = plan(stages, nr, p.max_recs, p.esc_cap, p.base_tiles).total;
     if (smem > budget) return (int)cudaErrorInvalidConfiguration;
