@@ -7,13 +7,17 @@
 // 1.1: greedy verification keeps the drafts equal to the target's argmax and
 // appends that argmax as a bonus.
 //
-// Tree build, one CTA.  With every edge log-probability <= 0 a child never
-// outranks its parent, so the budget's best nodes at depth d are among the
-// best (budget - n_req) children of the nodes kept at depth d-1.  The kernel
-// keeps exactly those per depth (radix select on the score, ties by
-// (request, path) which is the storage order), then takes the best `R` of
-// all kept nodes (ties by depth, then storage order) and sorts them into
-// request-grouped, best-first rows.
+// Tree build, one CTA.  Order of nodes: score descending, then depth, then
+// request, then path (candidate indices from the root).  Every edge
+// log-probability is <= 0, so a child comes after its parent, and a node's
+// children, ranked by their own FP32 score and then candidate index, come in
+// that order too.  Best-first selection therefore only ever needs, for each
+// selected node, its best child not yet taken: the next node of the tree is
+// the best of those "frontier" children.  One warp runs the R selections
+// (each lane keeps the best frontier child of the nodes it owns, a warp
+// argmax picks the winner, the winner's parent advances to its next child
+// and the new node's children are ranked by 16 lanes); the other warps check
+// and stage the lattice before, and write the request-grouped rows after.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -25,15 +29,11 @@ using namespace w12d;
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr uint32_t kInvalid = 0xFFFFFFFFu;
+constexpr int kCap = w12i::kMaxBudget;   // selected nodes
 
 struct TreeParams {
     int32_t n_req, p_max, n_cand, conditional, budget, R;
-    int32_t cand_shift;      // log2(n_cand) when n_cand is a power of two, else -1
-    int32_t stage_lattice;   // the lattice (log-probs + tokens) is copied to shared memory
-    // shared-memory carve-up (byte offsets), sized on the host
-    int32_t off_keys, off_score, off_token, off_parent, off_req, off_meta, off_sort, off_lp, off_lt;
+    int32_t stage_lattice;   // non-conditional log-probs and tokens copied to shared memory
     const int32_t *root_tok;
     const int32_t *cand_tok;
     const float *cand_logp;
@@ -44,287 +44,238 @@ struct TreeParams {
     uint8_t p_r[w12i::kMaxBudget];
 };
 
-struct Hdr {
+// Selected nodes, in selection order, plus the frontier child of each.
+struct Nodes {
+    unsigned long long key1[kCap];     // frontier child: ordered score << 32 | ~(depth << 16 | request); 0 = none
+    unsigned long long key2[kCap];     // frontier child: ~path
+    unsigned long long path[kCap];     // candidate index of depth d at bits 64 - 4d
+    unsigned long long perm[kCap];     // children ranked best first, 4 bits each
+    float score[kCap];
+    uint32_t dr[kCap];                 // depth << 16 | request
+    int32_t tok[kCap];
+    int32_t row[kCap];
+    int16_t par[kCap];
+    uint8_t rank[kCap];
+    uint8_t next[kCap];                // rank position of the frontier child
+    uint8_t nch[kCap];                 // children available (0 at the depth limit)
     uint8_t p_r[w12i::kMaxBudget];
-    uint32_t hist[256];
-    int32_t red[kWarps];
-    int32_t bcast[2];
-    int32_t lvl_begin[w12i::kMaxPositions + 2];
-    int32_t lvl_end[w12i::kMaxPositions + 2];
+    int32_t n_sel;
+    int32_t bad;
 };
 
-// ascending key == descending score (a total order on non-NaN floats)
-__device__ __forceinline__ uint32_t score_key(float s)
+// Order-preserving map of a finite float to an unsigned integer (larger
+// float, larger integer; -0 and +0 map alike, as they compare equal).
+__device__ __forceinline__ uint32_t ord_score(float s)
 {
-    const uint32_t u = __float_as_uint(s);
-    const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-    return ~ord;
+    const uint32_t u = __float_as_uint(__fadd_rn(s, 0.0f));
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
-
-__device__ __forceinline__ int warp_incl_scan(int x)
+__device__ __forceinline__ float unord_score(uint32_t o)
 {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    return x;
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
 }
-
-// block-wide sum (2 barriers)
-__device__ int block_sum(int v, Hdr &h)
+// the tree order as one comparison: larger (key1, key2) comes first
+__device__ __forceinline__ unsigned long long make_key1(float s, uint32_t dr)
 {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if ((threadIdx.x & 31) == 0) h.red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    int t = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) t += h.red[w];
-    __syncthreads();
-    return t;
-}
-
-// block-wide exclusive scan of one int per thread (2 barriers)
-__device__ int block_excl_scan(int v, Hdr &h)
-{
-    const int incl = warp_incl_scan(v);
-    if ((threadIdx.x & 31) == 31) h.red[threadIdx.x >> 5] = incl;
-    __syncthreads();
-    int before = 0;
-    for (int w = 0; w < (int)(threadIdx.x >> 5); ++w) before += h.red[w];
-    __syncthreads();
-    return before + incl - v;
-}
-
-// The K smallest of keys[0..n) (1 <= K <= n): threshold tau, and how many of
-// the keys equal to tau are taken (the lowest-index ones).  Expects h.hist
-// zeroed and leaves it zeroed.  2 barriers per 8-bit pass.
-__device__ void radix_select(const uint32_t *keys, int n, int K, uint32_t &tau, int &take_eq, Hdr &h)
-{
-    uint32_t prefix = 0, mask = 0;
-    int krem = K;
-    const int rounds = (n + kThreads - 1) / kThreads;   // uniform trip count: whole warps vote
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int it = 0; it < rounds; ++it) {
-            const int i = it * kThreads + threadIdx.x;
-            const uint32_t k = i < n ? keys[i] : 0u;
-            const bool counted = i < n && (k & mask) == prefix;
-            const uint32_t bin = counted ? ((k >> shift) & 255u) : 256u;
-            // one atomic per distinct bin per warp: scores of one depth share
-            // their top bits, so per-key atomics would serialise on one bin
-            const unsigned peers = __match_any_sync(0xffffffffu, bin);
-            if (counted && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h.hist[bin], (uint32_t)__popc(peers));
-        }
-        __syncthreads();
-        if (threadIdx.x < 32) {
-            const int lane = threadIdx.x;
-            int c[8], sum = 0;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                c[q] = (int)h.hist[lane * 8 + q];
-                h.hist[lane * 8 + q] = 0;
-                sum += c[q];
-            }
-            const int incl = warp_incl_scan(sum);
-            const int before = incl - sum;
-            if (before < krem && incl >= krem) {
-                int b = before;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    if (b + c[q] >= krem) {
-                        h.bcast[0] = lane * 8 + q;
-                        h.bcast[1] = b;
-                        break;
-                    }
-                    b += c[q];
-                }
-            }
-        }
-        __syncthreads();
-        prefix |= (uint32_t)h.bcast[0] << shift;
-        mask |= 255u << shift;
-        krem -= h.bcast[1];
-    }
-    tau = prefix;
-    take_eq = krem;
-}
-
-// Walk keys[0..n) in index order and call emit(i, out) for every selected
-// key: key < tau, or key == tau among the first take_eq such keys.  `out`
-// numbers the selected keys in index order.  Each thread owns a contiguous
-// chunk; one packed (less, equal) scan gives every position (2 barriers).
-template <class Emit>
-__device__ int select_ordered(const uint32_t *keys, int n, uint32_t tau, int take_eq, Hdr &h, Emit emit)
-{
-    const int chunk = (n + kThreads - 1) / kThreads;
-    const int lo = min(n, (int)threadIdx.x * chunk), hi = min(n, lo + chunk);
-    int lt = 0, eq = 0;
-    for (int i = lo; i < hi; ++i) {
-        const uint32_t k = keys[i];
-        lt += k < tau;
-        eq += k == tau;
-    }
-    const int packed_before = block_excl_scan((lt << 16) | eq, h);
-    int lt_before = packed_before >> 16, eq_before = packed_before & 0xFFFF;
-    for (int i = lo; i < hi; ++i) {
-        const uint32_t k = keys[i];
-        if (k < tau) {
-            emit(i, lt_before + min(eq_before, take_eq));
-            ++lt_before;
-        } else if (k == tau) {
-            if (eq_before < take_eq) emit(i, lt_before + eq_before);
-            ++eq_before;
-        }
-    }
-    int total_lt = 0, total_eq = 0;
-    if (threadIdx.x == kThreads - 1) h.bcast[0] = lt_before, h.bcast[1] = eq_before;
-    __syncthreads();
-    total_lt = h.bcast[0];
-    total_eq = h.bcast[1];
-    __syncthreads();
-    return total_lt + min(total_eq, take_eq);
+    return ((unsigned long long)ord_score(s) << 32) | (unsigned long long)(~dr);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) k_tree_build(const TreeParams p)
 {
     extern __shared__ __align__(16) uint8_t smem[];
-    Hdr &h = *reinterpret_cast<Hdr *>(smem);
-    uint32_t *keys = reinterpret_cast<uint32_t *>(smem + p.off_keys);
-    float *u_score = reinterpret_cast<float *>(smem + p.off_score);
-    int32_t *u_token = reinterpret_cast<int32_t *>(smem + p.off_token);
-    int16_t *u_parent = reinterpret_cast<int16_t *>(smem + p.off_parent);
-    int16_t *u_req = reinterpret_cast<int16_t *>(smem + p.off_req);
-    uint16_t *u_meta = reinterpret_cast<uint16_t *>(smem + p.off_meta);   // depth << 8 | rank
-    unsigned long long *sortbuf = reinterpret_cast<unsigned long long *>(smem + p.off_sort);
-    float *lp_s = reinterpret_cast<float *>(smem + p.off_lp);
-    int32_t *lt_s = reinterpret_cast<int32_t *>(smem + p.off_lt);
-    const int tid = threadIdx.x;
-    const int K = p.budget - p.n_req;   // non-root rows available
+    Nodes &n = *reinterpret_cast<Nodes *>(smem);
+    float *lp_s = reinterpret_cast<float *>(smem + sizeof(Nodes));
+    const int32_t lat = p.n_req * p.p_max * 16;
+    int32_t *lt_s = reinterpret_cast<int32_t *>(smem + sizeof(Nodes) + 4 * (p.stage_lattice ? lat : 0));
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int NC = p.n_cand, PM = p.p_max;
 
     pdl_wait();
-    for (int i = tid; i < 256; i += kThreads) h.hist[i] = 0;
-    for (int r = tid; r < p.n_req; r += kThreads) h.p_r[r] = p.p_r[r];
-    if (p.stage_lattice) {
-        const int n = p.n_req * p.p_max * 16;
-        for (int i = tid; i < n; i += kThreads) {
+    if (tid == 0) n.bad = 0;
+    for (int r = tid; r < p.n_req; r += kThreads) n.p_r[r] = p.p_r[r];
+    __syncthreads();
+    // every log-probability a node could use must be finite and <= 0
+    {
+        bool bad = false;
+        const int rows = p.conditional ? NC : 1;
+        const int per_req = PM * 16 * (p.conditional ? 16 : 1);
+        for (int64_t i = tid; i < (int64_t)p.n_req * per_req; i += kThreads) {
+            const int r = (int)(i / per_req), rem = (int)(i - (int64_t)r * per_req);
+            const int d = p.conditional ? rem / 256 : rem / 16;
+            const int pc = p.conditional ? (rem / 16) & 15 : 0, j = rem & 15;
+            if (d < n.p_r[r] && pc < rows && j < NC) {
+                const float v = p.cand_logp[i];
+                if (!(v <= 0.f) || isinf(v)) bad = true;
+            }
+        }
+        if (bad) n.bad = 1;
+    }
+    if (p.stage_lattice)
+        for (int i = tid; i < lat; i += kThreads) {
             lp_s[i] = p.cand_logp[i];
             lt_s[i] = p.cand_tok[i];
         }
-    }
-    // depth 0: the roots, in request order
-    for (int r = tid; r < p.n_req; r += kThreads) {
-        u_score[r] = 0.f;
-        u_parent[r] = -1;
-        u_req[r] = (int16_t)r;
-        u_token[r] = p.root_tok[r];
-        u_meta[r] = 0;
-    }
-    if (tid == 0) h.lvl_begin[0] = 0, h.lvl_end[0] = p.n_req;
     __syncthreads();
+    if (n.bad) {
+        if (tid == 0) atomicCAS(p.status, 0, (int32_t)W12_E_INVAL);
+        return;
+    }
 
-    auto edge = [&](int r, int d, int prank, int j) -> float {
-        const int64_t pos = (int64_t)r * p.p_max + (d - 1);
+    auto edge = [&](int r, int d, int prank, int j) -> float {   // d = child depth (1-based position)
+        const int64_t pos = (int64_t)r * PM + (d - 1);
         if (p.conditional) return p.cand_logp[(pos * 16 + prank) * 16 + j];
         return p.stage_lattice ? lp_s[pos * 16 + j] : p.cand_logp[pos * 16 + j];
     };
     auto cand_token = [&](int r, int d, int j) -> int32_t {
-        const int64_t pos = (int64_t)r * p.p_max + (d - 1);
+        const int64_t pos = (int64_t)r * PM + (d - 1);
         return p.stage_lattice ? lt_s[pos * 16 + j] : p.cand_tok[pos * 16 + j];
     };
-    auto split = [&](int ci, int &par_local, int &j) {
-        if (p.cand_shift >= 0) {
-            par_local = ci >> p.cand_shift;
-            j = ci & ((1 << p.cand_shift) - 1);
-        } else {
-            par_local = ci / p.n_cand;
-            j = ci - par_local * p.n_cand;
-        }
-    };
 
-    int nU = p.n_req;
-    bool bad_input = false;
-    for (int d = 1; d <= p.p_max && K > 0; ++d) {
-        const int pb = h.lvl_begin[d - 1], pe = h.lvl_end[d - 1];
-        const int ncand = (pe - pb) * p.n_cand;
-        if (ncand == 0) break;
-        int valid = 0;
-        for (int ci = tid; ci < ncand; ci += kThreads) {
-            int pl, j;
-            split(ci, pl, j);
-            const int par = pb + pl;
-            const int r = u_req[par];
-            uint32_t key = kInvalid;
-            if (d <= h.p_r[r]) {
-                const float e = edge(r, d, u_meta[par] & 0xFF, j);
-                if (!(e <= 0.f) || isinf(e)) bad_input = true;
-                key = score_key(__fadd_rn(u_score[par], e));
-                ++valid;
+    if (tid < 32) {
+        // ---------------------------------------------------- best-first (warp 0)
+        // Node x (score sx, dr, path, rank jx) was just selected: rank its
+        // children by FP32 score then index (all lanes) and store its fields.
+        // Returns the key of its best child (key1 = 0 when it has none).
+        auto expand = [&](int x, float sx, uint32_t dr, unsigned long long path, int jx, int par, int32_t tok,
+                          unsigned long long &k1, unsigned long long &k2) {
+            const int d = (int)(dr >> 16), r = (int)(dr & 0xFFFF);
+            const bool has = d < n.p_r[r];
+            float cs = -INFINITY;
+            if (has && lane < NC) cs = __fadd_rn(sx, edge(r, d + 1, jx, lane));
+            // rank = children before this one; branch-free so the warp stays converged
+            int pos = 0;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float o = __shfl_sync(0xffffffffu, cs, k);
+                pos += (int)((k < NC) & ((o > cs) | ((o == cs) & (k < lane))));
             }
-            keys[ci] = key;
+            const unsigned long long mine = (has && lane < NC) ? ((unsigned long long)lane << (4 * pos)) : 0ull;
+            const uint32_t lo = __reduce_or_sync(0xffffffffu, (uint32_t)mine);
+            const uint32_t hi = __reduce_or_sync(0xffffffffu, (uint32_t)(mine >> 32));
+            const unsigned long long perm = ((unsigned long long)hi << 32) | lo;
+            const int j0 = (int)(perm & 15ull);
+            const float best = __shfl_sync(0xffffffffu, cs, j0);
+            k1 = has ? make_key1(best, dr + (1u << 16)) : 0ull;
+            k2 = has ? ~(path | ((unsigned long long)j0 << (64 - 4 * (d + 1)))) : 0ull;
+            if (lane == 0) {
+                n.score[x] = sx;
+                n.dr[x] = dr;
+                n.path[x] = path;
+                n.rank[x] = (uint8_t)jx;
+                n.par[x] = (int16_t)par;
+                n.tok[x] = tok;
+                n.perm[x] = perm;
+                n.next[x] = 0;
+                n.nch[x] = has ? (uint8_t)NC : 0;
+                n.key1[x] = k1;
+                n.key2[x] = k2;
+            }
+        };
+        // lane-local best frontier child over the nodes this lane owns (x % 32 == lane)
+        unsigned long long b1 = 0, b2 = 0;
+        int bx = -1;
+        for (int r = 0; r < p.n_req; ++r) {   // roots, in request order
+            unsigned long long k1, k2;
+            expand(r, 0.f, (uint32_t)r, 0ull, 0, -1, p.root_tok[r], k1, k2);
+            if (lane == (r & 31) && k1 != 0 && (k1 > b1 || (k1 == b1 && k2 > b2))) b1 = k1, b2 = k2, bx = r;
         }
-        const int nvalid = block_sum(valid, h);
-        if (nvalid == 0) break;
-        uint32_t tau = kInvalid;   // with take_eq = 0: every valid key is taken
-        int take = 0;
-        if (nvalid > K) radix_select(keys, ncand, K, tau, take, h);
-        const int base = nU;
-        const int nsel = select_ordered(keys, ncand, tau, take, h, [&](int ci, int out) {
-            int pl, j;
-            split(ci, pl, j);
-            const int par = pb + pl;
-            const int r = u_req[par];
-            const int u = base + out;
-            u_score[u] = __fadd_rn(u_score[par], edge(r, d, u_meta[par] & 0xFF, j));
-            u_parent[u] = (int16_t)par;
-            u_req[u] = (int16_t)r;
-            u_token[u] = cand_token(r, d, j);
-            u_meta[u] = (uint16_t)((d << 8) | j);
-        });
-        nU += nsel;
-        if (tid == 0) h.lvl_begin[d] = base, h.lvl_end[d] = nU;
-        __syncthreads();
+        __syncwarp();
+        int t = p.n_req;
+        const int R = min(p.R, kCap);
+        for (; t < R; ++t) {
+            // warp argmax of the lane bests, most significant word first
+            const uint32_t h1 = (uint32_t)(b1 >> 32), l1 = (uint32_t)b1, h2 = (uint32_t)(b2 >> 32), l2 = (uint32_t)b2;
+            const uint32_t M1 = __reduce_max_sync(0xffffffffu, h1);
+            if (M1 == 0) break;   // every node of the lattice is taken
+            bool m = h1 == M1;
+            const uint32_t M2 = __reduce_max_sync(0xffffffffu, m ? l1 : 0u);
+            m = m && l1 == M2;
+            const uint32_t M3 = __reduce_max_sync(0xffffffffu, m ? h2 : 0u);
+            m = m && h2 == M3;
+            const uint32_t M4 = __reduce_max_sync(0xffffffffu, m ? l2 : 0u);
+            m = m && l2 == M4;
+            const int wl = __ffs(__ballot_sync(0xffffffffu, m)) - 1;
+            const int wx = __shfl_sync(0xffffffffu, bx, wl);
+            // node t = the frontier child of wx
+            const float st = unord_score(M1);
+            const uint32_t drt = ~M2;
+            const unsigned long long patht = ~(((unsigned long long)M3 << 32) | M4);
+            const int dt = (int)(drt >> 16);
+            const int j = (int)((patht >> (64 - 4 * dt)) & 15ull);
+            const int32_t tok = cand_token((int)(drt & 0xFFFF), dt, j);
+            // the parent moves on to its next child: every lane computes its new
+            // key from broadcast loads, issued before the new node's stores so
+            // that both chains overlap
+            const int nx = n.next[wx] + 1;
+            const unsigned long long pperm = n.perm[wx], ppath = n.path[wx];
+            const uint32_t pdr = n.dr[wx];
+            const float psc = n.score[wx];
+            const int prk = n.rank[wx], pnch = n.nch[wx];
+            const int pdc = (int)(pdr >> 16) + 1;
+            const int j2 = (int)((pperm >> (4 * (nx & 15))) & 15ull);
+            const bool more = nx < pnch;
+            const float pe = more ? edge((int)(pdr & 0xFFFF), pdc, prk, j2) : 0.f;
+            unsigned long long k1, k2;
+            expand(t, st, drt, patht, j, wx, tok, k1, k2);
+            // the parent's owner lane rescans
+            {
+                const unsigned long long p1 = more ? make_key1(__fadd_rn(psc, pe), pdr + (1u << 16)) : 0ull;
+                const unsigned long long p2 = more ? ~(ppath | ((unsigned long long)j2 << (64 - 4 * pdc))) : 0ull;
+                __syncwarp();
+                if (lane == 0) {
+                    n.next[wx] = (uint8_t)nx;
+                    n.key1[wx] = p1;
+                    n.key2[wx] = p2;
+                }
+                __syncwarp();
+                if (lane == wl) {
+                    b1 = 0, b2 = 0, bx = -1;
+                    for (int x = lane; x < t; x += 32) {
+                        const unsigned long long q1 = n.key1[x], q2 = n.key2[x];
+                        const bool better = (q1 > b1) | ((q1 == b1) & (q2 > b2));
+                        b1 = better ? q1 : b1;
+                        b2 = better ? q2 : b2;
+                        bx = better ? x : bx;
+                    }
+                    if (b1 == 0) bx = -1;
+                }
+            }
+            {
+                const bool better = (lane == (t & 31)) & (k1 != 0) & ((k1 > b1) | ((k1 == b1) & (k2 > b2)));
+                b1 = better ? k1 : b1;
+                b2 = better ? k2 : b2;
+                bx = better ? t : bx;
+            }
+            __syncwarp();
+        }
+        if (lane == 0) n.n_sel = t;
     }
-    if (bad_input) atomicCAS(p.status, 0, (int32_t)W12_E_INVAL);
+    __syncthreads();
 
-    // the best R of every kept node: score desc, then storage position
-    // (depth, request, path)
-    for (int i = tid; i < nU; i += kThreads) keys[i] = score_key(u_score[i]);
-    __syncthreads();
-    const int R = min(p.R, nU);
-    uint32_t tau = kInvalid;
-    int take = 0;
-    if (R < nU) radix_select(keys, nU, R, tau, take, h);
-    select_ordered(keys, nU, tau, take, h, [&](int u, int out) {
-        sortbuf[out] = ((unsigned long long)u_req[u] << 46) | ((unsigned long long)keys[u] << 14) |
-                       (unsigned long long)u;
-    });
-    // output row of each selected node = its rank under (request, score desc,
-    // storage position); then storage position -> row (reusing the keys)
-    int32_t *row_of = reinterpret_cast<int32_t *>(keys);
+    // ------------------------------------------- rows: grouped by request, selection order inside
+    const int R = n.n_sel;
     for (int i = tid; i < R; i += kThreads) {
-        const unsigned long long mine = sortbuf[i];
-        int rank_i = 0;
-        for (int j = 0; j < R; ++j) rank_i += sortbuf[j] < mine;
-        row_of[mine & 0x3FFFull] = rank_i;
+        const int r = (int)(n.dr[i] & 0xFFFF);
+        int row = 0;
+        for (int k = 0; k < R; ++k) {
+            const int rk = (int)(n.dr[k] & 0xFFFF);
+            row += rk < r || (rk == r && k < i);
+        }
+        n.row[i] = row;
     }
     __syncthreads();
     for (int i = tid; i < R; i += kThreads) {
-        const int u = (int)(sortbuf[i] & 0x3FFFull);
-        const int row = row_of[u];
-        const int pu = u_parent[u];
-        p.parent[row] = pu < 0 ? -1 : row_of[pu];
-        p.token[row] = u_token[u];
-        p.req[row] = u_req[u];
-        p.score[row] = u_score[u];
-        p.depth[row] = (uint8_t)(u_meta[u] >> 8);
-        p.rank[row] = (uint8_t)(u_meta[u] & 0xFF);
+        const int row = n.row[i];
+        p.parent[row] = n.par[i] < 0 ? -1 : n.row[n.par[i]];
+        p.token[row] = n.tok[i];
+        p.req[row] = (int32_t)(n.dr[i] & 0xFFFF);
+        p.score[row] = n.score[i];
+        p.depth[row] = (uint8_t)(n.dr[i] >> 16);
+        p.rank[row] = n.rank[i];
     }
-    // request row offsets: rows before request r = selected nodes of requests < r
     for (int r = tid; r <= p.n_req; r += kThreads) {
         int c = 0;
-        for (int j = 0; j < R; ++j) c += (int)(sortbuf[j] >> 46) < r;
+        for (int k = 0; k < R; ++k) c += (int)(n.dr[k] & 0xFFFF) < r;
         p.req_row_off[r] = c;
     }
     pdl_launch_dependents();
@@ -386,6 +337,7 @@ size_t tree_ws_bytes(int32_t n_req)
 
 int launch_tree_build(const TreeArgs &a, void *stream)
 {
+    if (a.n_req > kCap || a.budget > kCap || a.R > kCap) return (int)cudaErrorInvalidValue;
     TreeParams p{};
     p.n_req = a.n_req;
     p.p_max = a.p_max;
@@ -393,9 +345,6 @@ int launch_tree_build(const TreeArgs &a, void *stream)
     p.conditional = a.conditional;
     p.budget = a.budget;
     p.R = a.R;
-    p.cand_shift = -1;
-    for (int sft = 0; sft <= 4; ++sft)
-        if (a.n_cand == (1 << sft)) p.cand_shift = sft;
     p.root_tok = a.root_tok;
     p.cand_tok = a.cand_tok;
     p.cand_logp = a.cand_logp;
@@ -408,27 +357,11 @@ int launch_tree_build(const TreeArgs &a, void *stream)
     p.score = a.score;
     p.status = a.status;
     for (int r = 0; r < a.n_req; ++r) p.p_r[r] = (uint8_t)a.p_r_host[r];
-    // capacities: kept nodes of all depths, candidates of one depth, rows
-    const int K = a.budget - a.n_req;
-    const int umax = a.n_req + a.p_max * std::max(K, 0);
-    const int cmax = std::max(a.n_req, K) * a.n_cand;
-    const int kcap = std::max(umax, cmax);
-    auto up = [](int x) { return (x + 15) & ~15; };
-    int o = up((int)sizeof(Hdr));
-    p.off_keys = o, o = up(o + 4 * kcap);
-    p.off_score = o, o = up(o + 4 * umax);
-    p.off_token = o, o = up(o + 4 * umax);
-    p.off_parent = o, o = up(o + 2 * umax);
-    p.off_req = o, o = up(o + 2 * umax);
-    p.off_meta = o, o = up(o + 2 * umax);
-    p.off_sort = o, o = up(o + 8 * std::max(a.R, 1));
     const int lat = a.n_req * a.p_max * 16;
     const int limit = 227 * 1024;
+    int o = (int)sizeof(Nodes);
     p.stage_lattice = (!a.conditional && o + 8 * lat <= limit) ? 1 : 0;
-    p.off_lp = o;
-    p.off_lt = o + 4 * lat;
     if (p.stage_lattice) o += 8 * lat;
-    if (o > limit) return (int)cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(k_tree_build, cudaFuncAttributeMaxDynamicSharedMemorySize, o);
     if (e != cudaSuccess) return (int)e;
     k_tree_build<<<1, kThreads, o, static_cast<cudaStream_t>(stream)>>>(p);
