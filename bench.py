@@ -181,18 +181,30 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 class Workload:
-    def __init__(self, name, rows, device, seed=0):
+    def __init__(self, name, rows, device, seed=0, share=None, one_request=False):
+        """`share`: another Workload of the same name whose packed device
+        weights are reused (only the tree, its rows and the activations are
+        rebuilt for the new node budget).  `one_request`: a single request
+        drafting 16 positions (the rows of one best-first tree)."""
         import torch
         import speculative_decoding_tree_w12_gb300 as w12
         from speculative_decoding_tree_w12_gb300 import synth
 
         self.w12, self.torch, self.synth = w12, torch, synth
         w = synth.WORKLOADS[name]
+        if one_request:
+            w = synth.scaled(w, n_req=1, positions=(16,))
         if rows:
             w = synth.scaled(w, budget=int(rows))
         self.wl, self.name, self.device = w, name, device
         t0 = time.time()
         self.lat = synth.lattice(w, seed)
+        if share is not None:
+            self.lin_bits, self.lin, self.lin_hp = share.lin_bits, share.lin, share.lin_hp
+            self.head_bits, self.head_hp, self.head = share.head_bits, share.head_hp, share.head
+            self.head_n2 = share.head_n2
+            self._rows(seed)
+            return
         # weights: generate, pack on the host (library packer, self-checked), upload
         self.lin_bits, self.lin = [], []
         distinct = {}
@@ -214,6 +226,10 @@ class Workload:
         self.head = w12.DeviceWeight(self.head_hp, device)
         self.lin_hp = [distinct[(0, i)][1] for i in range(len(w.linears))]
         log(f"[bench] weights generated and packed in {time.time() - t0:.1f}s")
+        self._rows(seed)
+
+    def _rows(self, seed):
+        torch, w12, synth, w, device = self.torch, self.w12, self.synth, self.wl, self.device
         # tree (GPU), then the toy target's hidden rows for that tree
         self.dlat = w12.DeviceLattice(self.lat, device)
         max_n = max(n for n, _ in w.linears)
@@ -222,7 +238,10 @@ class Workload:
         torch.cuda.synchronize()
         self.R = self.tree.R
         th = self.tree.host()
-        self.h_bits = synth.hidden_rows(th["req"], th["parent"], th["token"], self.lat.truth, self.head_bits, seed)
+        if getattr(self, "head_n2", None) is None:
+            self.head_n2 = synth.head_norms(self.head_bits)
+        self.h_bits = synth.hidden_rows(th["req"], th["parent"], th["token"], self.lat.truth, self.head_bits, seed,
+                                        head_norm2=self.head_n2)
         self.x_bits = [synth.activations(self.R, k, seed, synth.STREAM_X + i) for i, (n, k) in enumerate(w.linears)]
         dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
         self.h = dev(self.h_bits)
@@ -382,6 +401,48 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------
+# step time vs tree rows
+# ---------------------------------------------------------------------------
+
+def rows_sweep(base: "Workload", budgets, K: int, W: int, device):
+    """Step time and W12 GB/s of the graph-captured step for each node budget
+    of a single-request tree (16 drafted positions, top-16), reusing the
+    packed weights of `base` (only the tree, its rows and the activations
+    change).  Same timing rules as the headline number."""
+    import torch
+    out = []
+    for b in budgets:
+        wk = Workload(base.name, int(b), device, share=base, one_request=True)
+        for _ in range(W):
+            wk.step()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            wk.step()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            wk.step()
+        for _ in range(W):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(K):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / K
+        if wk.ws.status() != 0:
+            raise RuntimeError(f"device status {wk.w12.status_str(wk.ws.status())} at budget {b}")
+        out.append({"rows": int(wk.R), "step_us": round(1e3 * ms, 2), "w12_gbs": round(wk.w12_bytes() / (ms * 1e-3) / 1e9, 1)})
+        del g
+    return out
+
+
+# ---------------------------------------------------------------------------
 # main
 # ---------------------------------------------------------------------------
 
@@ -396,6 +457,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cublas", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--rows-sweep", default=None,
+                    help="comma-separated node budgets timed after the headline (default: 1,8,32,64 for "
+                         "single-request workloads, none otherwise; 'none' to skip)")
     ap.add_argument("--gemm", default="auto", choices=["auto", "tcgen05", "warp_mma"],
                     help="GEMM kernel: the library's choice by row count, or one forced")
     args = ap.parse_args()
@@ -527,6 +591,17 @@ def main():
         except Exception as ex:
             cublas = {"error": str(ex)[:200]}
 
+    # --------------------------------------------------- step time vs rows
+    sweep = None
+    spec = args.rows_sweep
+    if spec is None:
+        spec = "1,8,32,64" if wk.wl.n_req == 1 else "none"
+    if spec != "none":
+        try:
+            sweep = rows_sweep(wk, [int(v) for v in spec.split(",") if v], max(10, min(K, 50)), W, device)
+        except Exception as ex:  # reported, never hidden
+            sweep = [{"error": str(ex)[:200]}]
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wk)
@@ -555,7 +630,10 @@ def main():
             "cpu_baseline": cpu,
             "clocks": clocks,
             "gpu_launches": K * wk.gpu_launches_per_step(per_weight),
+            "rows_sweep": sweep,
         }
+        if sweep and len(sweep) > 1 and all("step_us" in e for e in sweep):
+            line["rows_sweep_flatness"] = round(sweep[-1]["step_us"] / sweep[0]["step_us"], 4)
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()

@@ -11,22 +11,26 @@
 //                    lane quarter); a group takes every G-th record of the
 //                    CTA.  Thread = output channel: six 16-byte shared loads,
 //                    in-register decode of its 64 weights, escape patch, one
-//                    tcgen05.st of 32 columns into the group's A buffer.  The
-//                    group then meets at a named barrier and one of its
-//                    threads issues the record's four MMAs (M = 128 channels,
-//                    N = rows rounded up to 32, K = 16) into the group's own
-//                    FP32 accumulator, followed by one commit that frees both
-//                    the shared-memory stage and the A buffer.  No warp waits
-//                    on a signal from another role while records are in flight.
+//                    tcgen05.st of 32 columns into one of the group's A
+//                    buffers, then a non-blocking arrive on that buffer's
+//                    named barrier
+//   MMA warps        one per group: a named-barrier sync on the record's A
+//                    buffer, then one thread issues the record's four MMAs
+//                    (M = 128 channels, N = rows rounded up to 32, K = 16)
+//                    into the group's own FP32 accumulator and one commit that
+//                    frees both the shared-memory stage and the A buffer
 //   epilogue warps   tcgen05.ld of each group's accumulator for a finished
 //                    tile, summed in group order (deterministic); BF16 rows,
 //                    or the tile's (max, index) per row for the LM head; a
 //                    tile split between CTAs is published as a partial and
 //                    finished by the last contributor in CTA order.
 //
-// Every wait is bounded: on a timeout the kernel records W12_E_TIMEOUT, all
-// roles stop together (group exits are agreed at the named barrier), issued
-// MMAs are waited for, and tensor memory is released before the CTA exits.
+// Every mbarrier wait is bounded.  The named-barrier hand-off cannot hang:
+// decode warps arrive once for every record they own and the group's MMA warp
+// syncs once for every one of them, in order, whether or not a timeout has
+// stopped the work; the MMA warp commits every record, so an A buffer's next
+// arrival always follows the previous sync.  Issued MMAs and copies are
+// waited for, and tensor memory is released, before the CTA exits.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -41,12 +45,13 @@ namespace {
 constexpr int kProducerWarp = 0;   // also allocates tensor memory
 constexpr int kGroupWarp0 = 1;     // decode group g = warps 1 + 4g .. 4 + 4g
 constexpr int kMaxGroups = 2;
-constexpr int kEpiWarp0 = 1 + 4 * kMaxGroups;   // warps 9..12
+constexpr int kMmaWarp0 = 1 + 4 * kMaxGroups;   // MMA warp of group g = 9 + g
+constexpr int kEpiWarp0 = kMmaWarp0 + kMaxGroups; // warps 11..14
 constexpr int kThreads = (kEpiWarp0 + 4) * 32;
 constexpr int kACols = 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBarCaches = 1;      // named barrier: decode threads after filling the shared caches
-constexpr int kBarGroup0 = 2;      // named barrier per decode group (2, 3)
+constexpr int kBarA0 = 2;          // named barrier of A buffer (g, a): kBarA0 + g * a_bufs + a (<= 13)
 
 struct TcParams {
     const uint8_t *rec;
@@ -102,16 +107,9 @@ __host__ __device__ inline Plan plan(int stages, int nr, int max_recs, int esc_c
 __device__ __forceinline__ int cta_of_record(int64_t r, int G, int64_t T) { return (int)(((r + 1) * G - 1) / T); }
 __device__ __forceinline__ int64_t first_record(int c, int G, int64_t T) { return (int64_t)c * T / G; }
 
-// AND of `pred` over the `threads` threads meeting at named barrier `id`
-__device__ __forceinline__ bool bar_and(int id, int threads, bool pred)
+__device__ __forceinline__ void named_arrive(int id, int threads)
 {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)pred), "r"(id), "r"(threads)
-        : "memory");
-    return r != 0;
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_constant__ CUtensorMap xmap, const TcParams p)
@@ -207,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
                 }
             }
         }
-    } else if (warp < kEpiWarp0) {
+    } else if (warp < kMmaWarp0) {
         // --------------------------------------------------------------- decode
         const int g = (warp - kGroupWarp0) >> 2;
         const int wq = (warp - kGroupWarp0) & 3;     // warp within the group
@@ -230,24 +228,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
                 for (int i = dtid; i < esc_off_s[nrec] - e_lo; i += ndec) esc_s[i] = __ldg(p.esc + e_lo + i);
             named_bar(kBarCaches, ndec);
 
-            const bool issuer = (wq == 0 && lane == 0);
-            const uint32_t idesc = idesc_bf16_f32(128, NR);
             int64_t nt_cur = -1;
             ChanConst cc{0, 0};
-            int tiles_g = 0, dcur = 0, last_i = -1;
+            // every record of the group is visited: work is skipped after a
+            // timeout, but the hand-off to the MMA warp always takes place
             for (int j = 0;; ++j) {
                 const int i = g + j * GR;
                 if (i >= nrec) break;
                 const int s = i % S;
                 const int64_t r = rec_begin + i;
                 const int64_t nt = r / KT;
-                const int kt = (int)(r - nt * KT);
                 const int ab = j % NAG;
-                bool ok = mbar_wait(bar_full + 8 * s, (i / S) & 1, p.timeout_ns, p.status, abort_flag);
-                if (ok && j >= NAG) {
-                    // the A buffer's previous record (i - GR * NAG) must have finished its MMAs
+                bool ok = !*abort_flag;
+                if (ok) ok = mbar_wait(bar_full + 8 * s, (i / S) & 1, p.timeout_ns, p.status, abort_flag);
+                if (j >= NAG) {
+                    // A buffer ab last held record i - GR * NAG: its MMAs must be
+                    // done.  The MMA warp commits every record, so this wait
+                    // ends even after an abort; it is never skipped (the
+                    // buffer's named barrier is reused only after its sync).
                     const int ip = i - GR * NAG;
-                    ok = mbar_wait(bar_done + 8 * (ip % S), (ip / S) & 1, p.timeout_ns, p.status, abort_flag);
+                    int32_t no_abort = 0;
+                    if (!mbar_wait(bar_done + 8 * (ip % S), (ip / S) & 1, p.timeout_ns, p.status, &no_abort)) ok = false;
                 }
                 ok = __all_sync(0xffffffffu, ok && !*abort_flag);
                 if (ok) {
@@ -292,16 +293,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
                     tmem_st_wait();
                     tc_fence_before();
                 }
-                // the group agrees to go on (all four quarters are in the A buffer) or to stop
-                if (!bar_and(kBarGroup0 + g, 128, ok)) break;
-                if (issuer) {
+                __syncwarp();
+                named_arrive(kBarA0 + g * NAG + ab, 160);
+            }
+        }
+    } else if (warp < kEpiWarp0) {
+        // ------------------------------------------------------------------ MMA
+        const int g = warp - kMmaWarp0;
+        if (g < GR) {
+            const uint32_t idesc = idesc_bf16_f32(128, NR);
+            int tiles_g = 0, dcur = 0, last_i = -1;
+            for (int j = 0;; ++j) {
+                const int i = g + j * GR;
+                if (i >= nrec) break;
+                const int s = i % S, ab = j % NAG;
+                named_bar(kBarA0 + g * NAG + ab, 160);
+                if (lane == 0) {
                     tc_fence_after();
+                    const int kt = (int)((rec_begin + i) % KT);
                     const bool first = (i < GR) || (kt < GR);
                     const bool last = (i + GR >= nrec) || (kt + GR >= KT);
-                    bool go = true;
+                    bool go = !*abort_flag;
                     if (first) {
                         dcur = tiles_g % DB;
-                        if (tiles_g >= DB)
+                        if (go && tiles_g >= DB)
                             go = mbar_wait(bar_accempty + 8 * (g * 2 + dcur), ((tiles_g / DB) - 1) & 1, p.timeout_ns,
                                            p.status, abort_flag);
                         tc_fence_after();
@@ -312,19 +327,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
                             tc_mma_ts(d_t, a_t + ks * 8, bd + (uint64_t)(ks * 2), idesc, (first && ks == 0) ? 0u : 1u);
-                        tc_commit(bar_done + 8 * s);
-                        last_i = i;
-                        if (last) {
-                            tc_commit(bar_accfull + 8 * (g * 2 + dcur));
-                            ++tiles_g;
-                        }
-                    } else {
-                        *abort_flag = 1;
+                    }
+                    tc_commit(bar_done + 8 * s);   // always: frees the stage and the A buffer
+                    last_i = i;
+                    if (last) {
+                        if (go) tc_commit(bar_accfull + 8 * (g * 2 + dcur));
+                        ++tiles_g;
                     }
                 }
+                __syncwarp();
             }
             // tensor memory is released only after this group's issued MMAs finished
-            if (issuer && last_i >= 0) {
+            if (lane == 0 && last_i >= 0) {
                 int32_t no_abort = 0;
                 mbar_wait(bar_done + 8 * (last_i % S), (last_i / S) & 1, p.timeout_ns, p.status, &no_abort);
             }
@@ -500,7 +514,7 @@ namespace w12i {
 // more buffers first.
 bool tc_tmem_plan(int nr, int *groups, int *a_bufs, int *d_bufs)
 {
-    static const int cand[][3] = {{2, 4, 2}, {2, 2, 2}, {2, 2, 1}, {1, 4, 2}, {1, 4, 1}, {1, 2, 1}};
+    static const int cand[][3] = {{2, 6, 2}, {2, 4, 2}, {2, 2, 2}, {2, 2, 1}, {1, 4, 2}, {1, 4, 1}, {1, 2, 1}};
     for (const auto &c : cand) {
         if (c[0] * c[1] * 32 + c[0] * c[2] * nr <= (int)kTmemCols) {
             *groups = c[0], *a_bufs = c[1], *d_bufs = c[2];
