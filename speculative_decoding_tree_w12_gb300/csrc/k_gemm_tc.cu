@@ -308,37 +308,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
                 if (i >= nrec) break;
                 const int s = i % S, ab = j % NAG;
                 named_bar(kBarA0 + g * NAG + ab, 160);
-                if (lane == 0) {
+                // the whole warp runs this part (it stays converged); one
+                // elected lane issues the tensor-core instructions
+                tc_fence_after();
+                const int kt = (int)((rec_begin + i) % KT);
+                const bool first = (i < GR) || (kt < GR);
+                const bool last = (i + GR >= nrec) || (kt + GR >= KT);
+                bool go = !*abort_flag;
+                if (first) {
+                    dcur = tiles_g % DB;
+                    if (go && tiles_g >= DB)
+                        go = mbar_wait(bar_accempty + 8 * (g * 2 + dcur), ((tiles_g / DB) - 1) & 1, p.timeout_ns,
+                                       p.status, abort_flag);
+                    go = __all_sync(0xffffffffu, go);
                     tc_fence_after();
-                    const int kt = (int)((rec_begin + i) % KT);
-                    const bool first = (i < GR) || (kt < GR);
-                    const bool last = (i + GR >= nrec) || (kt + GR >= KT);
-                    bool go = !*abort_flag;
-                    if (first) {
-                        dcur = tiles_g % DB;
-                        if (go && tiles_g >= DB)
-                            go = mbar_wait(bar_accempty + 8 * (g * 2 + dcur), ((tiles_g / DB) - 1) & 1, p.timeout_ns,
-                                           p.status, abort_flag);
-                        tc_fence_after();
-                    }
-                    if (go) {
-                        const uint32_t d_t = tmem + d_col(g, dcur), a_t = tmem + a_col(g, ab);
-                        const uint64_t bd = smem_desc_sw128(x_s + s * xb);
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks)
-                            tc_mma_ts(d_t, a_t + ks * 8, bd + (uint64_t)(ks * 2), idesc, (first && ks == 0) ? 0u : 1u);
-                    }
-                    tc_commit(bar_done + 8 * s);   // always: frees the stage and the A buffer
-                    last_i = i;
-                    if (last) {
-                        if (go) tc_commit(bar_accfull + 8 * (g * 2 + dcur));
-                        ++tiles_g;
-                    }
                 }
-                __syncwarp();
+                if (go) {
+                    const uint32_t d_t = tmem + d_col(g, dcur), a_t = tmem + a_col(g, ab);
+                    const uint64_t bd = smem_desc_sw128(x_s + s * xb);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        tc_mma_ts_elect(d_t, a_t + ks * 8, bd + (uint64_t)(ks * 2), idesc, (first && ks == 0) ? 0u : 1u);
+                }
+                tc_commit_elect(bar_done + 8 * s);   // always: frees the stage and the A buffer
+                last_i = i;
+                if (last) {
+                    if (go) tc_commit_elect(bar_accfull + 8 * (g * 2 + dcur));
+                    ++tiles_g;
+                }
             }
             // tensor memory is released only after this group's issued MMAs finished
-            if (lane == 0 && last_i >= 0) {
+            if (last_i >= 0) {
                 int32_t no_abort = 0;
                 mbar_wait(bar_done + 8 * (last_i % S), (last_i / S) & 1, p.timeout_ns, p.status, &no_abort);
             }
