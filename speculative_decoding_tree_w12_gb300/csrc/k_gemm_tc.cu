@@ -5,8 +5,12 @@
 // cores, a fixed-order stream-K split), laid out for Blackwell's tensor
 // memory:
 //
-//   producer warp    bulk copy of each 12 KB record + 2-D TMA of the matching
-//                    activation block (128-byte swizzle) into a shared ring
+//   record producer  one 24 KB bulk copy per pair of consecutive records (L2
+//                    evict-first) into a ring; a slot is handed back as soon as
+//                    the decode warps have read it into registers, so most of
+//                    the ring is always in flight
+//   activation warp  2-D TMA of each record's activation block (128-byte
+//                    swizzle) into a second ring, freed by the record's commit
 //   decode groups    one or two groups of four warps (one per tensor-memory
 //                    lane quarter); a group takes every G-th record of the
 //                    CTA.  Thread = output channel: six 16-byte shared loads,
@@ -14,20 +18,19 @@
 //                    tcgen05.st of 32 columns into one of the group's A
 //                    buffers, then a non-blocking arrive on that buffer's
 //                    named barrier
-//   MMA warps        one per group: a named-barrier sync on the record's A
-//                    buffer, then one thread issues the record's four MMAs
-//                    (M = 128 channels, N = rows rounded up to 32, K = 16)
-//                    into the group's own FP32 accumulator and one commit that
-//                    frees both the shared-memory stage and the A buffer
-//   epilogue warps   tcgen05.ld of each group's accumulator for a finished
-//                    tile, summed in group order (deterministic); BF16 rows,
+//   MMA warp         takes the records in order: a named-barrier sync on the
+//                    record's A buffer, then one elected lane issues the
+//                    record's four MMAs (M = 128 channels, N = rows rounded up
+//                    to 32, K = 16) into the tile's FP32 accumulator and one
+//                    commit that frees the activation slot and the A buffer
+//   epilogue warps   tcgen05.ld of a finished tile's accumulator; BF16 rows,
 //                    or the tile's (max, index) per row for the LM head; a
 //                    tile split between CTAs is published as a partial and
 //                    finished by the last contributor in CTA order.
 //
 // Every mbarrier wait is bounded.  The named-barrier hand-off cannot hang:
-// decode warps arrive once for every record they own and the group's MMA warp
-// syncs once for every one of them, in order, whether or not a timeout has
+// decode warps arrive once for every record they own and the MMA warp syncs
+// once for every record, in order, whether or not a timeout has
 // stopped the work; the MMA warp commits every record, so an A buffer's next
 // arrival always follows the previous sync.  Issued MMAs and copies are
 // waited for, and tensor memory is released, before the CTA exits.
@@ -45,9 +48,11 @@ namespace {
 constexpr int kProducerWarp = 0;   // also allocates tensor memory
 constexpr int kGroupWarp0 = 1;     // decode group g = warps 1 + 4g .. 4 + 4g
 constexpr int kMaxGroups = 2;
-constexpr int kMmaWarp0 = 1 + 4 * kMaxGroups;   // MMA warp of group g = 9 + g
-constexpr int kEpiWarp0 = kMmaWarp0 + kMaxGroups; // warps 11..14
-constexpr int kThreads = (kEpiWarp0 + 4) * 32;
+constexpr int kMmaWarp = 1 + 4 * kMaxGroups;    // warp 9
+constexpr int kEpiWarp0 = kMmaWarp + 1;          // warps 10..13
+constexpr int kXWarp = kEpiWarp0 + 4;            // warp 14: activation copies
+constexpr int kThreads = (kXWarp + 1) * 32;
+constexpr int kRecPair = 2 * w12i::kRecBytes;
 constexpr int kACols = 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBarCaches = 1;      // named barrier: decode threads after filling the shared caches
@@ -62,7 +67,7 @@ struct TcParams {
     int32_t nr;          // MMA N: rows rounded up to 32
     int32_t groups;      // decode groups (1 or 2)
     int32_t a_bufs;      // A buffers per group
-    int32_t d_bufs;      // accumulators per group (1 or 2)
+    int32_t d_bufs;      // tile accumulators (1 or 2)
     uint16_t *y;
     int64_t ldy;
     float *s1_val;
@@ -73,23 +78,26 @@ struct TcParams {
     uint32_t mul16;
     int32_t debug_flags;
     uint64_t timeout_ns;
-    int32_t stages, max_recs, esc_cap, base_tiles;
+    int32_t stages;      // record-pair slots; the activation ring and the done
+                         // barriers have groups * a_bufs slots
+    int32_t max_recs, esc_cap, base_tiles;
 };
 
 struct Plan {
     int rec, x, bars, misc, escoff, esc, base, red, total;
 };
 
-__host__ __device__ inline Plan plan(int stages, int nr, int max_recs, int esc_cap, int base_tiles)
+// q = activation slots (= groups * A buffers per group)
+__host__ __device__ inline Plan plan(int stages, int q, int nr, int max_recs, int esc_cap, int base_tiles)
 {
     Plan p;
     int o = 0;
     p.rec = o;
-    o += stages * w12i::kRecBytes;            // 12 KB per stage keeps the 1024-byte alignment
+    o += stages * kRecPair;                   // 24 KB per slot keeps the 1024-byte alignment
     p.x = o;
-    o += stages * nr * 128;
+    o += q * nr * 128;
     p.bars = o;
-    o += 8 * (2 * stages + 4 * kMaxGroups * 2 + 2);   // full, done; acc full/empty [g][d]; epilogue sync
+    o += 8 * (2 * stages + 2 * q + 2 * 2 + 1);   // rec full/empty, x full, done, acc full/empty, epilogue
     p.misc = o;
     o += 32;
     p.escoff = o;
@@ -117,22 +125,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int S = p.stages, NR = p.nr, GR = p.groups, NAG = p.a_bufs, DB = p.d_bufs;
-    const Plan pl = plan(S, NR, p.max_recs, p.esc_cap, p.base_tiles);
+    const int Q = GR * NAG;
+    const Plan pl = plan(S, Q, NR, p.max_recs, p.esc_cap, p.base_tiles);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, cta = blockIdx.x;
     const int KT = p.k_tiles;
     const int64_t T = (int64_t)p.n_tiles * KT;
     const int64_t rec_begin = first_record(cta, G, T), rec_end = first_record(cta + 1, G, T);
     const int nrec = (int)(rec_end - rec_begin);
+    const int npairs = (nrec + 1) / 2;
     const int64_t nt_first = rec_begin / KT, nt_last = (rec_end - 1) / KT;
 
     const uint32_t rec_s = smem_u32(smem + pl.rec), x_s = smem_u32(smem + pl.x);
     const uint32_t xb = (uint32_t)NR * 128;
     const uint32_t bar0 = smem_u32(smem + pl.bars);
-    const uint32_t bar_full = bar0, bar_done = bar0 + 8 * S;
-    const uint32_t bar_accfull = bar_done + 8 * S;                  // [g][d]
-    const uint32_t bar_accempty = bar_accfull + 8 * kMaxGroups * 2;  // [g][d]
-    const uint32_t bar_epi = bar_accempty + 8 * kMaxGroups * 2;
+    const uint32_t bar_rfull = bar0, bar_rempty = bar0 + 8 * S;
+    const uint32_t bar_xfull = bar_rempty + 8 * S, bar_done = bar_xfull + 8 * Q;
+    const uint32_t bar_accfull = bar_done + 8 * Q, bar_accempty = bar_accfull + 16;
+    const uint32_t bar_epi = bar_accempty + 16;
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(smem + pl.misc);
     int32_t *last_flag = reinterpret_cast<int32_t *>(smem + pl.misc + 4);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + pl.misc + 8);
@@ -140,14 +150,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
     uint32_t *esc_s = reinterpret_cast<uint32_t *>(smem + pl.esc);
     uint8_t *base_s = smem + pl.base;
 
+    const bool drop_first = (p.debug_flags & 1) && cta == 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(bar_full + 8 * s, 1);   // the producer's expect_tx arrival (+ the copies' bytes)
-            mbar_init(bar_done + 8 * s, 1);   // one commit per record: its MMAs (and its reads) are done
+            mbar_init(bar_rfull + 8 * s, 1);    // producer's expect_tx arrival + the copy's bytes
+            mbar_init(bar_rempty + 8 * s, 8);   // the decode warps have read both records of the pair
         }
-        for (int b = 0; b < kMaxGroups * 2; ++b) {
-            mbar_init(bar_accfull + 8 * b, 1);    // commit after a tile's last MMA of the group
-            mbar_init(bar_accempty + 8 * b, 4);   // the four epilogue warps have read the accumulator
+        for (int s = 0; s < Q; ++s) {
+            mbar_init(bar_xfull + 8 * s, 1);    // activation warp's expect_tx arrival + the block
+            mbar_init(bar_done + 8 * s, 1);     // one commit per record: its MMAs are done
+        }
+        for (int d = 0; d < 2; ++d) {
+            mbar_init(bar_accfull + 8 * d, 1);    // commit after a tile's last MMA
+            mbar_init(bar_accempty + 8 * d, 4);   // the four epilogue warps have read the accumulator
         }
         mbar_init(bar_epi, 4);
         *abort_flag = 0;
@@ -162,50 +177,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
 
     const uint32_t d_col0 = (uint32_t)(GR * NAG * kACols);
     auto a_col = [&](int g, int a) { return (uint32_t)((g * NAG + a) * kACols); };
-    auto d_col = [&](int g, int d) { return d_col0 + (uint32_t)((g * DB + d) * NR); };
+    auto d_col = [&](int d) { return d_col0 + (uint32_t)(d * NR); };
 
     if (warp == kProducerWarp) {
-        // -------------------------------------------------------------- producer
+        // ------------------------------------------------------- record producer
         if (lane == 0) {
-            prefetch_tmap(&xmap);
             const uint64_t pol = policy_evict_first();
-            const bool drop_first = (p.debug_flags & 1) && cta == 0;
-            auto issue_w = [&](int i, int s) {
-                mbar_expect_tx(bar_full + 8 * s, (uint32_t)w12i::kRecBytes + xb);
-                if (!(drop_first && i == 0))
-                    bulk_g2s(rec_s + s * w12i::kRecBytes, p.rec + (rec_begin + i) * (int64_t)w12i::kRecBytes,
-                             (uint32_t)w12i::kRecBytes, bar_full + 8 * s, pol);
+            auto issue = [&](int m, int sl) {
+                const int n = min(2, nrec - 2 * m);
+                mbar_expect_tx(bar_rfull + 8 * sl, (uint32_t)(n * w12i::kRecBytes));
+                if (!(drop_first && m == 0))
+                    bulk_g2s(rec_s + sl * kRecPair, p.rec + (rec_begin + 2 * m) * (int64_t)w12i::kRecBytes,
+                             (uint32_t)(n * w12i::kRecBytes), bar_rfull + 8 * sl, pol);
             };
-            auto issue_x = [&](int i, int s) {
-                if (drop_first && i == 0) return;
-                const int kt = (int)((rec_begin + i) % KT);
-                tma_load_2d(x_s + s * xb, &xmap, kt * w12i::kTileK, 0, bar_full + 8 * s);
-            };
-            const int pre = min(S, nrec);
-            // weights do not depend on earlier kernels: start them before the
-            // programmatic-dependency wait
-            for (int i = 0; i < pre; ++i) issue_w(i, i);
-            pdl_wait();
-            for (int i = 0; i < pre; ++i) issue_x(i, i);
+            // weights do not depend on earlier kernels: no programmatic-dependency wait
+            const int pre = min(S, npairs);
+            for (int m = 0; m < pre; ++m) issue(m, m);
             int issued = pre;
-            for (int i = pre; i < nrec; ++i) {
-                const int s = i % S;
-                // stage s was last used by record i - S: wait for its MMAs
-                if (!mbar_wait(bar_done + 8 * s, ((i / S) - 1) & 1, p.timeout_ns, p.status, abort_flag)) break;
-                issue_w(i, s);
-                issue_x(i, s);
-                issued = i + 1;
+            for (int m = pre; m < npairs; ++m) {
+                const int sl = m % S;
+                // slot sl last held pair m - S: every decode warp must have read it
+                if (!mbar_wait(bar_rempty + 8 * sl, ((m / S) - 1) & 1, p.timeout_ns, p.status, abort_flag)) break;
+                issue(m, sl);
+                issued = m + 1;
             }
             if (*abort_flag) {
                 // leave no copy in flight
                 int32_t no_abort = 0;
-                for (int i = max(0, issued - S); i < issued; ++i) {
-                    if (drop_first && i == 0) continue;
-                    mbar_wait(bar_full + 8 * (i % S), (i / S) & 1, p.timeout_ns, p.status, &no_abort);
+                for (int m = max(0, issued - S); m < issued; ++m) {
+                    if (drop_first && m == 0) continue;
+                    mbar_wait(bar_rfull + 8 * (m % S), (m / S) & 1, p.timeout_ns, p.status, &no_abort);
                 }
             }
         }
-    } else if (warp < kMmaWarp0) {
+    } else if (warp < kMmaWarp) {
         // --------------------------------------------------------------- decode
         const int g = (warp - kGroupWarp0) >> 2;
         const int wq = (warp - kGroupWarp0) & 3;     // warp within the group
@@ -235,20 +240,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
             for (int j = 0;; ++j) {
                 const int i = g + j * GR;
                 if (i >= nrec) break;
-                const int s = i % S;
+                const int m = i >> 1, s = m % S;          // record pair m holds records 2m, 2m + 1
                 const int64_t r = rec_begin + i;
                 const int64_t nt = r / KT;
                 const int ab = j % NAG;
                 bool ok = !*abort_flag;
-                if (ok) ok = mbar_wait(bar_full + 8 * s, (i / S) & 1, p.timeout_ns, p.status, abort_flag);
-                if (j >= NAG) {
-                    // A buffer ab last held record i - GR * NAG: its MMAs must be
-                    // done.  The MMA warp commits every record, so this wait
-                    // ends even after an abort; it is never skipped (the
-                    // buffer's named barrier is reused only after its sync).
-                    const int ip = i - GR * NAG;
+                if (ok) ok = mbar_wait(bar_rfull + 8 * s, (m / S) & 1, p.timeout_ns, p.status, abort_flag);
+                if (i >= Q) {
+                    // A buffer ab last held record i - Q: its MMAs must be done.
+                    // The MMA warp commits every record, so this wait ends even
+                    // after an abort; it is never skipped (the buffer's named
+                    // barrier is reused only after its sync).
                     int32_t no_abort = 0;
-                    if (!mbar_wait(bar_done + 8 * (ip % S), (ip / S) & 1, p.timeout_ns, p.status, &no_abort)) ok = false;
+                    if (!mbar_wait(bar_done + 8 * (i % Q), ((i / Q) - 1) & 1, p.timeout_ns, p.status, &no_abort)) ok = false;
                 }
                 ok = __all_sync(0xffffffffu, ok && !*abort_flag);
                 if (ok) {
@@ -258,13 +262,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
                                                        : __ldg(p.base + nt * w12i::kTileN + c);
                         cc = chan_const(b);
                     }
-                    const uint8_t *rb = smem + pl.rec + s * w12i::kRecBytes;
+                    const uint8_t *rb = smem + pl.rec + s * kRecPair + (i & 1) * w12i::kRecBytes;
                     uint4 v[4], nb[2];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) v[q] = *reinterpret_cast<const uint4 *>(rb + (q * 128 + c) * 16);
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
                         nb[h] = *reinterpret_cast<const uint4 *>(rb + w12i::kViewBytes + (h * 128 + c) * 16);
+                    // the record is in registers: hand the slot back to the producer
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_rempty + 8 * s);
                     uint32_t a[32];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -297,53 +304,51 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
                 named_arrive(kBarA0 + g * NAG + ab, 160);
             }
         }
-    } else if (warp < kEpiWarp0) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------ MMA
-        const int g = warp - kMmaWarp0;
-        if (g < GR) {
-            const uint32_t idesc = idesc_bf16_f32(128, NR);
-            int tiles_g = 0, dcur = 0, last_i = -1;
-            for (int j = 0;; ++j) {
-                const int i = g + j * GR;
-                if (i >= nrec) break;
-                const int s = i % S, ab = j % NAG;
-                named_bar(kBarA0 + g * NAG + ab, 160);
-                // the whole warp runs this part (it stays converged); one
-                // elected lane issues the tensor-core instructions
+        const uint32_t idesc = idesc_bf16_f32(128, NR);
+        int tcount = 0, dcur = 0;
+        int kt = (int)(rec_begin - nt_first * KT);
+        for (int i = 0; i < nrec; ++i) {
+            const int g = i % GR, j = i / GR;
+            const int xs = i % Q, ab = j % NAG;
+            named_bar(kBarA0 + g * NAG + ab, 160);
+            // the whole warp runs this part (it stays converged); one elected
+            // lane issues the tensor-core instructions
+            tc_fence_after();
+            const bool first = (i == 0) || kt == 0;
+            const bool last = (i == nrec - 1) || kt == KT - 1;
+            bool go = !*abort_flag;
+            if (go) go = mbar_wait(bar_xfull + 8 * xs, (i / Q) & 1, p.timeout_ns, p.status, abort_flag);
+            go = __all_sync(0xffffffffu, go);
+            if (first) {
+                dcur = tcount % DB;
+                if (go && tcount >= DB)
+                    go = mbar_wait(bar_accempty + 8 * dcur, ((tcount / DB) - 1) & 1, p.timeout_ns, p.status,
+                                   abort_flag);
+                go = __all_sync(0xffffffffu, go);
                 tc_fence_after();
-                const int kt = (int)((rec_begin + i) % KT);
-                const bool first = (i < GR) || (kt < GR);
-                const bool last = (i + GR >= nrec) || (kt + GR >= KT);
-                bool go = !*abort_flag;
-                if (first) {
-                    dcur = tiles_g % DB;
-                    if (go && tiles_g >= DB)
-                        go = mbar_wait(bar_accempty + 8 * (g * 2 + dcur), ((tiles_g / DB) - 1) & 1, p.timeout_ns,
-                                       p.status, abort_flag);
-                    go = __all_sync(0xffffffffu, go);
-                    tc_fence_after();
-                }
-                if (go) {
-                    const uint32_t d_t = tmem + d_col(g, dcur), a_t = tmem + a_col(g, ab);
-                    const uint64_t bd = smem_desc_sw128(x_s + s * xb);
+            }
+            if (go) {
+                const uint32_t d_t = tmem + d_col(dcur), a_t = tmem + a_col(g, ab);
+                const uint64_t bd = smem_desc_sw128(x_s + xs * xb);
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        tc_mma_ts_elect(d_t, a_t + ks * 8, bd + (uint64_t)(ks * 2), idesc, (first && ks == 0) ? 0u : 1u);
-                }
-                tc_commit_elect(bar_done + 8 * s);   // always: frees the stage and the A buffer
-                last_i = i;
-                if (last) {
-                    if (go) tc_commit_elect(bar_accfull + 8 * (g * 2 + dcur));
-                    ++tiles_g;
-                }
+                for (int ks = 0; ks < 4; ++ks)
+                    tc_mma_ts_elect(d_t, a_t + ks * 8, bd + (uint64_t)(ks * 2), idesc, (first && ks == 0) ? 0u : 1u);
             }
-            // tensor memory is released only after this group's issued MMAs finished
-            if (last_i >= 0) {
-                int32_t no_abort = 0;
-                mbar_wait(bar_done + 8 * (last_i % S), (last_i / S) & 1, p.timeout_ns, p.status, &no_abort);
+            tc_commit_elect(bar_done + 8 * xs);   // always: frees the activation slot and the A buffer
+            if (last) {
+                if (go) tc_commit_elect(bar_accfull + 8 * dcur);
+                ++tcount;
             }
+            if (++kt == KT) kt = 0;
         }
-    } else {
+        // tensor memory is released only after every issued MMA finished
+        if (nrec > 0) {
+            int32_t no_abort = 0;
+            mbar_wait(bar_done + 8 * ((nrec - 1) % Q), ((nrec - 1) / Q) & 1, p.timeout_ns, p.status, &no_abort);
+        }
+    } else if (warp < kXWarp) {
         // ------------------------------------------------------------- epilogue
         const int quarter = warp & 3;
         const int c = quarter * 32 + lane;
@@ -360,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
             eph ^= 1u;
             return __all_sync(0xffffffffu, ok);
         };
-        int tg[kMaxGroups] = {0, 0};
+        int tcount = 0;
         // write (or reduce, for the LM head) 32 rows r0..r0+31 of this channel
         auto emit_rows = [&](int64_t nt, int r0, const float (&v)[32]) {
             if (p.mode == w12i::kModeLinear) {
@@ -401,20 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
         };
         for (int64_t nt = nt_first; nt <= nt_last; ++nt) {
             const int64_t t0 = nt * KT, t1 = t0 + KT;
-            // this CTA's records of the tile, [ia, ib) in CTA-local numbering
-            const int ia = (int)((rec_begin > t0 ? rec_begin : t0) - rec_begin);
-            const int ib = (int)((rec_end < t1 ? rec_end : t1) - rec_begin);
-            bool part[kMaxGroups];
-            int dsel[kMaxGroups];
-            bool ok = true;
-#pragma unroll
-            for (int g = 0; g < kMaxGroups; ++g) {
-                part[g] = g < GR && (ib - ia >= GR || ia % GR == g);
-                dsel[g] = tg[g] % DB;
-                if (part[g] && ok)
-                    ok = mbar_wait(bar_accfull + 8 * (g * 2 + dsel[g]), (tg[g] / DB) & 1, p.timeout_ns, p.status,
-                                   abort_flag);
-            }
+            const int dsel = tcount % DB;
+            const bool ok = mbar_wait(bar_accfull + 8 * dsel, (tcount / DB) & 1, p.timeout_ns, p.status, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
             const bool owned = rec_begin <= t0 && rec_end >= t1;
@@ -422,18 +415,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
             float *mine = p.partial + ((int64_t)(cta * 2 + slot) * NR) * w12i::kTileN;
             const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
             for (int r0 = 0; r0 < NR; r0 += 32) {
+                uint32_t raw[32];
+                tmem_ld_x32(lane_base + d_col(dsel) + r0, raw);
+                tmem_ld_wait();
                 float v[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = 0.f;
-#pragma unroll
-                for (int g = 0; g < kMaxGroups; ++g) {
-                    if (!part[g]) continue;
-                    uint32_t raw[32];
-                    tmem_ld_x32(lane_base + d_col(g, dsel[g]) + r0, raw);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] += __uint_as_float(raw[j]);
-                }
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]);
                 if (owned) {
                     emit_rows(nt, r0, v);
                 } else {
@@ -444,12 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
             }
             tc_fence_before();
             __syncwarp();
-#pragma unroll
-            for (int g = 0; g < kMaxGroups; ++g)
-                if (part[g]) {
-                    if (lane == 0) mbar_arrive(bar_accempty + 8 * (g * 2 + dsel[g]));
-                    ++tg[g];
-                }
+            if (lane == 0) mbar_arrive(bar_accempty + 8 * dsel);
+            ++tcount;
             if (owned) {
                 if (!head_finish(nt)) break;
                 continue;
@@ -477,6 +460,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
             }
             if (etid == 0) p.counters[nt] = 0;   // ready for the next launch using this slot
             if (!head_finish(nt)) break;
+        }
+    }
+
+    if (warp == kXWarp && lane == 0) {
+        // ---------------------------------------------------- activation copies
+        prefetch_tmap(&xmap);
+        pdl_wait();   // activations come from the previous kernel
+        int issued = 0;
+        for (int i = 0; i < nrec; ++i) {
+            const int xs = i % Q;
+            // slot xs last held record i - Q: its MMAs must be done
+            if (i >= Q && !mbar_wait(bar_done + 8 * xs, ((i / Q) - 1) & 1, p.timeout_ns, p.status, abort_flag)) break;
+            mbar_expect_tx(bar_xfull + 8 * xs, xb);
+            if (!(drop_first && i == 0))
+                tma_load_2d(x_s + xs * xb, &xmap, (int)((rec_begin + i) % KT) * w12i::kTileK, 0, bar_xfull + 8 * xs);
+            issued = i + 1;
+        }
+        if (*abort_flag) {
+            int32_t no_abort = 0;
+            for (int i = max(0, issued - Q); i < issued; ++i) {
+                if (drop_first && i == 0) continue;
+                mbar_wait(bar_xfull + 8 * (i % Q), (i / Q) & 1, p.timeout_ns, p.status, &no_abort);
+            }
         }
     }
 
@@ -509,19 +515,27 @@ EncodeTiledFn encode_fn_tc()
 
 namespace w12i {
 
-// Tensor-memory plan for MMA width nr: groups x A buffers x 32 columns, then
-// groups x accumulators x nr columns, within 512 columns.  More groups and
-// more buffers first.
-bool tc_tmem_plan(int nr, int *groups, int *a_bufs, int *d_bufs)
+// Buffer plan for MMA width nr: groups x A buffers x 32 columns plus
+// accumulators x nr columns within 512 tensor-memory columns; the activation
+// ring (groups x A buffers slots of nr x 128 bytes) and at least two
+// record-pair slots within the shared-memory budget.  Preference: two decode
+// groups, then as many record-pair slots (bytes in flight) as possible.
+bool tc_buffer_plan(int nr, int max_recs, int esc_cap, int base_tiles, int budget, int *groups, int *a_bufs,
+                    int *d_bufs, int *stages)
 {
-    static const int cand[][3] = {{2, 6, 2}, {2, 4, 2}, {2, 2, 2}, {2, 2, 1}, {1, 4, 2}, {1, 4, 1}, {1, 2, 1}};
-    for (const auto &c : cand) {
-        if (c[0] * c[1] * 32 + c[0] * c[2] * nr <= (int)kTmemCols) {
-            *groups = c[0], *a_bufs = c[1], *d_bufs = c[2];
-            return true;
-        }
+    static const int cand[][3] = {{2, 4, 2}, {2, 3, 2}, {2, 2, 2}, {2, 4, 1}, {2, 2, 1}, {1, 4, 2}, {1, 4, 1}, {1, 2, 1}};
+    int best = -1, best_st = 0;
+    for (int k = 0; k < (int)(sizeof(cand) / sizeof(cand[0])); ++k) {
+        const int g = cand[k][0], na = cand[k][1], db = cand[k][2];
+        if (g * na * kACols + db * nr > (int)kTmemCols) continue;
+        int st = 8;
+        while (st >= 2 && plan(st, g * na, nr, max_recs, esc_cap, base_tiles).total > budget) --st;
+        if (st < 2) continue;
+        if (best < 0 || (g > cand[best][0]) || (g == cand[best][0] && st > best_st)) best = k, best_st = st;
     }
-    return false;
+    if (best < 0) return false;
+    *groups = cand[best][0], *a_bufs = cand[best][1], *d_bufs = cand[best][2], *stages = best_st;
+    return true;
 }
 
 int launch_gemm_tc(const GemmArgs &a, void *stream)
@@ -551,7 +565,7 @@ int launch_gemm_tc(const GemmArgs &a, void *stream)
     p.R = a.R;
     p.mode = a.mode;
     p.nr = nr;
-    if (!tc_tmem_plan(nr, &p.groups, &p.a_bufs, &p.d_bufs)) return (int)cudaErrorInvalidValue;
+
     p.y = a.y;
     p.ldy = a.w.n;
     p.s1_val = a.stage1_val;
@@ -566,16 +580,9 @@ int launch_gemm_tc(const GemmArgs &a, void *stream)
     p.esc_cap = 2048;
     p.base_tiles = std::min<int>(64, (int)(p.max_recs / a.w.k_tiles + 2));
     const int budget = 227 * 1024;
-    // stages: as many as fit (at most 16), a multiple of the group count and
-    // never fewer than the A buffers in flight.  Then record i - S of a stage
-    // belongs to the same group as record i, so a group never sees the shared
-    // "done" barrier of a stage run more than one phase ahead of its wait.
-    int stages = 16;
-    while (stages - p.groups >= p.groups * p.a_bufs &&
-           plan(stages, nr, p.max_recs, p.esc_cap, p.base_tiles).total > budget)
-        stages -= p.groups;
-    p.stages = stages;
-    const int smem = plan(stages, nr, p.max_recs, p.esc_cap, p.base_tiles).total;
+    if (!tc_buffer_plan(nr, p.max_recs, p.esc_cap, p.base_tiles, budget, &p.groups, &p.a_bufs, &p.d_bufs, &p.stages))
+        return (int)cudaErrorInvalidConfiguration;
+    const int smem = plan(p.stages, p.groups * p.a_bufs, nr, p.max_recs, p.esc_cap, p.base_tiles).total;
     if (smem > budget) return (int)cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(k_w12_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return (int)e;
