@@ -401,6 +401,65 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------
+# quick pass (view planes only)
+# ---------------------------------------------------------------------------
+
+def quick_pass(wk: "Workload", K: int, W: int):
+    """The same layer and LM head read through the quick pass (w12_gemm_q /
+    w12_lmhead_argmax_q: the 8 KB view plane of every record, low mantissa
+    bits at the midpoint): graph-timed step (every linear + the head + the
+    argmax reduction), the head launch alone, and the top-1 agreement of the
+    quick argmax with the exact one on the step's rows."""
+    import torch
+    w12 = wk.w12
+    qs = [torch.empty_like(y) for y in wk.ys]
+    qam = torch.empty_like(wk.argmax)
+
+    def qstep():
+        for dw, x, y in zip(wk.lin, wk.xs, qs):
+            w12.w12_gemm(dw, x, wk.ws, y=y, quick=True)
+        w12.w12_lmhead_argmax(wk.head, wk.h, wk.ws, argmax=qam, quick=True)
+
+    def timed(fn):
+        for _ in range(W):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fn()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            fn()
+        for _ in range(W):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(K):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / K
+
+    ms_step = timed(qstep)
+    ms_head = timed(lambda: w12.w12_lmhead_argmax(wk.head, wk.h, wk.ws, argmax=qam, quick=True))
+    if wk.ws.status() != 0:
+        raise RuntimeError(f"device status {w12.status_str(wk.ws.status())}")
+    view = lambda d: d.nbytes - d.rec.numel() // 3    # the view plane is 8 of every 12 KB
+    qbytes = sum(view(d) for d in wk.lin) + view(wk.head)
+    wk.step()
+    torch.cuda.synchronize()
+    agree = float((qam == wk.argmax).float().mean().item())
+    return {"step_us": round(1e3 * ms_step, 2), "w12_view_bytes_per_step": int(qbytes),
+            "gbs": round(qbytes / (ms_step * 1e-3) / 1e9, 1),
+            "head_us": round(1e3 * ms_head, 2), "head_gbs": round(view(wk.head) / (ms_head * 1e-3) / 1e9, 1),
+            "top1_agreement": round(agree, 4), "rows": int(wk.R)}
+
+
+# ---------------------------------------------------------------------------
 # step time vs tree rows
 # ---------------------------------------------------------------------------
 
@@ -591,6 +650,13 @@ def main():
         except Exception as ex:
             cublas = {"error": str(ex)[:200]}
 
+    # ------------------------------------------------------- quick pass
+    quick = None
+    try:
+        quick = quick_pass(wk, K, W)
+    except Exception as ex:  # reported, never hidden
+        quick = {"error": str(ex)[:200]}
+
     # --------------------------------------------------- step time vs rows
     sweep = None
     spec = args.rows_sweep
@@ -631,6 +697,7 @@ def main():
             "clocks": clocks,
             "gpu_launches": K * wk.gpu_launches_per_step(per_weight),
             "rows_sweep": sweep,
+            "quick_pass": quick,
         }
         if sweep and len(sweep) > 1 and all("step_us" in e for e in sweep):
             line["rows_sweep_flatness"] = round(sweep[-1]["step_us"] / sweep[0]["step_us"], 4)

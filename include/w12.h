@@ -208,6 +208,22 @@ w12_status w12_gemm_static_scratch(const w12_weight *w, const uint16_t *x, int32
 w12_status w12_lmhead_argmax(const w12_weight *head, const uint16_t *h, int32_t R, int32_t *argmax,
                              float *maxlogit, void *ws, size_t ws_bytes, w12_stream_t stream);
 
+/*
+ * Quick pass (SpecPilot explainer, 4.1 "the 8-bit view is what the Q pass
+ * reads" and 4.3 TLV: the Q pass reads the view already nested in the W12
+ * record, its first 2/3, with the discarded mantissa bits set to the
+ * midpoint).  Same contract as w12_gemm and w12_lmhead_argmax, computed with
+ * the quick weights: every in-window weight keeps its sign, exponent and
+ * three high mantissa bits and takes 0b1000 as its four low mantissa bits;
+ * escaped weights keep their exact value.  Only the 8 KB view plane of each
+ * record is read (about 2/3 of the W12 bytes).  Runs on the warp-level MMA
+ * path for every row count (row slices of up to 64).
+ */
+w12_status w12_gemm_q(const w12_weight *w, const uint16_t *x, int32_t R, uint16_t *y, void *ws, size_t ws_bytes,
+                      w12_stream_t stream);
+w12_status w12_lmhead_argmax_q(const w12_weight *head, const uint16_t *h, int32_t R, int32_t *argmax,
+                               float *maxlogit, void *ws, size_t ws_bytes, w12_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Draft tree
  * ---------------------------------------------------------------------- */

@@ -48,11 +48,12 @@ def lib():
         L.orc_w12_layout.argtypes = [p, i64, i64, p, p]
         L.orc_w12_pack.argtypes = [p, i64, i64, p, p, p, p]
         L.orc_w12_unpack_rows.argtypes = [p, p, p, p, i64, i64, i64, i64, p]
+        L.orc_w12_unpack_rows_q.argtypes = [p, p, p, p, i64, i64, i64, i64, p]
         L.orc_gemm_f64.argtypes = [p, i64, p, i64, i64, p, C.c_int]
         L.orc_head_argmax.argtypes = [p, i64, p, i64, i64, p, p, p, p, C.c_int]
         L.orc_tree_build.argtypes = [i32, i32, i32, i32, p, p, p, p, i32, p, p, p, p, p, p, p, p]
         L.orc_tree_accept.argtypes = [i32, p, p, p, p, i32, i32, p, p, p, p]
-        for f in (L.orc_w12_layout, L.orc_w12_pack, L.orc_w12_unpack_rows, L.orc_gemm_f64,
+        for f in (L.orc_w12_layout, L.orc_w12_pack, L.orc_w12_unpack_rows, L.orc_w12_unpack_rows_q, L.orc_gemm_f64,
                   L.orc_head_argmax, L.orc_tree_build, L.orc_tree_accept):
             f.restype = C.c_int
         _lib = L
@@ -112,6 +113,17 @@ def w12_unpack(p: Packed, row0: int = 0, nrows: Optional[int] = None) -> np.ndar
     esc = p.esc if p.esc.size else np.zeros(1, dtype=np.uint32)
     _check(lib().orc_w12_unpack_rows(_ptr(p.rec), _ptr(p.base), _ptr(p.esc_tile_off), _ptr(esc),
                                      p.n, p.k, row0, nrows, _ptr(out)), "w12_unpack")
+    return out
+
+
+def w12_unpack_q(p: Packed, row0: int = 0, nrows: Optional[int] = None) -> np.ndarray:
+    """Quick-pass weights of rows ``[row0, row0 + nrows)`` as BF16 bits (R19:
+    view byte with the low mantissa nibble 0b1000; escapes exact)."""
+    nrows = p.n - row0 if nrows is None else nrows
+    out = np.empty((nrows, p.k), dtype=np.uint16)
+    esc = p.esc if p.esc.size else np.zeros(1, dtype=np.uint32)
+    _check(lib().orc_w12_unpack_rows_q(_ptr(p.rec), _ptr(p.base), _ptr(p.esc_tile_off), _ptr(esc),
+                                       p.n, p.k, row0, nrows, _ptr(out)), "w12_unpack_q")
     return out
 
 

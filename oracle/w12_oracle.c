@@ -54,6 +54,8 @@
  *   R14 a child at depth d uses position d (1-based); depth <= P_r.
  *   R15 chain mode = only rank-0 candidates (n_cand = 1).
  *   R16 if two accepted siblings had the same token the lowest row wins.
+ *   R19 quick pass: in-window weights from the view byte with the four low
+ *       mantissa bits set to 0b1000; escaped weights exact.
  */
 #include <math.h>
 #include <pthread.h>
@@ -246,6 +248,43 @@ static void *gemm_worker(void *p)
         }
     }
     return NULL;
+}
+
+/* R19: the quick pass (explainer 4.1 "the 8-bit view is what the Q pass reads";
+ * 4.3: the Q pass reads the view nested in the record with the discarded
+ * mantissa bits set to the midpoint).  In-window weights keep sign, exponent
+ * and the three high mantissa bits from the view byte and take 0b1000 as the
+ * low four; escaped weights keep their exact value (the escape list is part
+ * of the record's weight and is read as is). */
+int orc_w12_unpack_rows_q(const uint8_t *rec, const uint8_t *base, const int32_t *esc_tile_off,
+                          const uint32_t *esc, int64_t n, int64_t k, int64_t row0, int64_t nrows,
+                          uint16_t *out)
+{
+    if (!rec || !base || !esc_tile_off || !out || n % TILE_N || k % TILE_K || row0 < 0 || nrows < 0 ||
+        row0 + nrows > n)
+        return ORC_EINVAL;
+    int64_t kt_count = k / TILE_K;
+    for (int64_t ch = row0; ch < row0 + nrows; ++ch) {
+        int64_t nt = ch / TILE_N;
+        int c = (int)(ch % TILE_N);
+        int b = base[ch];
+        for (int64_t kt = 0; kt < kt_count; ++kt) {
+            int64_t t = nt * kt_count + kt;
+            const uint8_t *r = rec + t * REC_BYTES;
+            for (int kl = 0; kl < TILE_K; ++kl) {
+                int v = r[view_off(c, kl)];
+                int s = v >> 7, o = (v >> 3) & 0xF, mh = v & 7;
+                out[(ch - row0) * k + kt * TILE_K + kl] = (uint16_t)((s << 15) | ((b + o) << 7) | (mh << 4) | 0x8);
+            }
+            for (int32_t e = esc_tile_off[t]; e < esc_tile_off[t + 1]; ++e) {
+                uint32_t en = esc[e];
+                int nl = (int)(en >> 22) & 0x7F, kl = (int)(en >> 16) & 0x3F;
+                if (nl != c) continue;
+                out[(ch - row0) * k + kt * TILE_K + kl] = (uint16_t)(en & 0xFFFF);
+            }
+        }
+    }
+    return ORC_OK;
 }
 
 /* y[r][c] = sum_i x[r][i] * w[c][i], FP64 accumulation in index order. */

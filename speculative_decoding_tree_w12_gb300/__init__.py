@@ -93,6 +93,8 @@ def lib():
             "w12_gemm": ([p, p, i32, p, p, sz, p], C.c_int),
             "w12_gemm_static_scratch": ([p, p, i32, p, p], C.c_int),
             "w12_lmhead_argmax": ([p, p, i32, p, p, p, sz, p], C.c_int),
+            "w12_gemm_q": ([p, p, i32, p, p, sz, p], C.c_int),
+            "w12_lmhead_argmax_q": ([p, p, i32, p, p, p, sz, p], C.c_int),
             "w12_tree_build": ([p, i32, p, p, sz, p], C.c_int),
             "w12_tree_accept": ([p, i32, i32, p, p, p, p, p], C.c_int),
             "w12_verify_step": ([p, p, i32, i32, p, p, p, p, sz, p], C.c_int),
@@ -231,25 +233,32 @@ def w12_load_check(w: DeviceWeight, src_bf16, ws: Workspace, stream=None) -> int
     return int(mism.value)
 
 
-def w12_gemm(w: DeviceWeight, x, ws: Workspace, y=None, stream=None):
-    """``y = x . W^T`` (x: bf16 [R][k] on the device) -> bf16 [R][n]."""
+def w12_gemm(w: DeviceWeight, x, ws: Workspace, y=None, stream=None, quick: bool = False):
+    """``y = x . W^T`` (x: bf16 [R][k] on the device) -> bf16 [R][n].
+    ``quick``: the quick pass (``w12_gemm_q``, view planes only)."""
     import torch
     R = x.shape[0]
     if y is None:
         y = torch.empty((R, w.n), dtype=torch.bfloat16, device=x.device)
-    _check(lib().w12_gemm(C.byref(w.c), C.c_void_p(x.data_ptr()), R, C.c_void_p(y.data_ptr()), ws.ptr, ws.nbytes,
-                          _stream(stream)), "w12_gemm")
+    fn, name = (lib().w12_gemm_q, "w12_gemm_q") if quick else (lib().w12_gemm, "w12_gemm")
+    _check(fn(C.byref(w.c), C.c_void_p(x.data_ptr()), R, C.c_void_p(y.data_ptr()), ws.ptr, ws.nbytes,
+              _stream(stream)), name)
     return y
 
 
-def w12_lmhead_argmax(head: DeviceWeight, h, ws: Workspace, argmax=None, maxlogit=None, stream=None):
+def w12_lmhead_argmax(head: DeviceWeight, h, ws: Workspace, argmax=None, maxlogit=None, stream=None,
+                      quick: bool = False):
+    """Argmax over ``h . W_head^T`` per row -> int32 [R].  ``quick``: the quick
+    pass (``w12_lmhead_argmax_q``, view planes only)."""
     import torch
     R = h.shape[0]
     if argmax is None:
         argmax = torch.empty(R, dtype=torch.int32, device=h.device)
-    _check(lib().w12_lmhead_argmax(C.byref(head.c), C.c_void_p(h.data_ptr()), R, C.c_void_p(argmax.data_ptr()),
-                                   C.c_void_p(_dp(maxlogit)) if maxlogit is not None else None, ws.ptr, ws.nbytes,
-                                   _stream(stream)), "w12_lmhead_argmax")
+    fn, name = (lib().w12_lmhead_argmax_q, "w12_lmhead_argmax_q") if quick else \
+        (lib().w12_lmhead_argmax, "w12_lmhead_argmax")
+    _check(fn(C.byref(head.c), C.c_void_p(h.data_ptr()), R, C.c_void_p(argmax.data_ptr()),
+              C.c_void_p(_dp(maxlogit)) if maxlogit is not None else None, ws.ptr, ws.nbytes,
+              _stream(stream)), name)
     return argmax
 
 

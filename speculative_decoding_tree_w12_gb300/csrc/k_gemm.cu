@@ -53,9 +53,12 @@ struct KParams {
     int32_t base_tiles;     // n-tiles whose window bases fit the shared cache
 };
 
-template <int NB8, int WK, int RPS>
+// QV: the quick pass (only the 8 KB view plane of each record is read; the
+// low mantissa bits of in-window weights are taken as the midpoint 0b1000)
+template <int NB8, int WK, int RPS, bool QV = false>
 struct Cfg {
     static constexpr int kRecsPerStage = RPS;                  // records per shared-memory stage
+    static constexpr int kRecStride = QV ? w12i::kViewBytes : w12i::kRecBytes;   // bytes kept per record
     static constexpr int kRows = NB8 * 8;                     // rows per activation block
     static constexpr int kXBytes = kRows * 128;               // activation block: rows x 64 BF16
     static constexpr int kConsumerWarps = kWarpsN * WK;
@@ -70,14 +73,14 @@ struct SmemPlan {
     int rec_off, x_off, red_off, bar_off, flag_off, escoff_off, esc_off, base_off, total;
 };
 
-template <int NB8, int WK, int RPS>
+template <int NB8, int WK, int RPS, bool QV>
 __host__ __device__ inline SmemPlan smem_plan(int stages, int max_recs, int esc_cap, int base_tiles)
 {
-    using C = Cfg<NB8, WK, RPS>;
+    using C = Cfg<NB8, WK, RPS, QV>;
     SmemPlan s;
     int o = 0;
     s.rec_off = o;
-    o += stages * RPS * w12i::kRecBytes;
+    o += stages * RPS * C::kRecStride;
     s.x_off = o;
     o += stages * RPS * C::kXBytes;
     s.red_off = o;
@@ -99,15 +102,15 @@ __host__ __device__ inline SmemPlan smem_plan(int stages, int max_recs, int esc_
 __device__ __forceinline__ int cta_of_record(int64_t r, int G, int64_t T) { return (int)(((r + 1) * G - 1) / T); }
 __device__ __forceinline__ int64_t first_record(int c, int G, int64_t T) { return (int64_t)c * T / G; }
 
-template <int NB8, int WK, int RPS>
-__global__ void __launch_bounds__(Cfg<NB8, WK, RPS>::kThreads, 1)
+template <int NB8, int WK, int RPS, bool QV>
+__global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
     k_w12_gemm(const __grid_constant__ CUtensorMap xmap, const KParams p)
 {
-    using C = Cfg<NB8, WK, RPS>;
+    using C = Cfg<NB8, WK, RPS, QV>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // the 128-byte swizzle of the activation blocks needs 1024-byte alignment
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const SmemPlan sp = smem_plan<NB8, WK, RPS>(p.stages, p.max_recs, p.esc_cap, p.base_tiles);
+    const SmemPlan sp = smem_plan<NB8, WK, RPS, QV>(p.stages, p.max_recs, p.esc_cap, p.base_tiles);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, cta = blockIdx.x;
@@ -151,10 +154,20 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS>::kThreads, 1)
             auto recs_in = [&](int j) { return min(RPS, nrec - j * RPS); };
             auto issue_w = [&](int j, int sl) {
                 const int n = recs_in(j);
-                mbar_expect_tx(bar_full + 8 * sl, (uint32_t)n * (w12i::kRecBytes + C::kXBytes));
-                if (!(drop_first && j == 0))
-                    bulk_g2s(rec_s + sl * RPS * w12i::kRecBytes, p.rec + (rec_begin + j * RPS) * (int64_t)w12i::kRecBytes,
-                             (uint32_t)n * w12i::kRecBytes, bar_full + 8 * sl, pol);
+                mbar_expect_tx(bar_full + 8 * sl, (uint32_t)n * (C::kRecStride + C::kXBytes));
+                if (!(drop_first && j == 0)) {
+                    if constexpr (QV) {
+                        // the view plane of each record: its first 8 KB
+                        for (int r = 0; r < n; ++r)
+                            bulk_g2s(rec_s + (sl * RPS + r) * C::kRecStride,
+                                     p.rec + (rec_begin + j * RPS + r) * (int64_t)w12i::kRecBytes,
+                                     (uint32_t)w12i::kViewBytes, bar_full + 8 * sl, pol);
+                    } else {
+                        bulk_g2s(rec_s + sl * RPS * w12i::kRecBytes,
+                                 p.rec + (rec_begin + j * RPS) * (int64_t)w12i::kRecBytes, (uint32_t)n * w12i::kRecBytes,
+                                 bar_full + 8 * sl, pol);
+                    }
+                }
             };
             auto issue_x = [&](int j, int sl) {
                 if (drop_first && j == 0) return;
@@ -392,7 +405,9 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS>::kThreads, 1)
 #pragma unroll
             for (int kgl = 0; kgl < C::kKgPerWarp; ++kgl) {
                 const int kg = wk * C::kKgPerWarp + kgl;
-                if (kgl == 0 || (kg & 1) == 0) {
+                if constexpr (QV) {
+                    nib_lo = nib_hi = 0x88888888u;   // every low mantissa nibble = 0b1000
+                } else if (kgl == 0 || (kg & 1) == 0) {
                     nib_lo = rw[(w12i::kViewBytes + (kg >> 1) * 2048 + mb * 256) / 4];
                     nib_hi = rw[(w12i::kViewBytes + (kg >> 1) * 2048 + mb * 256 + 128) / 4];
                 }
@@ -455,7 +470,7 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS>::kThreads, 1)
         }
     };
     auto rec_words = [&](int q) {
-        return reinterpret_cast<const uint32_t *>(rec_thread + (s * RPS + q) * w12i::kRecBytes);
+        return reinterpret_cast<const uint32_t *>(rec_thread + (s * RPS + q) * C::kRecStride);
     };
     auto rec_x = [&](int q) { return x_s + (s * RPS + q) * C::kXBytes; };
 
@@ -551,10 +566,10 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-template <int NB8, int WK, int RPS>
+template <int NB8, int WK, int RPS, bool QV = false>
 int launch_t(const w12i::GemmArgs &a, const CUtensorMap &xmap, cudaStream_t st)
 {
-    using C = Cfg<NB8, WK, RPS>;
+    using C = Cfg<NB8, WK, RPS, QV>;
     const int64_t T = (int64_t)a.w.n_tiles * a.w.k_tiles;
     const int G = (int)std::min<int64_t>(a.num_sms, T);
     const int max_recs = (int)((T + G - 1) / G);
@@ -582,14 +597,16 @@ int launch_t(const w12i::GemmArgs &a, const CUtensorMap &xmap, cudaStream_t st)
     p.base_tiles = std::min<int>(64, (int)(max_recs / a.w.k_tiles + 2));
     const int budget = 227 * 1024;
     int stages = 8;
-    while (stages > 2 && smem_plan<NB8, WK, RPS>(stages, max_recs, p.esc_cap, p.base_tiles).total > budget) --stages;
+    while (stages > 2 && smem_plan<NB8, WK, RPS, QV>(stages, max_recs, p.esc_cap, p.base_tiles).total > budget)
+        --stages;
     p.stages = stages;
-    const int smem = smem_plan<NB8, WK, RPS>(stages, max_recs, p.esc_cap, p.base_tiles).total;
+    const int smem = smem_plan<NB8, WK, RPS, QV>(stages, max_recs, p.esc_cap, p.base_tiles).total;
     if (smem > budget) return (int)cudaErrorInvalidConfiguration;
-    cudaError_t e = cudaFuncSetAttribute(k_w12_gemm<NB8, WK, RPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(k_w12_gemm<NB8, WK, RPS, QV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return (int)e;
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, k_w12_gemm<NB8, WK, RPS>);
+    e = cudaFuncGetAttributes(&fa, k_w12_gemm<NB8, WK, RPS, QV>);
     if (e != cudaSuccess) return (int)e;
     if (fa.maxThreadsPerBlock < C::kThreads) return (int)cudaErrorLaunchOutOfResources;
     cudaLaunchConfig_t cfg{};
@@ -602,7 +619,7 @@ int launch_t(const w12i::GemmArgs &a, const CUtensorMap &xmap, cudaStream_t st)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 1 : 0;
-    return (int)cudaLaunchKernelEx(&cfg, k_w12_gemm<NB8, WK, RPS>, xmap, p);
+    return (int)cudaLaunchKernelEx(&cfg, k_w12_gemm<NB8, WK, RPS, QV>, xmap, p);
 }
 
 }  // namespace
@@ -627,6 +644,14 @@ int launch_gemm(const GemmArgs &a, void *stream)
     if (r != CUDA_SUCCESS) return (int)cudaErrorInvalidValue;
     // 8 consumer warps (two 16-K groups each); two records per stage up to 32
     // rows (one wait and one release per 24 KB), one record per stage at 64 rows
+    if (a.qview) {
+        switch (nb8) {
+        case 1: return launch_t<1, 2, 2, true>(a, xmap, st);
+        case 2: return launch_t<2, 2, 2, true>(a, xmap, st);
+        case 4: return launch_t<4, 2, 2, true>(a, xmap, st);
+        default: return launch_t<8, 2, 1, true>(a, xmap, st);
+        }
+    }
     switch (nb8) {
     case 1: return launch_t<1, 2, 2>(a, xmap, st);
     case 2: return launch_t<2, 2, 2>(a, xmap, st);

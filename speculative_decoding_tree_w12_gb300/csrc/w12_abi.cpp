@@ -165,9 +165,9 @@ w12_status ws_check(void *ws, size_t ws_bytes, const WsLayout &L)
 }
 
 int gemm_slices(const DevWeight &dw, const uint16_t *x, int32_t R, int mode, uint16_t *y, const Ws &ws, int &slot,
-                bool pdl, cudaStream_t st)
+                bool pdl, cudaStream_t st, bool qview = false)
 {
-    const bool tc = use_tc(R);
+    const bool tc = !qview && use_tc(R);
     const int32_t step = tc ? R : kPartialRows;
     for (int32_t r0 = 0; r0 < R; r0 += step) {
         GemmArgs a{};
@@ -185,6 +185,7 @@ int gemm_slices(const DevWeight &dw, const uint16_t *x, int32_t R, int mode, uin
         a.pdl = pdl;
         a.debug_flags = g_debug_flags;
         a.timeout_ns = g_timeout_ns;
+        a.qview = qview;
         const int e = tc ? launch_gemm_tc(a, st) : launch_gemm(a, st);
         if (e) return e;
         if (int pe = prof_mark(st)) return pe;
@@ -312,8 +313,10 @@ w12_status w12_load_check(const w12_weight *w, const uint16_t *src_bf16, int64_t
     return host == 0 ? W12_OK : W12_E_MISMATCH;
 }
 
-w12_status w12_gemm(const w12_weight *w, const uint16_t *x, int32_t R, uint16_t *y, void *ws, size_t ws_bytes,
-                    w12_stream_t stream)
+namespace {
+
+w12_status gemm_entry(const w12_weight *w, const uint16_t *x, int32_t R, uint16_t *y, void *ws, size_t ws_bytes,
+                      w12_stream_t stream, bool qview)
 {
     w12_status s = weight_ok(w);
     if (s != W12_OK) return s;
@@ -326,7 +329,21 @@ w12_status w12_gemm(const w12_weight *w, const uint16_t *x, int32_t R, uint16_t 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (int ce = W.clear_counters(st)) return cuda_status(ce);
     int slot = 0;
-    return cuda_status(gemm_slices(dev_weight(w), x, R, kModeLinear, y, W, slot, false, st));
+    return cuda_status(gemm_slices(dev_weight(w), x, R, kModeLinear, y, W, slot, false, st, qview));
+}
+
+}  // namespace
+
+w12_status w12_gemm(const w12_weight *w, const uint16_t *x, int32_t R, uint16_t *y, void *ws, size_t ws_bytes,
+                    w12_stream_t stream)
+{
+    return gemm_entry(w, x, R, y, ws, ws_bytes, stream, false);
+}
+
+w12_status w12_gemm_q(const w12_weight *w, const uint16_t *x, int32_t R, uint16_t *y, void *ws, size_t ws_bytes,
+                      w12_stream_t stream)
+{
+    return gemm_entry(w, x, R, y, ws, ws_bytes, stream, true);
 }
 
 w12_status w12_gemm_static_scratch(const w12_weight *w, const uint16_t *x, int32_t R, uint16_t *y,
@@ -352,8 +369,10 @@ w12_status w12_gemm_static_scratch(const w12_weight *w, const uint16_t *x, int32
     return cuda_status(launch_gemm_static_scratch(a, stream));
 }
 
-w12_status w12_lmhead_argmax(const w12_weight *head, const uint16_t *h, int32_t R, int32_t *argmax, float *maxlogit,
-                             void *ws, size_t ws_bytes, w12_stream_t stream)
+namespace {
+
+w12_status head_entry(const w12_weight *head, const uint16_t *h, int32_t R, int32_t *argmax, float *maxlogit,
+                      void *ws, size_t ws_bytes, w12_stream_t stream, bool qview)
 {
     w12_status s = weight_ok(head);
     if (s != W12_OK) return s;
@@ -367,8 +386,22 @@ w12_status w12_lmhead_argmax(const w12_weight *head, const uint16_t *h, int32_t 
     if (int ce = W.clear_counters(st)) return cuda_status(ce);
     int slot = 0;
     const DevWeight dw = dev_weight(head);
-    if (int e = gemm_slices(dw, h, R, kModeHead, nullptr, W, slot, false, st)) return cuda_status(e);
+    if (int e = gemm_slices(dw, h, R, kModeHead, nullptr, W, slot, false, st, qview)) return cuda_status(e);
     return cuda_status(launch_argmax_stage2(W.s1_val(), W.s1_idx(), R, dw.n_tiles, argmax, maxlogit, true, st));
+}
+
+}  // namespace
+
+w12_status w12_lmhead_argmax(const w12_weight *head, const uint16_t *h, int32_t R, int32_t *argmax, float *maxlogit,
+                             void *ws, size_t ws_bytes, w12_stream_t stream)
+{
+    return head_entry(head, h, R, argmax, maxlogit, ws, ws_bytes, stream, false);
+}
+
+w12_status w12_lmhead_argmax_q(const w12_weight *head, const uint16_t *h, int32_t R, int32_t *argmax,
+                               float *maxlogit, void *ws, size_t ws_bytes, w12_stream_t stream)
+{
+    return head_entry(head, h, R, argmax, maxlogit, ws, ws_bytes, stream, true);
 }
 
 w12_status w12_tree_build(const w12_lattice *lat, int32_t budget, w12_tree *out, void *ws, size_t ws_bytes,

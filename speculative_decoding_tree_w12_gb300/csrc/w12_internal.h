@@ -68,6 +68,7 @@ struct GemmArgs {
     int32_t *status;
     int num_sms;
     bool pdl;                // launched as a programmatic dependent of the previous kernel
+    bool qview;              // quick pass: view planes only, low mantissa bits = 0b1000 (warp-MMA path)
     int32_t debug_flags;
     uint64_t timeout_ns;
 };

@@ -178,6 +178,53 @@ def test_lmhead_argmax_detects_planted_defect(w12):
 
 
 # ---------------------------------------------------------------------------
+# quick pass (view planes only)
+# ---------------------------------------------------------------------------
+
+QUICK_GEMM_CASES = [
+    (1024, 512, 8, 0.01, 0.01),
+    (640, 4096, 32, 0.0, 0.0),
+    (256, 5120, 64, 0.0, 0.001),
+    (512, 1024, 100, 0.0, 0.0),      # two row slices
+    (128, 64, 5, 0.0, 0.0),
+]
+
+
+@pytest.mark.parametrize("n,k,R,outl,zero", QUICK_GEMM_CASES)
+def test_gemm_quick_matches_oracle(w12, n, k, R, outl, zero):
+    w = synth.weights(n, k, n + k + R, 21, outl, zero)
+    x = synth.activations(R, k, n + k + R, 22)
+    pk = oracle.w12_pack(w)
+    ref = oracle.gemm_f64(x, oracle.w12_unpack_q(pk))
+    dw = _packed(w12, w)
+    ws = w12.Workspace(R, n)
+    y = w12.w12_gemm(dw, _dev_bf16(x), ws, quick=True)
+    y2 = w12.w12_gemm(dw, _dev_bf16(x), ws, quick=True)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    got = synth.bf16_bits_to_f32(_bits(y)).astype(np.float64)
+    assert H.gemm_rel_err(got, ref) <= H.GEMM_REL_TOL
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))   # deterministic
+
+
+@pytest.mark.parametrize("V,K,R", [(4096, 512, 8), (8192, 1024, 33), (2048, 384, 70)])
+def test_lmhead_argmax_quick_matches_oracle(w12, V, K, R):
+    wh = synth.weights(V, K, V + K, 23)
+    pk = oracle.w12_pack(wh)
+    wq = oracle.w12_unpack_q(pk)
+    h = synth.activations(R, K, V + K, 24)
+    am, _, mg = oracle.head_argmax(h, wq)
+    dw = _packed(w12, wh)
+    ws = w12.Workspace(R, 0, V)
+    got = w12.w12_lmhead_argmax(dw, _dev_bf16(h), ws, quick=True)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    gated = mg > H.MARGIN_GATE
+    assert gated.mean() > 0.9
+    assert np.array_equal(got.cpu().numpy()[gated], am[gated])
+
+
+# ---------------------------------------------------------------------------
 # tree build and acceptance
 # ---------------------------------------------------------------------------
 

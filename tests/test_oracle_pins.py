@@ -128,6 +128,51 @@ def test_w12_gaussian_escape_rate_and_bits():
 
 
 # ---------------------------------------------------------------------------
+# Quick pass (explainer 4.1, 4.3; reading R19)
+# ---------------------------------------------------------------------------
+
+def _quick_closed_form(w: np.ndarray, base: np.ndarray) -> np.ndarray:
+    """From the source bits alone: escaped weights (exponent field outside
+    [b, b+15]) stay exact; every other weight keeps its upper 12 bits and
+    takes 0b1000 as its low mantissa nibble."""
+    e = (w.astype(np.int64) >> 7) & 0xFF
+    b = base.astype(np.int64)[:, None]
+    escaped = (e < b) | (e > b + 15)
+    return np.where(escaped, w, (w & 0xFFF0) | 0x0008).astype(np.uint16)
+
+
+def test_quick_decode_closed_form_gaussian_with_escapes():
+    w = synth.weights(512, 256, 4, 31, 0.01, 0.01)
+    p = oracle.w12_pack(w)
+    assert p.n_escapes > 0
+    assert np.array_equal(oracle.w12_unpack_q(p), _quick_closed_form(w, p.base))
+
+
+def test_quick_decode_closed_form_every_bf16_pattern():
+    w = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(1024, 64)
+    p = oracle.w12_pack(w)
+    assert np.array_equal(oracle.w12_unpack_q(p), _quick_closed_form(w, p.base))
+
+
+def test_quick_decode_is_exact_when_low_nibble_is_the_midpoint():
+    w = synth.weights(256, 128, 5, 32)
+    w = ((w & 0xFFF0) | 0x0008).astype(np.uint16)
+    p = oracle.w12_pack(w)
+    assert np.array_equal(oracle.w12_unpack_q(p), oracle.w12_unpack(p))
+
+
+def test_quick_decode_error_bound():
+    """An in-window quick weight differs from the exact one by at most half
+    of its low-nibble range: |q - w| <= 8 units of the last mantissa place."""
+    w = synth.weights(256, 128, 6, 33)
+    p = oracle.w12_pack(w)
+    q = oracle.w12_unpack_q(p)
+    diff = np.abs((q.astype(np.int64) & 0xF) - (w.astype(np.int64) & 0xF))
+    assert diff.max() <= 8
+    assert np.array_equal(q & 0xFFF0, w & 0xFFF0)
+
+
+# ---------------------------------------------------------------------------
 # GEMM (explainer 1.1, 2.1) and LM-head argmax
 # ---------------------------------------------------------------------------
 
