@@ -57,7 +57,6 @@ struct KParams {
 // low mantissa bits of in-window weights are taken as the midpoint 0b1000)
 template <int NB8, int WK, int RPS, bool QV = false>
 struct Cfg {
-    static constexpr int kRecsPerStage = RPS;                  // records per shared-memory stage
     static constexpr int kRecStride = QV ? w12i::kViewBytes : w12i::kRecBytes;   // bytes kept per record
     static constexpr int kRows = NB8 * 8;                     // rows per activation block
     static constexpr int kXBytes = kRows * 128;               // activation block: rows x 64 BF16
@@ -70,7 +69,7 @@ struct Cfg {
 };
 
 struct SmemPlan {
-    int rec_off, x_off, red_off, bar_off, flag_off, escoff_off, esc_off, base_off, total;
+    int rec_off, x_off, red_off, bar_off, flag_off, escoff_off, esc_off, emask_off, base_off, total;
 };
 
 template <int NB8, int WK, int RPS, bool QV>
@@ -93,6 +92,8 @@ __host__ __device__ inline SmemPlan smem_plan(int stages, int max_recs, int esc_
     o += ((max_recs + 1) * 4 + 15) / 16 * 16;
     s.esc_off = o;
     o += esc_cap * 4;
+    s.emask_off = o;
+    o += (max_recs + 15) / 16 * 16;
     s.base_off = o;
     o += base_tiles * w12i::kTileN;
     s.total = o + 1024;   // slack to align the window to 1024 bytes at run time
@@ -130,6 +131,7 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
     int32_t *last_flag = reinterpret_cast<int32_t *>(smem + sp.flag_off + 4);
     int32_t *esc_off_s = reinterpret_cast<int32_t *>(smem + sp.escoff_off);
     uint32_t *esc_s = reinterpret_cast<uint32_t *>(smem + sp.esc_off);
+    uint8_t *emask_s = smem + sp.emask_off;
     uint8_t *base_s = smem + sp.base_off;
 
     if (threadIdx.x == 0) {
@@ -231,6 +233,18 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
     const bool esc_cached = (esc_off_s[nrec] - e_lo) <= p.esc_cap;
     if (esc_cached)
         for (int i = ctid; i < esc_off_s[nrec] - e_lo; i += C::kConsumers) esc_s[i] = __ldg(p.esc + e_lo + i);
+    // per record, a bit for every consumer warp whose part of the record
+    // holds an escape: the record loop skips the escape list without reading it
+    static_assert(C::kConsumerWarps <= 8, "one mask byte per record");
+    for (int i = ctid; i < nrec; i += C::kConsumers) {
+        uint32_t m = 0;
+        for (int e = esc_off_s[i]; e < esc_off_s[i + 1]; ++e) {
+            const uint32_t en = __ldg(p.esc + e);
+            const int nl = (en >> 22) & 0x7F, kg = ((en >> 16) & 0x3F) >> 4;
+            m |= 1u << ((nl >> 5) + kWarpsN * (kg / C::kKgPerWarp));
+        }
+        emask_s[i] = (uint8_t)m;
+    }
     if (!cons_sync0()) return;
 
     float acc[2][NB8][4];
@@ -282,32 +296,32 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
                 rb[(row + 1) * C::kRedStride + ch + 8] = acc[mb][nb][3];
             }
         if (!cons_sync()) return false;
-        // 2. sum the K-slices in order into red[0]
         const int R = p.R;
         const int rows = min(R, C::kRows);
-        for (int e = ctid; e < rows * 32; e += C::kConsumers) {
-            const int row = e >> 5, c4 = (e & 31) * 4;
-            float4 v = *reinterpret_cast<float4 *>(red + row * C::kRedStride + c4);
+        // the tile's value at (row, 4 channels from c4): the K-slices summed in
+        // slice order, or (nslices = 1) red[0] once it holds the finished sum
+        auto tile4 = [&](int row, int c4, int nslices) {
+            float4 v = *reinterpret_cast<const float4 *>(red + row * C::kRedStride + c4);
 #pragma unroll
-            for (int s = 1; s < WK; ++s) {
-                const float4 w = *reinterpret_cast<float4 *>(red + (s * C::kRows + row) * C::kRedStride + c4);
+            for (int sl = 1; sl < WK; ++sl) {
+                if (sl >= nslices) break;
+                const float4 w = *reinterpret_cast<const float4 *>(red + (sl * C::kRows + row) * C::kRedStride + c4);
                 v.x += w.x, v.y += w.y, v.z += w.z, v.w += w.w;
             }
-            *reinterpret_cast<float4 *>(red + row * C::kRedStride + c4) = v;
-        }
-        if (!cons_sync()) return false;
+            return v;
+        };
 
         const int64_t t0 = nt * KT, t1 = t0 + KT;
         const bool owned = rec_begin <= t0 && rec_end >= t1;
         bool finish = owned;
+        int nslices = WK;
         if (!owned) {
-            // 3. publish this CTA's partial (slot 0 for its first tile, 1 for its last)
+            // 2. publish this CTA's partial (slot 0 for its first tile, 1 for its last)
             const int slot = (nt == nt_first) ? 0 : 1;
             float *mine = p.partial + ((int64_t)(cta * 2 + slot) * C::kRows) * w12i::kTileN;
             for (int e = ctid; e < rows * 32; e += C::kConsumers) {
                 const int row = e >> 5, c4 = (e & 31) * 4;
-                __stcg(reinterpret_cast<float4 *>(mine + row * w12i::kTileN + c4),
-                       *reinterpret_cast<float4 *>(red + row * C::kRedStride + c4));
+                __stcg(reinterpret_cast<float4 *>(mine + row * w12i::kTileN + c4), tile4(row, c4, WK));
             }
             __threadfence();
             if (!cons_sync()) return false;
@@ -320,7 +334,7 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
             finish = *last_flag != 0;
             if (finish) {
                 __threadfence();
-                // 4. the last contributor sums every partial in CTA order
+                // 3. the last contributor sums every partial in CTA order into red[0]
                 for (int e = ctid; e < rows * 32; e += C::kConsumers) {
                     const int row = e >> 5, c4 = (e & 31) * 4;
                     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -334,40 +348,59 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
                 }
                 if (ctid == 0) p.counters[nt] = 0;   // ready for the next launch using this slot
                 if (!cons_sync()) return false;
+                nslices = 1;
             }
         }
         if (finish) {
             if (p.mode == w12i::kModeLinear) {
-                // 5a. BF16 (round to nearest even) rows of 128 channels
+                // 4a. BF16 (round to nearest even) rows of 128 channels
                 for (int e = ctid; e < rows * 32; e += C::kConsumers) {
                     const int row = e >> 5, c4 = (e & 31) * 4;
-                    const float4 v = *reinterpret_cast<float4 *>(red + row * C::kRedStride + c4);
+                    const float4 v = tile4(row, c4, nslices);
                     uint2 packed;
                     packed.x = pack_bf16x2(v.x, v.y);
                     packed.y = pack_bf16x2(v.z, v.w);
                     *reinterpret_cast<uint2 *>(p.y + row * p.ldy + nt * w12i::kTileN + c4) = packed;
                 }
             } else {
-                // 5b. per row: (max, lowest index) over the tile's 128 tokens
-                for (int row = cw; row < rows; row += C::kConsumerWarps) {
-                    float bv = __int_as_float(0x7fc00000);
-                    int32_t bi = 0x7fffffff;
+                // 4b. per row: (max, lowest index) over the tile's 128 tokens; a
+                // warp reduces four of its rows side by side
+                constexpr int kU = 4;
+                for (int r0 = cw; r0 < rows; r0 += kU * C::kConsumerWarps) {
+                    float bv[kU];
+                    int32_t bi[kU];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int ch = lane * 4 + q;
-                        const float v = red[row * C::kRedStride + ch];
-                        if (beats(v, ch, bv, bi)) bv = v, bi = ch;
+                    for (int u = 0; u < kU; ++u) {
+                        bv[u] = __int_as_float(0x7fc00000);
+                        bi[u] = 0x7fffffff;
+                        const int row = r0 + u * C::kConsumerWarps;
+                        if (row < rows) {
+                            const float4 v = tile4(row, lane * 4, nslices);
+                            const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                if (beats(vv[q], lane * 4 + q, bv[u], bi[u])) bv[u] = vv[q], bi[u] = lane * 4 + q;
+                        }
                     }
 #pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) {
-                        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                        const int32_t oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                        if (beats(ov, oi, bv, bi)) bv = ov, bi = oi;
-                    }
+                    for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                        for (int u = 0; u < kU; ++u) {
+                            const float ov = __shfl_xor_sync(0xffffffffu, bv[u], off);
+                            const int32_t oi = __shfl_xor_sync(0xffffffffu, bi[u], off);
+                            if (beats(ov, oi, bv[u], bi[u])) bv[u] = ov, bi[u] = oi;
+                        }
                     if (lane == 0) {
-                        p.s1_val[(int64_t)row * p.n_tiles + nt] = bv;
-                        p.s1_idx[(int64_t)row * p.n_tiles + nt] =
-                            (bi == 0x7fffffff) ? (int32_t)(nt * w12i::kTileN) : (int32_t)(nt * w12i::kTileN + bi);
+#pragma unroll
+                        for (int u = 0; u < kU; ++u) {
+                            const int row = r0 + u * C::kConsumerWarps;
+                            if (row < rows) {
+                                p.s1_val[(int64_t)row * p.n_tiles + nt] = bv[u];
+                                p.s1_idx[(int64_t)row * p.n_tiles + nt] = (bi[u] == 0x7fffffff)
+                                                                              ? (int32_t)(nt * w12i::kTileN)
+                                                                              : (int32_t)(nt * w12i::kTileN + bi[u]);
+                            }
+                        }
                     }
                 }
             }
@@ -419,29 +452,43 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
             }
         }
     };
-    // escaped slots of record i: the owning lane replaces the filler by the exact value
-    auto patch_rec = [&](int i, Frag &fa) {
+    // escaped slots of record i: the warp reads up to 32 entries at once,
+    // keeps the ones inside its 32 channels x (16 * kKgPerWarp) K, and the
+    // owning lane replaces the filler by the exact value
+    auto patch_rec = [&](int i, Frag &fa, bool has) {
+        if (!has) return;
         const int32_t e0 = esc_off_s[i] - e_lo, e1 = esc_off_s[i + 1] - e_lo;
-        for (int e = e0; e < e1; ++e) {
-            const uint32_t en = esc_cached ? esc_s[e] : __ldg(p.esc + e_lo + e);
-            const int nl = (en >> 22) & 0x7F, kl = (en >> 16) & 0x3F;
-            const int kg = kl >> 4;
-            if ((nl >> 5) != mw || (kg / C::kKgPerWarp) != wk) continue;
-            const int kk = kl & 15;
-            if (lane != ((nl & 7) * 4 + ((kk & 7) >> 1))) continue;
-            const int mb_e = (nl >> 4) & 1, kgl_e = kg % C::kKgPerWarp;
-            const int j_e = (kk >> 3) * 2 + ((nl >> 3) & 1);
-            const uint32_t val = en & 0xFFFFu;
-            const bool upper = kk & 1;
+        for (int eb = e0; eb < e1; eb += 32) {
+            const int e = eb + lane;
+            uint32_t en = 0;
+            bool own = false;
+            if (e < e1) {
+                en = esc_cached ? esc_s[e] : __ldg(p.esc + e_lo + e);
+                const int nl = (en >> 22) & 0x7F, kg = ((en >> 16) & 0x3F) >> 4;
+                own = (nl >> 5) == mw && (kg / C::kKgPerWarp) == wk;
+            }
+            uint32_t mine = __ballot_sync(0xffffffffu, own);
+            while (mine) {
+                const int src = __ffs(mine) - 1;
+                mine &= mine - 1;
+                const uint32_t ent = __shfl_sync(0xffffffffu, en, src);
+                const int nl = (ent >> 22) & 0x7F, kl = (ent >> 16) & 0x3F;
+                const int kk = kl & 15;
+                if (lane != ((nl & 7) * 4 + ((kk & 7) >> 1))) continue;
+                const int mb_e = (nl >> 4) & 1, kgl_e = (kl >> 4) % C::kKgPerWarp;
+                const int j_e = (kk >> 3) * 2 + ((nl >> 3) & 1);
+                const uint32_t val = ent & 0xFFFFu;
+                const bool upper = kk & 1;
 #pragma unroll
-            for (int mb = 0; mb < 2; ++mb)
+                for (int mb = 0; mb < 2; ++mb)
 #pragma unroll
-                for (int kgl = 0; kgl < C::kKgPerWarp; ++kgl)
+                    for (int kgl = 0; kgl < C::kKgPerWarp; ++kgl)
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        if (mb == mb_e && kgl == kgl_e && j == j_e)
-                            fa[mb][kgl][j] = upper ? ((fa[mb][kgl][j] & 0x0000FFFFu) | (val << 16))
-                                                   : ((fa[mb][kgl][j] & 0xFFFF0000u) | val);
+                        for (int j = 0; j < 4; ++j)
+                            if (mb == mb_e && kgl == kgl_e && j == j_e)
+                                fa[mb][kgl][j] = upper ? ((fa[mb][kgl][j] & 0x0000FFFFu) | (val << 16))
+                                                       : ((fa[mb][kgl][j] & 0xFFFF0000u) | val);
+            }
         }
     };
     // activations (B operand) from the swizzled TMA block, then MMA
@@ -475,6 +522,8 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
     auto rec_x = [&](int q) { return x_s + (s * RPS + q) * C::kXBytes; };
 
     for (int i = 0; i < nrec;) {
+        // escape bits of the stage's records (bit cw: record i, bit 8 + cw: record i + 1)
+        const uint32_t em = (uint32_t)emask_s[i] | ((i + 1 < nrec) ? (uint32_t)emask_s[i + 1] << 8 : 0u);
         if (!mbar_try_wait(bar_full + 8 * s, full_phase) &&
             !mbar_wait(bar_full + 8 * s, full_phase, p.timeout_ns, p.status, abort_flag))
             return;
@@ -490,8 +539,8 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
                 Frag f0, f1;
                 decode_rec(rec_words(0), f0);
                 decode_rec(rec_words(1), f1);
-                patch_rec(i, f0);
-                patch_rec(i + 1, f1);
+                patch_rec(i, f0, (em >> cw) & 1u);
+                patch_rec(i + 1, f1, (em >> (8 + cw)) & 1u);
                 mma_rec(rec_x(0), f0);
                 mma_rec(rec_x(1), f1);
                 q += 2, i += 2, kt += 2;
@@ -499,7 +548,7 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
             } else {
                 Frag f0;
                 decode_rec(rec_words(q), f0);
-                patch_rec(i, f0);
+                patch_rec(i, f0, (em >> (8 * q + cw)) & 1u);
                 mma_rec(rec_x(q), f0);
                 ++q, ++i;
                 if (++kt == KT) kt = 0, ++nt;
