@@ -29,7 +29,6 @@ using namespace w12d;
 
 namespace {
 
-constexpr int kWarpsN = 4;            // consumer warps across the 128 channels (32 each)
 
 struct KParams {
     const uint8_t *rec;
@@ -55,11 +54,12 @@ struct KParams {
 
 // QV: the quick pass (only the 8 KB view plane of each record is read; the
 // low mantissa bits of in-window weights are taken as the midpoint 0b1000)
-template <int NB8, int WK, int RPS, bool QV = false>
+template <int NB8, int WK, int RPS, bool QV = false, int MB = 2>
 struct Cfg {
     static constexpr int kRecStride = QV ? w12i::kViewBytes : w12i::kRecBytes;   // bytes kept per record
     static constexpr int kRows = NB8 * 8;                     // rows per activation block
     static constexpr int kXBytes = kRows * 128;               // activation block: rows x 64 BF16
+    static constexpr int kWarpsN = 8 / MB;                    // consumer warps across the 128 channels (16 * MB each)
     static constexpr int kConsumerWarps = kWarpsN * WK;
     static constexpr int kConsumers = kConsumerWarps * 32;
     static constexpr int kThreads = kConsumers + 32;          // + producer warp
@@ -72,10 +72,10 @@ struct SmemPlan {
     int rec_off, x_off, red_off, bar_off, flag_off, escoff_off, esc_off, emask_off, base_off, total;
 };
 
-template <int NB8, int WK, int RPS, bool QV>
+template <int NB8, int WK, int RPS, bool QV, int MB>
 __host__ __device__ inline SmemPlan smem_plan(int stages, int max_recs, int esc_cap, int base_tiles)
 {
-    using C = Cfg<NB8, WK, RPS, QV>;
+    using C = Cfg<NB8, WK, RPS, QV, MB>;
     SmemPlan s;
     int o = 0;
     s.rec_off = o;
@@ -93,7 +93,7 @@ __host__ __device__ inline SmemPlan smem_plan(int stages, int max_recs, int esc_
     s.esc_off = o;
     o += esc_cap * 4;
     s.emask_off = o;
-    o += (max_recs + 15) / 16 * 16;
+    o += (max_recs * 2 + 15) / 16 * 16;
     s.base_off = o;
     o += base_tiles * w12i::kTileN;
     s.total = o + 1024;   // slack to align the window to 1024 bytes at run time
@@ -103,15 +103,15 @@ __host__ __device__ inline SmemPlan smem_plan(int stages, int max_recs, int esc_
 __device__ __forceinline__ int cta_of_record(int64_t r, int G, int64_t T) { return (int)(((r + 1) * G - 1) / T); }
 __device__ __forceinline__ int64_t first_record(int c, int G, int64_t T) { return (int64_t)c * T / G; }
 
-template <int NB8, int WK, int RPS, bool QV>
-__global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
+template <int NB8, int WK, int RPS, bool QV, int MB>
+__global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV, MB>::kThreads, 1)
     k_w12_gemm(const __grid_constant__ CUtensorMap xmap, const KParams p)
 {
-    using C = Cfg<NB8, WK, RPS, QV>;
+    using C = Cfg<NB8, WK, RPS, QV, MB>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // the 128-byte swizzle of the activation blocks needs 1024-byte alignment
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const SmemPlan sp = smem_plan<NB8, WK, RPS, QV>(p.stages, p.max_recs, p.esc_cap, p.base_tiles);
+    const SmemPlan sp = smem_plan<NB8, WK, RPS, QV, MB>(p.stages, p.max_recs, p.esc_cap, p.base_tiles);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, cta = blockIdx.x;
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
     int32_t *last_flag = reinterpret_cast<int32_t *>(smem + sp.flag_off + 4);
     int32_t *esc_off_s = reinterpret_cast<int32_t *>(smem + sp.escoff_off);
     uint32_t *esc_s = reinterpret_cast<uint32_t *>(smem + sp.esc_off);
-    uint8_t *emask_s = smem + sp.emask_off;
+    uint16_t *emask_s = reinterpret_cast<uint16_t *>(smem + sp.emask_off);
     uint8_t *base_s = smem + sp.base_off;
 
     if (threadIdx.x == 0) {
@@ -208,6 +208,7 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
 
     // ---------------------------------------------------------------- consumers
     const int cw = warp;                 // consumer warp 0 .. kConsumerWarps-1
+    constexpr int kWarpsN = C::kWarpsN;
     const int mw = cw % kWarpsN, wk = cw / kWarpsN;
     const int g = lane >> 2, t = lane & 3;
     const int ctid = threadIdx.x;        // 0 .. kConsumers-1
@@ -235,20 +236,20 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
         for (int i = ctid; i < esc_off_s[nrec] - e_lo; i += C::kConsumers) esc_s[i] = __ldg(p.esc + e_lo + i);
     // per record, a bit for every consumer warp whose part of the record
     // holds an escape: the record loop skips the escape list without reading it
-    static_assert(C::kConsumerWarps <= 8, "one mask byte per record");
+    static_assert(C::kConsumerWarps <= 16, "one 16-bit mask per record");
     for (int i = ctid; i < nrec; i += C::kConsumers) {
         uint32_t m = 0;
         for (int e = esc_off_s[i]; e < esc_off_s[i + 1]; ++e) {
             const uint32_t en = __ldg(p.esc + e);
             const int nl = (en >> 22) & 0x7F, kg = ((en >> 16) & 0x3F) >> 4;
-            m |= 1u << ((nl >> 5) + kWarpsN * (kg / C::kKgPerWarp));
+            m |= 1u << (nl / (16 * MB) + kWarpsN * (kg / C::kKgPerWarp));
         }
-        emask_s[i] = (uint8_t)m;
+        emask_s[i] = (uint16_t)m;
     }
     if (!cons_sync0()) return;
 
-    float acc[2][NB8][4];
-    ChanConst cc[2][2];
+    float acc[MB][NB8][4];
+    ChanConst cc[MB][2];
     int64_t cur_nt = -1;
     uint32_t cons_phase = cons_phase0;
     // barrier over the consumer threads with a bounded wait; false = aborted
@@ -262,16 +263,16 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
 
     auto load_consts = [&](int64_t nt) {
 #pragma unroll
-        for (int mb = 0; mb < 2; ++mb)
+        for (int mb = 0; mb < MB; ++mb)
 #pragma unroll
             for (int hi = 0; hi < 2; ++hi) {
-                const int ch = mw * 32 + mb * 16 + hi * 8 + g;
+                const int ch = mw * 16 * MB + mb * 16 + hi * 8 + g;
                 const uint32_t b = base_cached ? base_s[(nt - nt_first) * w12i::kTileN + ch]
                                                : __ldg(p.base + nt * w12i::kTileN + ch);
                 cc[mb][hi] = chan_const(b);
             }
 #pragma unroll
-        for (int mb = 0; mb < 2; ++mb)
+        for (int mb = 0; mb < MB; ++mb)
 #pragma unroll
             for (int nb = 0; nb < NB8; ++nb)
 #pragma unroll
@@ -284,10 +285,10 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
         if (*abort_flag) return false;
         // 1. every consumer warp drops its accumulators into red[wk][row][ch]
 #pragma unroll
-        for (int mb = 0; mb < 2; ++mb)
+        for (int mb = 0; mb < MB; ++mb)
 #pragma unroll
             for (int nb = 0; nb < NB8; ++nb) {
-                const int ch = mw * 32 + mb * 16 + g;
+                const int ch = mw * 16 * MB + mb * 16 + g;
                 const int row = nb * 8 + 2 * t;
                 float *rb = red + (wk * C::kRows) * C::kRedStride;
                 rb[row * C::kRedStride + ch] = acc[mb][nb][0];
@@ -416,7 +417,7 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
     // record loop; what varies inside it is a compile-time offset.
     //   view word (kg, mb, hi): thread base + kg*2048 + mb*256 + hi*128
     //   nibble word:            thread base + 8192 + (kg/2)*2048 + mb*256 + hi*128
-    const uint8_t *rec_thread = smem + sp.rec_off + (mw * 32 + g) * 16 + 4 * t;
+    const uint8_t *rec_thread = smem + sp.rec_off + (mw * 16 * MB + g) * 16 + 4 * t;
     uint32_t x_thread[C::kKgPerWarp];
 #pragma unroll
     for (int kgl = 0; kgl < C::kKgPerWarp; ++kgl) {
@@ -429,11 +430,11 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
             x_thread[kgl] = ((q >> 1) * 8 + (lane & 7)) * 128 + ((chunk ^ (lane & 7)) << 4);
         }
     }
-    using Frag = uint32_t[2][C::kKgPerWarp][4];
+    using Frag = uint32_t[MB][C::kKgPerWarp][4];
     // decode this warp's 32 channels x (16 * kKgPerWarp) K of one record
     auto decode_rec = [&](const uint32_t *rw, Frag &fa) {
 #pragma unroll
-        for (int mb = 0; mb < 2; ++mb) {
+        for (int mb = 0; mb < MB; ++mb) {
             uint32_t nib_lo = 0, nib_hi = 0;
 #pragma unroll
             for (int kgl = 0; kgl < C::kKgPerWarp; ++kgl) {
@@ -465,7 +466,7 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
             if (e < e1) {
                 en = esc_cached ? esc_s[e] : __ldg(p.esc + e_lo + e);
                 const int nl = (en >> 22) & 0x7F, kg = ((en >> 16) & 0x3F) >> 4;
-                own = (nl >> 5) == mw && (kg / C::kKgPerWarp) == wk;
+                own = nl / (16 * MB) == mw && (kg / C::kKgPerWarp) == wk;
             }
             uint32_t mine = __ballot_sync(0xffffffffu, own);
             while (mine) {
@@ -475,12 +476,12 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
                 const int nl = (ent >> 22) & 0x7F, kl = (ent >> 16) & 0x3F;
                 const int kk = kl & 15;
                 if (lane != ((nl & 7) * 4 + ((kk & 7) >> 1))) continue;
-                const int mb_e = (nl >> 4) & 1, kgl_e = (kl >> 4) % C::kKgPerWarp;
+                const int mb_e = (nl >> 4) % MB, kgl_e = (kl >> 4) % C::kKgPerWarp;
                 const int j_e = (kk >> 3) * 2 + ((nl >> 3) & 1);
                 const uint32_t val = ent & 0xFFFFu;
                 const bool upper = kk & 1;
 #pragma unroll
-                for (int mb = 0; mb < 2; ++mb)
+                for (int mb = 0; mb < MB; ++mb)
 #pragma unroll
                     for (int kgl = 0; kgl < C::kKgPerWarp; ++kgl)
 #pragma unroll
@@ -500,7 +501,7 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
                 uint32_t b0, b1;
                 ldsm_x2(xa, b0, b1);
 #pragma unroll
-                for (int mb = 0; mb < 2; ++mb) mma_bf16_16816(acc[mb][0], fa[mb][kgl], b0, b1);
+                for (int mb = 0; mb < MB; ++mb) mma_bf16_16816(acc[mb][0], fa[mb][kgl], b0, b1);
             } else {
                 uint32_t b[NB8][2];
                 ldsm_x4_off<0>(xa, b[0][0], b[0][1], b[1][0], b[1][1]);
@@ -512,7 +513,7 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
 #pragma unroll
                 for (int nb = 0; nb < NB8; ++nb)
 #pragma unroll
-                    for (int mb = 0; mb < 2; ++mb) mma_bf16_16816(acc[mb][nb], fa[mb][kgl], b[nb][0], b[nb][1]);
+                    for (int mb = 0; mb < MB; ++mb) mma_bf16_16816(acc[mb][nb], fa[mb][kgl], b[nb][0], b[nb][1]);
             }
         }
     };
@@ -522,8 +523,8 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
     auto rec_x = [&](int q) { return x_s + (s * RPS + q) * C::kXBytes; };
 
     for (int i = 0; i < nrec;) {
-        // escape bits of the stage's records (bit cw: record i, bit 8 + cw: record i + 1)
-        const uint32_t em = (uint32_t)emask_s[i] | ((i + 1 < nrec) ? (uint32_t)emask_s[i + 1] << 8 : 0u);
+        // escape bits of the stage's records (bit cw: record i, bit 16 + cw: record i + 1)
+        const uint32_t em = (uint32_t)emask_s[i] | ((i + 1 < nrec) ? (uint32_t)emask_s[i + 1] << 16 : 0u);
         if (!mbar_try_wait(bar_full + 8 * s, full_phase) &&
             !mbar_wait(bar_full + 8 * s, full_phase, p.timeout_ns, p.status, abort_flag))
             return;
@@ -540,7 +541,7 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
                 decode_rec(rec_words(0), f0);
                 decode_rec(rec_words(1), f1);
                 patch_rec(i, f0, (em >> cw) & 1u);
-                patch_rec(i + 1, f1, (em >> (8 + cw)) & 1u);
+                patch_rec(i + 1, f1, (em >> (16 + cw)) & 1u);
                 mma_rec(rec_x(0), f0);
                 mma_rec(rec_x(1), f1);
                 q += 2, i += 2, kt += 2;
@@ -548,7 +549,7 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV>::kThreads, 1)
             } else {
                 Frag f0;
                 decode_rec(rec_words(q), f0);
-                patch_rec(i, f0, (em >> (8 * q + cw)) & 1u);
+                patch_rec(i, f0, (em >> (16 * q + cw)) & 1u);
                 mma_rec(rec_x(q), f0);
                 ++q, ++i;
                 if (++kt == KT) kt = 0, ++nt;
@@ -615,10 +616,10 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-template <int NB8, int WK, int RPS, bool QV = false>
+template <int NB8, int WK, int RPS, bool QV = false, int MB = 2>
 int launch_t(const w12i::GemmArgs &a, const CUtensorMap &xmap, cudaStream_t st)
 {
-    using C = Cfg<NB8, WK, RPS, QV>;
+    using C = Cfg<NB8, WK, RPS, QV, MB>;
     const int64_t T = (int64_t)a.w.n_tiles * a.w.k_tiles;
     const int G = (int)std::min<int64_t>(a.num_sms, T);
     const int max_recs = (int)((T + G - 1) / G);
@@ -646,16 +647,16 @@ int launch_t(const w12i::GemmArgs &a, const CUtensorMap &xmap, cudaStream_t st)
     p.base_tiles = std::min<int>(64, (int)(max_recs / a.w.k_tiles + 2));
     const int budget = 227 * 1024;
     int stages = 8;
-    while (stages > 2 && smem_plan<NB8, WK, RPS, QV>(stages, max_recs, p.esc_cap, p.base_tiles).total > budget)
+    while (stages > 2 && smem_plan<NB8, WK, RPS, QV, MB>(stages, max_recs, p.esc_cap, p.base_tiles).total > budget)
         --stages;
     p.stages = stages;
-    const int smem = smem_plan<NB8, WK, RPS, QV>(stages, max_recs, p.esc_cap, p.base_tiles).total;
+    const int smem = smem_plan<NB8, WK, RPS, QV, MB>(stages, max_recs, p.esc_cap, p.base_tiles).total;
     if (smem > budget) return (int)cudaErrorInvalidConfiguration;
     cudaError_t e =
-        cudaFuncSetAttribute(k_w12_gemm<NB8, WK, RPS, QV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaFuncSetAttribute(k_w12_gemm<NB8, WK, RPS, QV, MB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return (int)e;
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, k_w12_gemm<NB8, WK, RPS, QV>);
+    e = cudaFuncGetAttributes(&fa, k_w12_gemm<NB8, WK, RPS, QV, MB>);
     if (e != cudaSuccess) return (int)e;
     if (fa.maxThreadsPerBlock < C::kThreads) return (int)cudaErrorLaunchOutOfResources;
     cudaLaunchConfig_t cfg{};
@@ -668,7 +669,7 @@ int launch_t(const w12i::GemmArgs &a, const CUtensorMap &xmap, cudaStream_t st)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 1 : 0;
-    return (int)cudaLaunchKernelEx(&cfg, k_w12_gemm<NB8, WK, RPS, QV>, xmap, p);
+    return (int)cudaLaunchKernelEx(&cfg, k_w12_gemm<NB8, WK, RPS, QV, MB>, xmap, p);
 }
 
 }  // namespace
@@ -691,20 +692,23 @@ int launch_gemm(const GemmArgs &a, void *stream)
                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return (int)cudaErrorInvalidValue;
-    // 8 consumer warps (two 16-K groups each); two records per stage up to 32
-    // rows (one wait and one release per 24 KB), one record per stage at 64 rows
+    // Two 16-K groups of consumer warps: 16 warps of 16 channels up to 16 rows
+    // (more warps hide the decode chain's latency; the register cap of 544
+    // threads still fits those row counts), 8 warps of 32 channels above.  Two
+    // records per stage up to 32 rows (one wait and one release per 24 KB),
+    // one record per stage at 64 rows.
     if (a.qview) {
         switch (nb8) {
-        case 1: return launch_t<1, 2, 2, true>(a, xmap, st);
-        case 2: return launch_t<2, 2, 2, true>(a, xmap, st);
-        case 4: return launch_t<4, 2, 2, true>(a, xmap, st);
+        case 1: return launch_t<1, 2, 2, true, 1>(a, xmap, st);
+        case 2: return launch_t<2, 2, 2, true, 1>(a, xmap, st);
+        case 4: return launch_t<4, 2, 2, true, 2>(a, xmap, st);
         default: return launch_t<8, 2, 1, true>(a, xmap, st);
         }
     }
     switch (nb8) {
-    case 1: return launch_t<1, 2, 2>(a, xmap, st);
-    case 2: return launch_t<2, 2, 2>(a, xmap, st);
-    case 4: return launch_t<4, 2, 2>(a, xmap, st);
+    case 1: return launch_t<1, 2, 2, false, 1>(a, xmap, st);
+    case 2: return launch_t<2, 2, 2, false, 1>(a, xmap, st);
+    case 4: return launch_t<4, 2, 2, false, 2>(a, xmap, st);
     default: return launch_t<8, 2, 1>(a, xmap, st);
     }
 }
