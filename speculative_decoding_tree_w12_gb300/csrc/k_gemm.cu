@@ -29,7 +29,6 @@ using namespace w12d;
 
 namespace {
 
-
 struct KParams {
     const uint8_t *rec;
     const uint8_t *base;
@@ -335,17 +334,26 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV, MB>::kThreads, 1)
             finish = *last_flag != 0;
             if (finish) {
                 __threadfence();
-                // 3. the last contributor sums every partial in CTA order into red[0]
+                // 3. the last contributor sums every partial in CTA order into
+                // red[0].  Every contributor after the first starts inside this
+                // tile (its slot 0); the first one's slot depends on where it starts.
+                const int sl_first = (first_record(c_first, G, T) >= t0) ? 0 : 1;
+                const float *part0 = p.partial + (int64_t)(c_first * 2 + sl_first) * C::kRows * w12i::kTileN;
+                const float *part1 = p.partial + (int64_t)((c_first + 1) * 2) * C::kRows * w12i::kTileN;
+                constexpr int64_t kSlot2 = 2 * (int64_t)C::kRows * w12i::kTileN;   // floats between CTAs' slot 0
                 for (int e = ctid; e < rows * 32; e += C::kConsumers) {
-                    const int row = e >> 5, c4 = (e & 31) * 4;
+                    const int off = (e >> 5) * w12i::kTileN + (e & 31) * 4;
                     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int c = c_first; c <= c_last; ++c) {
-                        const int sl = (nt == first_record(c, G, T) / KT) ? 0 : 1;
-                        const float *src = p.partial + ((int64_t)(c * 2 + sl) * C::kRows) * w12i::kTileN;
-                        const float4 w = __ldcg(reinterpret_cast<const float4 *>(src + row * w12i::kTileN + c4));
+                    {
+                        const float4 w = __ldcg(reinterpret_cast<const float4 *>(part0 + off));
                         v.x += w.x, v.y += w.y, v.z += w.z, v.w += w.w;
                     }
-                    *reinterpret_cast<float4 *>(red + row * C::kRedStride + c4) = v;
+#pragma unroll 4
+                    for (int c = 0; c < c_last - c_first; ++c) {
+                        const float4 w = __ldcg(reinterpret_cast<const float4 *>(part1 + c * kSlot2 + off));
+                        v.x += w.x, v.y += w.y, v.z += w.z, v.w += w.w;
+                    }
+                    *reinterpret_cast<float4 *>(red + (e >> 5) * C::kRedStride + (e & 31) * 4) = v;
                 }
                 if (ctid == 0) p.counters[nt] = 0;   // ready for the next launch using this slot
                 if (!cons_sync()) return false;
