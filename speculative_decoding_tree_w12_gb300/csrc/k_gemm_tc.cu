@@ -194,12 +194,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
             const int pre = min(S, npairs);
             for (int m = 0; m < pre; ++m) issue(m, m);
             int issued = pre;
+            // slot and reuse parity of pair m, advanced without divisions
+            int sl = pre % S;
+            uint32_t rph = (uint32_t)((pre / S) - 1) & 1u;
             for (int m = pre; m < npairs; ++m) {
-                const int sl = m % S;
                 // slot sl last held pair m - S: every decode warp must have read it
-                if (!mbar_wait(bar_rempty + 8 * sl, ((m / S) - 1) & 1, p.timeout_ns, p.status, abort_flag)) break;
+                if (!mbar_wait(bar_rempty + 8 * sl, rph, p.timeout_ns, p.status, abort_flag)) break;
                 issue(m, sl);
                 issued = m + 1;
+                if (++sl == S) sl = 0, rph ^= 1u;
             }
             if (*abort_flag) {
                 // leave no copy in flight
@@ -237,22 +240,38 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
             ChanConst cc{0, 0};
             // every record of the group is visited: work is skipped after a
             // timeout, but the hand-off to the MMA warp always takes place
+            // per-record indices advanced without divisions: pair m = i / 2 in
+            // slot s (fill parity sph), tile nt / k-tile kt of record i, A
+            // buffer ab, activation slot iq (fill parity iph)
+            int m = 0, s = 0;
+            uint32_t sph = 0;
+            int64_t nt = (rec_begin + g) / KT;
+            int kt = (int)((rec_begin + g) - nt * KT);
+            int ab = 0, iq = g;
+            uint32_t iph = 0;
             for (int j = 0;; ++j) {
                 const int i = g + j * GR;
                 if (i >= nrec) break;
-                const int m = i >> 1, s = m % S;          // record pair m holds records 2m, 2m + 1
-                const int64_t r = rec_begin + i;
-                const int64_t nt = r / KT;
-                const int ab = j % NAG;
+                if (j > 0) {
+                    while (m < (i >> 1)) {   // record pair m holds records 2m, 2m + 1
+                        ++m;
+                        if (++s == S) s = 0, sph ^= 1u;
+                    }
+                    kt += GR;
+                    while (kt >= KT) kt -= KT, ++nt;
+                    if (++ab == NAG) ab = 0;
+                    iq += GR;
+                    if (iq >= Q) iq -= Q, iph ^= 1u;
+                }
                 bool ok = !*abort_flag;
-                if (ok) ok = mbar_wait(bar_rfull + 8 * s, (m / S) & 1, p.timeout_ns, p.status, abort_flag);
+                if (ok) ok = mbar_wait(bar_rfull + 8 * s, sph, p.timeout_ns, p.status, abort_flag);
                 if (i >= Q) {
                     // A buffer ab last held record i - Q: its MMAs must be done.
                     // The MMA warp commits every record, so this wait ends even
                     // after an abort; it is never skipped (the buffer's named
                     // barrier is reused only after its sync).
                     int32_t no_abort = 0;
-                    if (!mbar_wait(bar_done + 8 * (i % Q), ((i / Q) - 1) & 1, p.timeout_ns, p.status, &no_abort)) ok = false;
+                    if (!mbar_wait(bar_done + 8 * iq, iph ^ 1u, p.timeout_ns, p.status, &no_abort)) ok = false;
                 }
                 ok = __all_sync(0xffffffffu, ok && !*abort_flag);
                 if (ok) {
@@ -309,9 +328,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
         const uint32_t idesc = idesc_bf16_f32(128, NR);
         int tcount = 0, dcur = 0;
         int kt = (int)(rec_begin - nt_first * KT);
+        // group g, A buffer ab and activation slot xs (fill parity xph) of
+        // record i, advanced without divisions
+        int g = 0, ab = 0, xs = 0;
+        uint32_t xph = 0;
         for (int i = 0; i < nrec; ++i) {
-            const int g = i % GR, j = i / GR;
-            const int xs = i % Q, ab = j % NAG;
+            if (i > 0) {
+                if (++g == GR) {
+                    g = 0;
+                    if (++ab == NAG) ab = 0;
+                }
+                if (++xs == Q) xs = 0, xph ^= 1u;
+            }
             named_bar(kBarA0 + g * NAG + ab, 160);
             // the whole warp runs this part (it stays converged); one elected
             // lane issues the tensor-core instructions
@@ -319,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
             const bool first = (i == 0) || kt == 0;
             const bool last = (i == nrec - 1) || kt == KT - 1;
             bool go = !*abort_flag;
-            if (go) go = mbar_wait(bar_xfull + 8 * xs, (i / Q) & 1, p.timeout_ns, p.status, abort_flag);
+            if (go) go = mbar_wait(bar_xfull + 8 * xs, xph, p.timeout_ns, p.status, abort_flag);
             go = __all_sync(0xffffffffu, go);
             if (first) {
                 dcur = tcount % DB;
@@ -468,14 +496,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
         prefetch_tmap(&xmap);
         pdl_wait();   // activations come from the previous kernel
         int issued = 0;
+        int xs = 0, kt = (int)(rec_begin - nt_first * KT);
+        uint32_t xph = 0;   // fill parity of slot xs
         for (int i = 0; i < nrec; ++i) {
-            const int xs = i % Q;
             // slot xs last held record i - Q: its MMAs must be done
-            if (i >= Q && !mbar_wait(bar_done + 8 * xs, ((i / Q) - 1) & 1, p.timeout_ns, p.status, abort_flag)) break;
+            if (i >= Q && !mbar_wait(bar_done + 8 * xs, xph ^ 1u, p.timeout_ns, p.status, abort_flag)) break;
             mbar_expect_tx(bar_xfull + 8 * xs, xb);
             if (!(drop_first && i == 0))
-                tma_load_2d(x_s + xs * xb, &xmap, (int)((rec_begin + i) % KT) * w12i::kTileK, 0, bar_xfull + 8 * xs);
+                tma_load_2d(x_s + xs * xb, &xmap, kt * w12i::kTileK, 0, bar_xfull + 8 * xs);
             issued = i + 1;
+            if (++xs == Q) xs = 0, xph ^= 1u;
+            if (++kt == KT) kt = 0;
         }
         if (*abort_flag) {
             int32_t no_abort = 0;

@@ -90,6 +90,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tree_build(const TreeParams p)
     const int tid = threadIdx.x, lane = tid & 31;
     const int NC = p.n_cand, PM = p.p_max;
 
+    // the next kernel (the first verify GEMM) may start now: it streams weights
+    // into its shared memory and waits for this grid before it reads rows
+    pdl_launch_dependents();
     pdl_wait();
     if (tid == 0) n.bad = 0;
     for (int r = tid; r < p.n_req; r += kThreads) n.p_r[r] = p.p_r[r];
@@ -278,7 +281,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_tree_build(const TreeParams p)
         for (int k = 0; k < R; ++k) c += (int)(n.dr[k] & 0xFFFF) < r;
         p.req_row_off[r] = c;
     }
-    pdl_launch_dependents();
 }
 
 // one warp per request: walk down from the root along children whose token
