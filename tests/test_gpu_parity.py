@@ -265,6 +265,44 @@ def test_tree_build_bit_exact(w12, name, kw):
     _tree_equal(t.host(), ref)
 
 
+def _tree_case(w12, lat, budget):
+    ref = oracle.tree_build(lat, budget)
+    dl = w12.DeviceLattice(lat)
+    ws = w12.Workspace(1, 0, 0, lat.n_req)
+    t = w12.w12_tree_build(dl, budget, ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    assert t.R == ref.R
+    _tree_equal(t.host(), ref)
+
+
+@pytest.mark.parametrize("n_req,budget", [(2, 40), (3, 7), (31, 200), (33, 100)])
+def test_tree_build_request_counts(w12, n_req, budget):
+    """One warp per request covers 2..32 requests; 33 goes to the one-warp build."""
+    w = synth.scaled(synth.WORKLOADS["batched_27b"], vocab=4096, hidden=512, n_req=n_req, budget=budget, seed=11)
+    _tree_case(w12, synth.lattice(w), budget)
+
+
+def test_tree_build_one_request_dominates(w12):
+    """A request whose edges are almost free takes nearly the whole budget:
+    more nodes than a per-request store holds, so the build falls back to the
+    one-warp selection."""
+    w = synth.scaled(synth.WORKLOADS["batched_27b"], vocab=4096, hidden=512, n_req=4, budget=200, seed=12)
+    lat = synth.lattice(w)
+    lat.cand_logp[0] = np.float32(-1e-4)
+    lat.p_r[0] = 16
+    _tree_case(w12, lat, 200)
+
+
+def test_tree_build_equal_scores(w12):
+    """Every edge has the same log-probability: the order falls to depth,
+    request and path, across the per-request warps."""
+    w = synth.scaled(synth.WORKLOADS["batched_27b"], vocab=4096, hidden=512, n_req=8, budget=120, seed=13)
+    lat = synth.lattice(w)
+    lat.cand_logp[:] = np.float32(-0.5)
+    _tree_case(w12, lat, 120)
+
+
 def test_tree_build_flags_positive_logp(w12):
     w = synth.scaled(synth.WORKLOADS["single_27b"], vocab=4096, hidden=512)
     lat = synth.lattice(w)
