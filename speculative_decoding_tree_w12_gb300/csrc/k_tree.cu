@@ -179,6 +179,15 @@ __device__ __forceinline__ WarpMax warp_max(unsigned long long b1, unsigned long
     WarpMax w;
     w.M1 = __reduce_max_sync(0xffffffffu, h1);
     bool m = h1 == w.M1;
+    const uint32_t top = __ballot_sync(0xffffffffu, m);
+    if ((top & (top - 1)) == 0) {
+        // one lane holds the best score: its other words come by shuffle
+        w.lane = __ffs(top) - 1;
+        w.M2 = __shfl_sync(0xffffffffu, l1, w.lane);
+        w.M3 = __shfl_sync(0xffffffffu, h2, w.lane);
+        w.M4 = __shfl_sync(0xffffffffu, l2, w.lane);
+        return w;
+    }
     w.M2 = __reduce_max_sync(0xffffffffu, m ? l1 : 0u);
     m = m && l1 == w.M2;
     w.M3 = __reduce_max_sync(0xffffffffu, m ? h2 : 0u);
@@ -454,7 +463,9 @@ __global__ void __launch_bounds__(1024, 1) k_tree_build_par(const TreeParams p)
     // per-request generation passes
     unsigned long long b1 = 0, b2 = 0;
     int bx = -1, t = 1;
-    int limit = min(kPW, 1 + 2 * ((B + NR - 1) / NR) + 2);
+    // first limit: the average share plus a little; unsettled requests grow
+    // their limit by half each pass
+    int limit = min(kPW, 1 + (B + NR - 1) / NR + 2);
     ReqNodes &q = s.rn[warp];
     add_root(q, L, NC, p_r, 0, warp, p.root_tok[warp], b1, b2, bx);
     bool settled = false;
@@ -476,7 +487,7 @@ __global__ void __launch_bounds__(1024, 1) k_tree_build_par(const TreeParams p)
                 atomicAdd(&s.pending, 1);
                 if (limit == kPW) s.overflow = 1;
             }
-            if (!settled) limit = min(kPW, 2 * limit);
+            if (!settled) limit = min(kPW, limit + max(2, limit / 2));
         }
         __syncthreads();
         const int pending = s.pending, overflow = s.overflow;
