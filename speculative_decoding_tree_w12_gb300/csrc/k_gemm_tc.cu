@@ -6,11 +6,11 @@
 // memory:
 //
 //   record producer  one 24 KB bulk copy per pair of consecutive records (L2
-//                    evict-first) into a ring; a slot is handed back as soon as
-//                    the decode warps have read it into registers, so most of
-//                    the ring is always in flight
-//   activation warp  2-D TMA of each record's activation block (128-byte
-//                    swizzle) into a second ring, freed by the record's commit
+//                    evict-first) into a ring, and right behind it the pair's
+//                    two activation blocks (2-D TMA, 128-byte swizzle) into an
+//                    activation ring; a record slot is handed back as soon as
+//                    the decode warps have read the pair into registers, an
+//                    activation slot once the pair's MMAs are done
 //   decode groups    one or two groups of four warps (one per tensor-memory
 //                    lane quarter); a group takes every G-th record of the
 //                    CTA.  Thread = output channel: six 16-byte shared loads,
@@ -21,8 +21,9 @@
 //   MMA warp         takes the records in order: a named-barrier sync on the
 //                    record's A buffer, then one elected lane issues the
 //                    record's four MMAs (M = 128 channels, N = rows rounded up
-//                    to 32, K = 16) into the tile's FP32 accumulator and one
-//                    commit that frees the activation slot and the A buffer
+//                    to 32, K = 16) into the tile's FP32 accumulator, a commit
+//                    that frees the A buffer and, after a pair, one that frees
+//                    the activation slot
 //   epilogue warps   tcgen05.ld of a finished tile's accumulator; BF16 rows,
 //                    or the tile's (max, index) per row for the LM head; a
 //                    tile split between CTAs is published as a partial and
@@ -50,8 +51,7 @@ constexpr int kGroupWarp0 = 1;     // decode group g = warps 1 + 4g .. 4 + 4g
 constexpr int kMaxGroups = 2;
 constexpr int kMmaWarp = 1 + 4 * kMaxGroups;    // warp 9
 constexpr int kEpiWarp0 = kMmaWarp + 1;          // warps 10..13
-constexpr int kXWarp = kEpiWarp0 + 4;            // warp 14: activation copies
-constexpr int kThreads = (kXWarp + 1) * 32;
+constexpr int kThreads = (kEpiWarp0 + 4) * 32;   // 14 warps
 constexpr int kRecPair = 2 * w12i::kRecBytes;
 constexpr int kACols = 32;
 constexpr uint32_t kTmemCols = 512;
@@ -68,6 +68,7 @@ struct TcParams {
     int32_t groups;      // decode groups (1 or 2)
     int32_t a_bufs;      // A buffers per group
     int32_t d_bufs;      // tile accumulators (1 or 2)
+    int32_t x_slots;     // activation ring: slots of one record pair's activation blocks
     uint16_t *y;
     int64_t ldy;
     float *s1_val;
@@ -87,17 +88,17 @@ struct Plan {
     int rec, x, bars, misc, escoff, esc, base, red, total;
 };
 
-// q = activation slots (= groups * A buffers per group)
-__host__ __device__ inline Plan plan(int stages, int q, int nr, int max_recs, int esc_cap, int base_tiles)
+// q = A buffers over all groups; sx = activation pair slots
+__host__ __device__ inline Plan plan(int stages, int q, int sx, int nr, int max_recs, int esc_cap, int base_tiles)
 {
     Plan p;
     int o = 0;
     p.rec = o;
     o += stages * kRecPair;                   // 24 KB per slot keeps the 1024-byte alignment
     p.x = o;
-    o += q * nr * 128;
+    o += sx * 2 * nr * 128;
     p.bars = o;
-    o += 8 * (2 * stages + 2 * q + 2 * 2 + 1);   // rec full/empty, x full, done, acc full/empty, epilogue
+    o += 8 * (2 * stages + q + 2 * sx + 2 * 2 + 1);   // rec full/empty, A done, x full/done, acc full/empty, epilogue
     p.misc = o;
     o += 32;
     p.escoff = o;
@@ -115,6 +116,14 @@ __host__ __device__ inline Plan plan(int stages, int q, int nr, int max_recs, in
 __device__ __forceinline__ int cta_of_record(int64_t r, int G, int64_t T) { return (int)(((r + 1) * G - 1) / T); }
 __device__ __forceinline__ int64_t first_record(int c, int G, int64_t T) { return (int64_t)c * T / G; }
 
+// one lane of a converged warp
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t e;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
+    return e != 0;
+}
+
 __device__ __forceinline__ void named_arrive(int id, int threads)
 {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
@@ -124,9 +133,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const int S = p.stages, NR = p.nr, GR = p.groups, NAG = p.a_bufs, DB = p.d_bufs;
+    const int S = p.stages, NR = p.nr, GR = p.groups, NAG = p.a_bufs, DB = p.d_bufs, SX = p.x_slots;
     const int Q = GR * NAG;
-    const Plan pl = plan(S, Q, NR, p.max_recs, p.esc_cap, p.base_tiles);
+    const Plan pl = plan(S, Q, SX, NR, p.max_recs, p.esc_cap, p.base_tiles);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, cta = blockIdx.x;
     const int KT = p.k_tiles;
@@ -140,8 +149,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
     const uint32_t xb = (uint32_t)NR * 128;
     const uint32_t bar0 = smem_u32(smem + pl.bars);
     const uint32_t bar_rfull = bar0, bar_rempty = bar0 + 8 * S;
-    const uint32_t bar_xfull = bar_rempty + 8 * S, bar_done = bar_xfull + 8 * Q;
-    const uint32_t bar_accfull = bar_done + 8 * Q, bar_accempty = bar_accfull + 16;
+    const uint32_t bar_done = bar_rempty + 8 * S;
+    const uint32_t bar_xfull = bar_done + 8 * Q, bar_xdone = bar_xfull + 8 * SX;
+    const uint32_t bar_accfull = bar_xdone + 8 * SX, bar_accempty = bar_accfull + 16;
     const uint32_t bar_epi = bar_accempty + 16;
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(smem + pl.misc);
     int32_t *last_flag = reinterpret_cast<int32_t *>(smem + pl.misc + 4);
@@ -156,9 +166,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
             mbar_init(bar_rfull + 8 * s, 1);    // producer's expect_tx arrival + the copy's bytes
             mbar_init(bar_rempty + 8 * s, 8);   // the decode warps have read both records of the pair
         }
-        for (int s = 0; s < Q; ++s) {
-            mbar_init(bar_xfull + 8 * s, 1);    // activation warp's expect_tx arrival + the block
-            mbar_init(bar_done + 8 * s, 1);     // one commit per record: its MMAs are done
+        for (int s = 0; s < Q; ++s) mbar_init(bar_done + 8 * s, 1);   // one commit per record: its MMAs are done
+        for (int s = 0; s < SX; ++s) {
+            mbar_init(bar_xfull + 8 * s, 1);    // producer's expect_tx arrival + the pair's activation blocks
+            mbar_init(bar_xdone + 8 * s, 1);    // one commit per pair: the MMAs reading the slot are done
         }
         for (int d = 0; d < 2; ++d) {
             mbar_init(bar_accfull + 8 * d, 1);    // commit after a tile's last MMA
@@ -190,26 +201,54 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
                     bulk_g2s(rec_s + sl * kRecPair, p.rec + (rec_begin + 2 * m) * (int64_t)w12i::kRecBytes,
                              (uint32_t)(n * w12i::kRecBytes), bar_rfull + 8 * sl, pol);
             };
-            // weights do not depend on earlier kernels: no programmatic-dependency wait
+            // activation blocks of pair m (k-tile kt0 for its first record) into
+            // pair slot xsl, right behind the pair's records in the copy queue
+            auto issue_x = [&](int m, int xsl, int kt0) {
+                const int n = min(2, nrec - 2 * m);
+                mbar_expect_tx(bar_xfull + 8 * xsl, (uint32_t)n * xb);
+                if (drop_first && m == 0) return;
+                for (int r = 0; r < n; ++r) {
+                    const int kt = (kt0 + r < KT) ? kt0 + r : kt0 + r - KT;
+                    tma_load_2d(x_s + (uint32_t)(xsl * 2 + r) * xb, &xmap, kt * w12i::kTileK, 0, bar_xfull + 8 * xsl);
+                }
+            };
+            prefetch_tmap(&xmap);
+            // weights do not depend on earlier kernels: they start before the
+            // programmatic-dependency wait, the activations after it
             const int pre = min(S, npairs);
             for (int m = 0; m < pre; ++m) issue(m, m);
+            pdl_wait();
+            int kt0 = (int)(rec_begin - nt_first * KT);   // k-tile of record 2m
+            auto adv = [&]() {
+                kt0 += 2;
+                while (kt0 >= KT) kt0 -= KT;
+            };
+            for (int m = 0; m < pre; ++m) issue_x(m, m, kt0), adv();
             int issued = pre;
-            // slot and reuse parity of pair m, advanced without divisions
-            int sl = pre % S;
-            uint32_t rph = (uint32_t)((pre / S) - 1) & 1u;
+            // record slot / activation slot of pair m and their reuse parities,
+            // advanced without divisions (the activation ring is at least as deep)
+            int sl = pre % S, xsl = pre % SX;
+            uint32_t rph = (uint32_t)((pre / S) - 1) & 1u, xph = (uint32_t)((pre / SX) - 1) & 1u;
             for (int m = pre; m < npairs; ++m) {
                 // slot sl last held pair m - S: every decode warp must have read it
                 if (!mbar_wait(bar_rempty + 8 * sl, rph, p.timeout_ns, p.status, abort_flag)) break;
+                // activation slot xsl last held pair m - SX: its MMAs must be done
+                if (m >= SX && !mbar_wait(bar_xdone + 8 * xsl, xph, p.timeout_ns, p.status, abort_flag)) break;
                 issue(m, sl);
+                issue_x(m, xsl, kt0);
+                adv();
                 issued = m + 1;
                 if (++sl == S) sl = 0, rph ^= 1u;
+                if (++xsl == SX) xsl = 0, xph ^= 1u;
             }
             if (*abort_flag) {
                 // leave no copy in flight
                 int32_t no_abort = 0;
-                for (int m = max(0, issued - S); m < issued; ++m) {
+                for (int m = max(0, issued - SX); m < issued; ++m) {
                     if (drop_first && m == 0) continue;
-                    mbar_wait(bar_rfull + 8 * (m % S), (m / S) & 1, p.timeout_ns, p.status, &no_abort);
+                    if (m >= issued - S)
+                        mbar_wait(bar_rfull + 8 * (m % S), (m / S) & 1, p.timeout_ns, p.status, &no_abort);
+                    mbar_wait(bar_xfull + 8 * (m % SX), (m / SX) & 1, p.timeout_ns, p.status, &no_abort);
                 }
             }
         }
@@ -328,9 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
         const uint32_t idesc = idesc_bf16_f32(128, NR);
         int tcount = 0, dcur = 0;
         int kt = (int)(rec_begin - nt_first * KT);
-        // group g, A buffer ab and activation slot xs (fill parity xph) of
-        // record i, advanced without divisions
-        int g = 0, ab = 0, xs = 0;
+        // group g, A buffer ab, A-buffer done slot aq and activation pair slot
+        // xsl (fill parity xph) of record i, advanced without divisions
+        int g = 0, ab = 0, aq = 0, xsl = 0;
         uint32_t xph = 0;
         for (int i = 0; i < nrec; ++i) {
             if (i > 0) {
@@ -338,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
                     g = 0;
                     if (++ab == NAG) ab = 0;
                 }
-                if (++xs == Q) xs = 0, xph ^= 1u;
+                if (++aq == Q) aq = 0;
             }
             named_bar(kBarA0 + g * NAG + ab, 160);
             // the whole warp runs this part (it stays converged); one elected
@@ -346,8 +385,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
             tc_fence_after();
             const bool first = (i == 0) || kt == 0;
             const bool last = (i == nrec - 1) || kt == KT - 1;
+            const bool pair_end = (i & 1) || i == nrec - 1;
             bool go = !*abort_flag;
-            if (go) go = mbar_wait(bar_xfull + 8 * xs, xph, p.timeout_ns, p.status, abort_flag);
+            if (go && (i & 1) == 0) go = mbar_wait(bar_xfull + 8 * xsl, xph, p.timeout_ns, p.status, abort_flag);
             go = __all_sync(0xffffffffu, go);
             if (first) {
                 dcur = tcount % DB;
@@ -357,18 +397,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
                 go = __all_sync(0xffffffffu, go);
                 tc_fence_after();
             }
-            if (go) {
-                const uint32_t d_t = tmem + d_col(dcur), a_t = tmem + a_col(g, ab);
-                const uint64_t bd = smem_desc_sw128(x_s + xs * xb);
+            if (elect_one()) {
+                if (go) {
+                    const uint32_t d_t = tmem + d_col(dcur), a_t = tmem + a_col(g, ab);
+                    const uint64_t bd = smem_desc_sw128(x_s + (uint32_t)(xsl * 2 + (i & 1)) * xb);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    tc_mma_ts_elect(d_t, a_t + ks * 8, bd + (uint64_t)(ks * 2), idesc, (first && ks == 0) ? 0u : 1u);
+                    for (int ks = 0; ks < 4; ++ks)
+                        tc_mma_ts(d_t, a_t + ks * 8, bd + (uint64_t)(ks * 2), idesc, (first && ks == 0) ? 0u : 1u);
+                }
+                tc_commit(bar_done + 8 * aq);                 // always: frees the A buffer
+                if (pair_end) tc_commit(bar_xdone + 8 * xsl);   // always: frees the activation slot
+                if (last && go) tc_commit(bar_accfull + 8 * dcur);
             }
-            tc_commit_elect(bar_done + 8 * xs);   // always: frees the activation slot and the A buffer
-            if (last) {
-                if (go) tc_commit_elect(bar_accfull + 8 * dcur);
-                ++tcount;
-            }
+            __syncwarp();
+            if (last) ++tcount;
+            if (pair_end && ++xsl == SX) xsl = 0, xph ^= 1u;
             if (++kt == KT) kt = 0;
         }
         // tensor memory is released only after every issued MMA finished
@@ -376,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
             int32_t no_abort = 0;
             mbar_wait(bar_done + 8 * ((nrec - 1) % Q), ((nrec - 1) / Q) & 1, p.timeout_ns, p.status, &no_abort);
         }
-    } else if (warp < kXWarp) {
+    } else {
         // ------------------------------------------------------------- epilogue
         const int quarter = warp & 3;
         const int c = quarter * 32 + lane;
@@ -402,19 +445,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
                 for (int j = 0; j < 32; ++j)
                     if (r0 + j < rows) yc[(int64_t)(r0 + j) * p.ldy] = (uint16_t)(pack_bf16x2(v[j], 0.f) & 0xFFFFu);
             } else {
+                // (max, lowest index) over the warp's 32 channels for 32 rows at
+                // once: at each of five steps a lane keeps half of its rows,
+                // trades the other half with its partner and combines; lane l
+                // ends with row r0 + l (31 trades instead of 32 x 5)
+                float bv[32];
+                int32_t bi[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    if (r0 + j >= rows) break;
-                    float bv = v[j];
-                    int32_t bi = c;
+                for (int j = 0; j < 32; ++j) bv[j] = v[j], bi[j] = c;
 #pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) {
-                        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                        const int32_t oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                        if (beats(ov, oi, bv, bi)) bv = ov, bi = oi;
+                for (int h = 16; h > 0; h >>= 1) {
+                    const bool upper = (lane & h) != 0;
+#pragma unroll
+                    for (int k = 0; k < h; ++k) {
+                        const float keep_v = upper ? bv[h + k] : bv[k], send_v = upper ? bv[k] : bv[h + k];
+                        const int32_t keep_i = upper ? bi[h + k] : bi[k], send_i = upper ? bi[k] : bi[h + k];
+                        const float ov = __shfl_xor_sync(0xffffffffu, send_v, h);
+                        const int32_t oi = __shfl_xor_sync(0xffffffffu, send_i, h);
+                        const bool take = beats(ov, oi, keep_v, keep_i);
+                        bv[k] = take ? ov : keep_v;
+                        bi[k] = take ? oi : keep_i;
                     }
-                    if (lane == 0) red_v[ew * NR + r0 + j] = bv, red_i[ew * NR + r0 + j] = bi;
                 }
+                if (r0 + lane < rows) red_v[ew * NR + r0 + lane] = bv[0], red_i[ew * NR + r0 + lane] = bi[0];
             }
         };
         // LM head: combine the four warps' per-row winners into the tile's (max, index)
@@ -491,32 +544,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
         }
     }
 
-    if (warp == kXWarp && lane == 0) {
-        // ---------------------------------------------------- activation copies
-        prefetch_tmap(&xmap);
-        pdl_wait();   // activations come from the previous kernel
-        int issued = 0;
-        int xs = 0, kt = (int)(rec_begin - nt_first * KT);
-        uint32_t xph = 0;   // fill parity of slot xs
-        for (int i = 0; i < nrec; ++i) {
-            // slot xs last held record i - Q: its MMAs must be done
-            if (i >= Q && !mbar_wait(bar_done + 8 * xs, xph ^ 1u, p.timeout_ns, p.status, abort_flag)) break;
-            mbar_expect_tx(bar_xfull + 8 * xs, xb);
-            if (!(drop_first && i == 0))
-                tma_load_2d(x_s + xs * xb, &xmap, kt * w12i::kTileK, 0, bar_xfull + 8 * xs);
-            issued = i + 1;
-            if (++xs == Q) xs = 0, xph ^= 1u;
-            if (++kt == KT) kt = 0;
-        }
-        if (*abort_flag) {
-            int32_t no_abort = 0;
-            for (int i = max(0, issued - Q); i < issued; ++i) {
-                if (drop_first && i == 0) continue;
-                mbar_wait(bar_xfull + 8 * (i % Q), (i / Q) & 1, p.timeout_ns, p.status, &no_abort);
-            }
-        }
-    }
-
     // all roles done (or stopped): release tensor memory
     tc_fence_before();
     __syncthreads();
@@ -552,20 +579,27 @@ namespace w12i {
 // record-pair slots within the shared-memory budget.  Preference: two decode
 // groups, then as many record-pair slots (bytes in flight) as possible.
 bool tc_buffer_plan(int nr, int max_recs, int esc_cap, int base_tiles, int budget, int *groups, int *a_bufs,
-                    int *d_bufs, int *stages)
+                    int *d_bufs, int *stages, int *x_slots)
 {
     static const int cand[][3] = {{2, 4, 2}, {2, 3, 2}, {2, 2, 2}, {2, 4, 1}, {2, 2, 1}, {1, 4, 2}, {1, 4, 1}, {1, 2, 1}};
-    int best = -1, best_st = 0;
+    int best = -1, best_st = 0, best_sx = 0;
     for (int k = 0; k < (int)(sizeof(cand) / sizeof(cand[0])); ++k) {
         const int g = cand[k][0], na = cand[k][1], db = cand[k][2];
         if (g * na * kACols + db * nr > (int)kTmemCols) continue;
-        int st = 8;
-        while (st >= 2 && plan(st, g * na, nr, max_recs, esc_cap, base_tiles).total > budget) --st;
-        if (st < 2) continue;
-        if (best < 0 || (g > cand[best][0]) || (g == cand[best][0] && st > best_st)) best = k, best_st = st;
+        // the most record-pair slots, then an activation ring up to two pairs deeper
+        int st = 0, sx = 0;
+        for (int s = 8; s >= 2 && st == 0; --s)
+            for (int x = s + 2; x >= s; --x)
+                if (plan(s, g * na, x, nr, max_recs, esc_cap, base_tiles).total <= budget) {
+                    st = s, sx = x;
+                    break;
+                }
+        if (st == 0) continue;
+        if (best < 0 || (g > cand[best][0]) || (g == cand[best][0] && (st > best_st || (st == best_st && sx > best_sx))))
+            best = k, best_st = st, best_sx = sx;
     }
     if (best < 0) return false;
-    *groups = cand[best][0], *a_bufs = cand[best][1], *d_bufs = cand[best][2], *stages = best_st;
+    *groups = cand[best][0], *a_bufs = cand[best][1], *d_bufs = cand[best][2], *stages = best_st, *x_slots = best_sx;
     return true;
 }
 
@@ -585,7 +619,12 @@ int launch_gemm_tc(const GemmArgs &a, void *stream)
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return (int)cudaErrorInvalidValue;
     const int64_t T = (int64_t)a.w.n_tiles * a.w.k_tiles;
-    const int G = (int)std::min<int64_t>(a.num_sms, T);
+    // A tile split between CTAs costs each contributor an nr x 128 FP32
+    // partial and the last one a read of all of them; with many rows and few
+    // records (a small linear at 256 rows) that reduction outweighs the
+    // records, so every CTA gets at least nr / 8 records.
+    const int64_t min_recs = std::max(1, nr / 8);
+    const int G = (int)std::max<int64_t>(1, std::min<int64_t>(a.num_sms, T / min_recs));
     TcParams p{};
     p.rec = a.w.rec;
     p.base = a.w.base;
@@ -611,9 +650,10 @@ int launch_gemm_tc(const GemmArgs &a, void *stream)
     p.esc_cap = 2048;
     p.base_tiles = std::min<int>(64, (int)(p.max_recs / a.w.k_tiles + 2));
     const int budget = 227 * 1024;
-    if (!tc_buffer_plan(nr, p.max_recs, p.esc_cap, p.base_tiles, budget, &p.groups, &p.a_bufs, &p.d_bufs, &p.stages))
+    if (!tc_buffer_plan(nr, p.max_recs, p.esc_cap, p.base_tiles, budget, &p.groups, &p.a_bufs, &p.d_bufs, &p.stages,
+                        &p.x_slots))
         return (int)cudaErrorInvalidConfiguration;
-    const int smem = plan(p.stages, p.groups * p.a_bufs, nr, p.max_recs, p.esc_cap, p.base_tiles).total;
+    const int smem = plan(p.stages, p.groups * p.a_bufs, p.x_slots, nr, p.max_recs, p.esc_cap, p.base_tiles).total;
     if (smem > budget) return (int)cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(k_w12_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return (int)e;

@@ -45,13 +45,17 @@ constexpr int kPartialRows = 64;         // rows per warp-MMA launch (larger R i
 int partial_rows(int32_t R) { return std::max(kPartialRows, (R + 31) / 32 * 32); }
 
 // Path choice: the tensor-memory kernel streams the weights once for any
-// R <= 256; the warp-MMA kernel covers R <= 64 per pass.  Debug flag bit 1
-// forces the tensor-memory path, bit 2 the warp-MMA path.
+// R <= 256; the warp-MMA kernel covers R <= 64 per pass and is the faster one
+// up to 32 rows (on GB300 the LM head at 32 rows: 286 against 311 us; at 64
+// rows: 388 against 338 us).  Debug flag bit 1 forces the tensor-memory path,
+// bit 2 the warp-MMA path.
+constexpr int32_t kTcMinRows = 33;
+
 bool use_tc(int32_t R)
 {
     if (g_debug_flags & 2) return true;
     if (g_debug_flags & 4) return false;
-    return R > kPartialRows;
+    return R >= kTcMinRows;
 }
 
 int num_sms()
