@@ -45,17 +45,23 @@ constexpr int kPartialRows = 64;         // rows per warp-MMA launch (larger R i
 int partial_rows(int32_t R) { return std::max(kPartialRows, (R + 31) / 32 * 32); }
 
 // Path choice: the tensor-memory kernel streams the weights once for any
-// R <= 256; the warp-MMA kernel covers R <= 64 per pass and is the faster one
-// up to 32 rows (on GB300 the LM head at 32 rows: 286 against 311 us; at 64
-// rows: 388 against 338 us).  Debug flag bit 1 forces the tensor-memory path,
-// bit 2 the warp-MMA path.
+// R <= 256; the warp-MMA kernel covers R <= 64 per pass.  Measured on GB300
+// (27B-like shapes), the warp-MMA kernel is the faster one up to 32 rows, and
+// from 33 to 64 rows for weights of under about 100 records per SM (QKV, O,
+// down: 37, 32, 58 against 55, 52, 75 us at 64 rows); the tensor-memory
+// kernel for the larger ones (gate/up 92 against 98 us, LM head 311 against
+// 389 us).  Debug flag bit 1 forces the tensor-memory path, bit 2 the
+// warp-MMA path.
+int num_sms();
 constexpr int32_t kTcMinRows = 33;
+constexpr int64_t kTcMinRecsPerSm = 100;
 
-bool use_tc(int32_t R)
+bool use_tc(int32_t R, int64_t records)
 {
     if (g_debug_flags & 2) return true;
     if (g_debug_flags & 4) return false;
-    return R >= kTcMinRows;
+    if (R > kPartialRows) return true;
+    return R >= kTcMinRows && records >= kTcMinRecsPerSm * num_sms();
 }
 
 int num_sms()
@@ -171,7 +177,7 @@ w12_status ws_check(void *ws, size_t ws_bytes, const WsLayout &L)
 int gemm_slices(const DevWeight &dw, const uint16_t *x, int32_t R, int mode, uint16_t *y, const Ws &ws, int &slot,
                 bool pdl, cudaStream_t st, bool qview = false)
 {
-    const bool tc = !qview && use_tc(R);
+    const bool tc = !qview && use_tc(R, (int64_t)dw.n_tiles * dw.k_tiles);
     const int32_t step = tc ? R : kPartialRows;
     for (int32_t r0 = 0; r0 < R; r0 += step) {
         GemmArgs a{};
