@@ -85,7 +85,7 @@ struct TcParams {
 };
 
 struct Plan {
-    int rec, x, bars, misc, escoff, esc, base, red, total;
+    int rec, x, bars, misc, escoff, esc, emask, base, red, total;
 };
 
 // q = A buffers over all groups; sx = activation pair slots
@@ -105,6 +105,8 @@ __host__ __device__ inline Plan plan(int stages, int q, int sx, int nr, int max_
     o += ((max_recs + 1) * 4 + 15) / 16 * 16;
     p.esc = o;
     o += esc_cap * 4;
+    p.emask = o;
+    o += (max_recs + 15) / 16 * 16;
     p.base = o;
     o += (base_tiles * w12i::kTileN + 15) / 16 * 16;
     p.red = o;
@@ -158,6 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + pl.misc + 8);
     int32_t *esc_off_s = reinterpret_cast<int32_t *>(smem + pl.escoff);
     uint32_t *esc_s = reinterpret_cast<uint32_t *>(smem + pl.esc);
+    uint8_t *emask_s = smem + pl.emask;
     uint8_t *base_s = smem + pl.base;
 
     const bool drop_first = (p.debug_flags & 1) && cta == 0;
@@ -273,6 +276,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
             const bool esc_cached = (esc_off_s[nrec] - e_lo) <= p.esc_cap;
             if (esc_cached)
                 for (int i = dtid; i < esc_off_s[nrec] - e_lo; i += ndec) esc_s[i] = __ldg(p.esc + e_lo + i);
+            // per record, a bit for every 32-channel quarter that holds an
+            // escape: the other quarters' warps skip the escape list
+            for (int i = dtid; i < nrec; i += ndec) {
+                uint32_t msk = 0;
+                for (int e = esc_off_s[i]; e < esc_off_s[i + 1]; ++e) msk |= 1u << ((__ldg(p.esc + e) >> 27) & 3u);
+                emask_s[i] = (uint8_t)msk;
+            }
             named_bar(kBarCaches, ndec);
 
             int64_t nt_cur = -1;
@@ -302,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
                     iq += GR;
                     if (iq >= Q) iq -= Q, iph ^= 1u;
                 }
+                const bool has_esc = (emask_s[i] >> quarter) & 1u;
                 bool ok = !*abort_flag;
                 if (ok) ok = mbar_wait(bar_rfull + 8 * s, sph, p.timeout_ns, p.status, abort_flag);
                 if (i >= Q) {
@@ -341,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
                             decode_word(vw[w], nw[w] >> ((q & 1) * 4), cc, p.mul16, a[8 * q + w], a[8 * q + 4 + w]);
                     }
                     // escaped slots of this channel: the exact value replaces the filler
-                    const int32_t e0 = esc_off_s[i] - e_lo, e1 = esc_off_s[i + 1] - e_lo;
+                    const int32_t e0 = has_esc ? esc_off_s[i] - e_lo : 0, e1 = has_esc ? esc_off_s[i + 1] - e_lo : 0;
                     for (int e = e0; e < e1; ++e) {
                         const uint32_t en = esc_cached ? esc_s[e] : __ldg(p.esc + e_lo + e);
                         const int nl = (en >> 22) & 0x7F;
