@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tree_build(const TreeParams p)
 }
 
 // ---------------------------------------------------------------------------
-// one warp per request (2 .. 32 requests)
+// one warp per request (2 .. 32 requests), or per child of the root (one request)
 // ---------------------------------------------------------------------------
 //
 // The selected set is the first R - n_req non-root nodes of the tree order
@@ -372,7 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tree_build(const TreeParams p)
 // nodes in tree order; each request's count follows from a binary search of
 // ranks, where a node's rank is the number of generated nodes before it.
 // A request that needs more nodes than its store holds sends the CTA to the
-// one-warp build.
+// one-warp build.  With one request the same argument holds for the subtrees
+// of the root's children: each is generated by its own warp, and a selected
+// node's row is one more than the number of selected nodes before it.
 
 constexpr int kPW = 64;   // nodes per request store (root included)
 
@@ -410,16 +412,16 @@ struct ParShared {
 
 constexpr size_t kParSmem = sizeof(ParShared) > sizeof(Nodes) ? sizeof(ParShared) : sizeof(Nodes);
 
-// number of generated non-root nodes (all requests) that come before (h1, h2);
-// lane q searches request q's sequence, which is in tree order
-__device__ __forceinline__ int count_before(const ParShared &s, int n_req, unsigned long long h1,
-                                            unsigned long long h2)
+// number of generated nodes (positions first.. of every sequence) that come
+// before (h1, h2); lane q searches sequence q, which is in tree order
+__device__ __forceinline__ int count_before(const ParShared &s, int n_seq, unsigned long long h1,
+                                            unsigned long long h2, int first)
 {
     const int lane = threadIdx.x & 31;
     int c = 0;
-    if (lane < n_req) {
+    if (lane < n_seq) {
         const ReqNodes &q = s.rn[lane];
-        int lo = 1, hi = s.n_gen[lane];   // first position in [1, n_gen) not before h
+        int lo = first, hi = s.n_gen[lane];   // first position in [first, n_gen) not before h
         while (lo < hi) {
             const int mid = (lo + hi) >> 1;
             const unsigned long long a1 = q.own1(mid), a2 = q.own2(mid);
@@ -427,7 +429,7 @@ __device__ __forceinline__ int count_before(const ParShared &s, int n_req, unsig
             lo = before ? mid + 1 : lo;
             hi = before ? hi : mid;
         }
-        c = lo - 1;
+        c = lo - first;
     }
     return (int)__reduce_add_sync(0xffffffffu, (uint32_t)c);
 }
@@ -458,16 +460,34 @@ __global__ void __launch_bounds__(1024, 1) k_tree_build_par(const TreeParams p)
     }
     const Lattice L{&p, lp_s, lt_s};
     const int R = min(p.R, kCap);
+    // sequences: one per request, or (one request) one per child of the root,
+    // whose subtree is a sequence of its own; position 0 of a request sequence
+    // is its root, of a subtree sequence the child, which counts as selected
+    const bool sub = NR == 1;
+    const int NS = sub ? NC : NR, first = sub ? 0 : 1;
     const int B = max(R - NR, 0);   // non-root nodes to select
 
-    // per-request generation passes
+    // generation passes
     unsigned long long b1 = 0, b2 = 0;
     int bx = -1, t = 1;
-    // first limit: the average share plus a little; unsettled requests grow
+    // first limit: the average share plus a little; unsettled sequences grow
     // their limit by half each pass
-    int limit = min(kPW, 1 + (B + NR - 1) / NR + 2);
+    int limit = min(kPW, 1 + (B + NS - 1) / NS + 2);
     ReqNodes &q = s.rn[warp];
-    add_root(q, L, NC, p_r, 0, warp, p.root_tok[warp], b1, b2, bx);
+    if (sub) {
+        // child `warp` of the root: its score is the edge itself (0 + e)
+        const float sc = __fadd_rn(0.f, L.edge(0, 1, 0, warp));
+        const uint32_t dr = 1u << 16;
+        const unsigned long long path = (unsigned long long)warp << 60;
+        unsigned long long perm, k1, k2;
+        bool has;
+        rank_children(L, NC, p_r[0], sc, dr, path, warp, perm, k1, k2, has);
+        if (lane == 0) q.store(0, sc, dr, path, warp, -1, L.token(0, 1, warp), perm, has ? NC : 0, k1, k2);
+        if (lane == 0 && k1 != 0) b1 = k1, b2 = k2, bx = 0;
+        __syncwarp();
+    } else {
+        add_root(q, L, NC, p_r, 0, warp, p.root_tok[warp], b1, b2, bx);
+    }
     bool settled = false;
     for (;;) {
         if (!settled) {
@@ -482,7 +502,7 @@ __global__ void __launch_bounds__(1024, 1) k_tree_build_par(const TreeParams p)
         __syncthreads();
         if (!settled) {
             const unsigned long long h1 = s.head1[warp], h2 = s.head2[warp];
-            settled = h1 == 0 || count_before(s, NR, h1, h2) >= B;
+            settled = h1 == 0 || count_before(s, NS, h1, h2, first) >= B;
             if (!settled && lane == 0) {
                 atomicAdd(&s.pending, 1);
                 if (limit == kPW) s.overflow = 1;
@@ -504,19 +524,52 @@ __global__ void __launch_bounds__(1024, 1) k_tree_build_par(const TreeParams p)
         return;
     }
 
-    // selection: request q keeps its first k_q non-root nodes, the largest k
-    // whose k-th node has fewer than B generated nodes before it
+    // selection: sequence q keeps its nodes at positions first .. first + k_q - 1,
+    // the largest k_q whose last node has fewer than B generated nodes before it
     {
         const int ng = s.n_gen[warp];
-        int lo = 0, hi = ng - 1;   // k in [lo, hi]
+        int lo = 0, hi = ng - first;   // k in [lo, hi]
         while (lo < hi) {
             const int k = (lo + hi + 1) >> 1;
-            const int before = count_before(s, NR, q.own1(k), q.own2(k));
+            const int x = first + k - 1;
+            const int before = count_before(s, NS, q.own1(x), q.own2(x), first);
             if (before < B) lo = k; else hi = k - 1;
         }
         if (lane == 0) s.k_sel[warp] = lo;
     }
     __syncthreads();
+    if (sub) {
+        // one request: row 0 is the root, a selected node's row is one more than
+        // the number of selected nodes before it in the tree order
+        const int cnt = s.k_sel[warp];
+        for (int i = 0; i < cnt; ++i) {
+            const int rk = count_before(s, NS, q.own1(i), q.own2(i), 0);
+            if (lane == 0) q.key1[i] = (unsigned long long)(1 + rk);   // the node's row (frontier keys are done with)
+        }
+        __syncwarp();
+        for (int i = lane; i < cnt; i += 32) {
+            const int row = (int)q.key1[i];
+            p.parent[row] = q.par[i] < 0 ? 0 : (int)q.key1[q.par[i]];
+            p.token[row] = q.tok[i];
+            p.req[row] = 0;
+            p.score[row] = q.score[i];
+            p.depth[row] = (uint8_t)(q.dr[i] >> 16);
+            p.rank[row] = q.rank[i];
+        }
+        if (tid == 0) {
+            int total = 1;
+            for (int w = 0; w < NS; ++w) total += s.k_sel[w];
+            p.parent[0] = -1;
+            p.token[0] = p.root_tok[0];
+            p.req[0] = 0;
+            p.score[0] = 0.f;
+            p.depth[0] = 0;
+            p.rank[0] = 0;
+            p.req_row_off[0] = 0;
+            p.req_row_off[1] = total;
+        }
+        return;
+    }
     if (tid == 0) {
         int o = 0;
         for (int r = 0; r < NR; ++r) s.row_off[r] = o, o += 1 + s.k_sel[r];
@@ -618,14 +671,15 @@ int launch_tree_build(const TreeArgs &a, void *stream)
     const int lat = a.n_req * a.p_max * 16;
     const int limit = 227 * 1024;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (a.n_req >= 2 && a.n_req <= 32) {
-        // one warp per request
+    const bool sub = a.n_req == 1 && a.n_cand >= 2 && a.p_max >= 1 && a.p_r_host[0] >= 1;
+    if ((a.n_req >= 2 && a.n_req <= 32) || sub) {
+        // one warp per request, or (one request) per child of the root
         int o = (int)kParSmem + 528;
         p.stage_lattice = (!a.conditional && o + 8 * lat <= limit) ? 1 : 0;
         if (p.stage_lattice) o += 8 * lat;
         cudaError_t e = cudaFuncSetAttribute(k_tree_build_par, cudaFuncAttributeMaxDynamicSharedMemorySize, o);
         if (e != cudaSuccess) return (int)e;
-        k_tree_build_par<<<1, 32 * a.n_req, o, st>>>(p);
+        k_tree_build_par<<<1, 32 * (sub ? a.n_cand : a.n_req), o, st>>>(p);
         return (int)cudaGetLastError();
     }
     int o = (int)sizeof(Nodes);

@@ -238,6 +238,10 @@ TREE_CASES = [
     ("batched_27b", dict(vocab=4096, hidden=512, budget=512, seed=4)),
     ("batched_27b", dict(vocab=4096, hidden=512, budget=24, seed=5)),       # roots only
     ("single_27b", dict(vocab=4096, hidden=512, positions=(2,), budget=500, n_cand=3, seed=6)),  # exhausted
+    ("single_27b", dict(vocab=4096, hidden=512, conditional=True, seed=7)),
+    ("single_27b", dict(vocab=4096, hidden=512, budget=200, seed=8)),       # a subtree outgrows its store
+    ("single_27b", dict(vocab=4096, hidden=512, budget=120, n_cand=5, seed=9)),
+    ("single_27b", dict(vocab=4096, hidden=512, positions=(1,), budget=20, seed=10)),  # depth 1 only
 ]
 
 
@@ -301,6 +305,15 @@ def test_tree_build_equal_scores(w12):
     lat = synth.lattice(w)
     lat.cand_logp[:] = np.float32(-0.5)
     _tree_case(w12, lat, 120)
+
+
+def test_tree_build_one_request_equal_scores(w12):
+    """One request split over the root's children, every edge equal: the
+    order falls to depth and path across the subtree warps."""
+    w = synth.scaled(synth.WORKLOADS["single_27b"], vocab=4096, hidden=512, budget=40, seed=14)
+    lat = synth.lattice(w)
+    lat.cand_logp[:] = np.float32(-0.5)
+    _tree_case(w12, lat, 40)
 
 
 def test_tree_build_flags_positive_logp(w12):
