@@ -102,7 +102,7 @@ def load_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("k_gemm.cu", "w12_device.cuh"):
+    for f in ("k_gemm.cu", "k_gemm_tc.cu", "w12_device.cuh", "w12_abi.cpp"):
         with open(os.path.join(ROOT, "speculative_decoding_tree_w12_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -686,7 +686,7 @@ def main():
             "pct_of_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
             "pct_of_measured_hbm": round(100 * value / world / peak, 2),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": "k_w12_gemm",
+                         "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": "k_w12_gemm + k_w12_gemm_tc",
                          "peak_kind": peak_kind,
                          "note": "all W12 GEMM launches of a step (linears + LM head), serialised, "
                                  "algorithmic bytes (W12 + activations + outputs) / summed launch time"},

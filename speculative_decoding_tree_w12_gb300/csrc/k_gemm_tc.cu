@@ -11,7 +11,7 @@
 //                    activation ring; a record slot is handed back as soon as
 //                    the decode warps have read the pair into registers, an
 //                    activation slot once the pair's MMAs are done
-//   decode groups    one or two groups of four warps (one per tensor-memory
+//   decode groups    one to four groups of four warps (one per tensor-memory
 //                    lane quarter); a group takes every G-th record of the
 //                    CTA.  Thread = output channel: six 16-byte shared loads,
 //                    in-register decode of its 64 weights, escape patch, one
@@ -48,10 +48,10 @@ namespace {
 
 constexpr int kProducerWarp = 0;   // also allocates tensor memory
 constexpr int kGroupWarp0 = 1;     // decode group g = warps 1 + 4g .. 4 + 4g
-constexpr int kMaxGroups = 2;
-constexpr int kMmaWarp = 1 + 4 * kMaxGroups;    // warp 9
-constexpr int kEpiWarp0 = kMmaWarp + 1;          // warps 10..13
-constexpr int kThreads = (kEpiWarp0 + 4) * 32;   // 14 warps
+constexpr int kMaxGroups = 4;
+constexpr int kMmaWarp = 1 + 4 * kMaxGroups;    // warp 17
+constexpr int kEpiWarp0 = kMmaWarp + 1;          // warps 18..21
+constexpr int kThreads = (kEpiWarp0 + 4) * 32;   // 22 warps
 constexpr int kRecPair = 2 * w12i::kRecBytes;
 constexpr int kACols = 32;
 constexpr uint32_t kTmemCols = 512;
@@ -292,7 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
             // per-record indices advanced without divisions: pair m = i / 2 in
             // slot s (fill parity sph), tile nt / k-tile kt of record i, A
             // buffer ab, activation slot iq (fill parity iph)
-            int m = 0, s = 0;
+            // record g sits in pair g / 2 (slot g / 2: there are at least two slots)
+            int m = g >> 1, s = g >> 1;
             uint32_t sph = 0;
             int64_t nt = (rec_begin + g) / KT;
             int kt = (int)((rec_begin + g) - nt * KT);
@@ -587,12 +588,16 @@ namespace w12i {
 // Buffer plan for MMA width nr: groups x A buffers x 32 columns plus
 // accumulators x nr columns within 512 tensor-memory columns; the activation
 // ring (groups x A buffers slots of nr x 128 bytes) and at least two
-// record-pair slots within the shared-memory budget.  Preference: two decode
-// groups, then as many record-pair slots (bytes in flight) as possible.
+// record-pair slots within the shared-memory budget.  Preference: two
+// accumulators (the epilogue of one tile overlaps the next tile's MMAs), then
+// more decode groups, then as many record-pair slots (bytes in flight) as
+// possible.
 bool tc_buffer_plan(int nr, int max_recs, int esc_cap, int base_tiles, int budget, int *groups, int *a_bufs,
                     int *d_bufs, int *stages, int *x_slots)
 {
-    static const int cand[][3] = {{2, 4, 2}, {2, 3, 2}, {2, 2, 2}, {2, 4, 1}, {2, 2, 1}, {1, 4, 2}, {1, 4, 1}, {1, 2, 1}};
+    // (groups, A buffers per group, accumulators); named barriers 2 .. 2 + groups * A buffers - 1 stay below 16
+    static const int cand[][3] = {{4, 3, 2}, {4, 2, 2}, {4, 2, 1}, {3, 4, 2}, {3, 3, 2}, {3, 2, 2}, {3, 2, 1},
+                                  {2, 4, 2}, {2, 3, 2}, {2, 2, 2}, {2, 4, 1}, {2, 2, 1}, {1, 4, 2}, {1, 4, 1}, {1, 2, 1}};
     int best = -1, best_st = 0, best_sx = 0;
     for (int k = 0; k < (int)(sizeof(cand) / sizeof(cand[0])); ++k) {
         const int g = cand[k][0], na = cand[k][1], db = cand[k][2];
@@ -606,7 +611,8 @@ bool tc_buffer_plan(int nr, int max_recs, int esc_cap, int base_tiles, int budge
                     break;
                 }
         if (st == 0) continue;
-        if (best < 0 || (g > cand[best][0]) || (g == cand[best][0] && (st > best_st || (st == best_st && sx > best_sx))))
+        if (best < 0 || (db > cand[best][2]) || (db == cand[best][2] && g > cand[best][0]) ||
+            (db == cand[best][2] && g == cand[best][0] && (st > best_st || (st == best_st && sx > best_sx))))
             best = k, best_st = st, best_sx = sx;
     }
     if (best < 0) return false;

@@ -46,22 +46,23 @@ int partial_rows(int32_t R) { return std::max(kPartialRows, (R + 31) / 32 * 32);
 
 // Path choice: the tensor-memory kernel streams the weights once for any
 // R <= 256; the warp-MMA kernel covers R <= 64 per pass.  Measured on GB300
-// (27B-like shapes), the warp-MMA kernel is the faster one up to 32 rows, and
-// from 33 to 64 rows for weights of under about 100 records per SM (QKV, O,
-// down: 37, 32, 58 against 55, 52, 75 us at 64 rows); the tensor-memory
-// kernel for the larger ones (gate/up 92 against 98 us, LM head 311 against
-// 389 us).  Debug flag bit 1 forces the tensor-memory path, bit 2 the
-// warp-MMA path.
+// (27B-like shapes, microseconds per launch, warp-MMA against tcgen05):
+//   16 rows: warp-MMA faster for every weight (LM head 246 / 265);
+//   32 rows: tcgen05 faster for gate/up (78 / 73) and the LM head (292 / 266),
+//            warp-MMA for QKV, O and down (under 100 records per SM);
+//   64 rows: tcgen05 faster from down (72 records per SM: 58 / 56) up,
+//            warp-MMA for QKV and O.
+// Debug flag bit 1 forces the tensor-memory path, bit 2 the warp-MMA path.
 int num_sms();
-constexpr int32_t kTcMinRows = 33;
-constexpr int64_t kTcMinRecsPerSm = 100;
 
 bool use_tc(int32_t R, int64_t records)
 {
     if (g_debug_flags & 2) return true;
     if (g_debug_flags & 4) return false;
     if (R > kPartialRows) return true;
-    return R >= kTcMinRows && records >= kTcMinRecsPerSm * num_sms();
+    if (R <= 16) return false;
+    const int64_t per_sm = records / num_sms();
+    return R <= 32 ? per_sm >= 100 : per_sm >= 50;
 }
 
 int num_sms()
