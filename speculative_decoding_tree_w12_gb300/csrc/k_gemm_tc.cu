@@ -226,31 +226,51 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
                 kt0 += 2;
                 while (kt0 >= KT) kt0 -= KT;
             };
-            for (int m = 0; m < pre; ++m) issue_x(m, m, kt0), adv();
-            int issued = pre;
-            // record slot / activation slot of pair m and their reuse parities,
-            // advanced without divisions (the activation ring is at least as deep)
-            int sl = pre % S, xsl = pre % SX;
-            uint32_t rph = (uint32_t)((pre / S) - 1) & 1u, xph = (uint32_t)((pre / SX) - 1) & 1u;
-            for (int m = pre; m < npairs; ++m) {
-                // slot sl last held pair m - S: every decode warp must have read it
-                if (!mbar_wait(bar_rempty + 8 * sl, rph, p.timeout_ns, p.status, abort_flag)) break;
-                // activation slot xsl last held pair m - SX: its MMAs must be done
-                if (m >= SX && !mbar_wait(bar_xdone + 8 * xsl, xph, p.timeout_ns, p.status, abort_flag)) break;
-                issue(m, sl);
-                issue_x(m, xsl, kt0);
-                adv();
-                issued = m + 1;
-                if (++sl == S) sl = 0, rph ^= 1u;
-                if (++xsl == SX) xsl = 0, xph ^= 1u;
+            // Records and activations advance on their own: record pair mr waits
+            // for its slot (the decode warps read pair mr - S), activation pair mx
+            // for its slot (the MMAs of pair mx - SX), and neither holds up the
+            // other.  Slots and reuse parities are advanced without divisions.
+            int mr = pre, mx = 0;
+            int sl = pre % S, xsl = 0;
+            uint32_t rph = (uint32_t)((pre / S) - 1) & 1u, xph = 1u;
+            bool stalled = false;
+            uint64_t t_idle = 0;
+            while ((mr < npairs || mx < npairs) && !stalled) {
+                bool moved = false;
+                if (mr < npairs && mbar_try_wait(bar_rempty + 8 * sl, rph)) {
+                    issue(mr, sl);
+                    ++mr;
+                    if (++sl == S) sl = 0, rph ^= 1u;
+                    moved = true;
+                }
+                if (mx < npairs && (mx < SX || mbar_try_wait(bar_xdone + 8 * xsl, xph))) {
+                    issue_x(mx, xsl, kt0);
+                    adv();
+                    ++mx;
+                    if (++xsl == SX) xsl = 0, xph ^= 1u;
+                    moved = true;
+                }
+                if (moved) {
+                    t_idle = 0;
+                } else if (*abort_flag) {
+                    stalled = true;
+                } else if (t_idle == 0) {
+                    t_idle = globaltimer();
+                } else if (globaltimer() - t_idle > p.timeout_ns) {
+                    atomicCAS(p.status, 0, static_cast<int32_t>(W12_E_TIMEOUT));
+                    *abort_flag = 1;
+                    stalled = true;
+                }
             }
             if (*abort_flag) {
                 // leave no copy in flight
                 int32_t no_abort = 0;
-                for (int m = max(0, issued - SX); m < issued; ++m) {
+                for (int m = max(0, mr - S); m < mr; ++m) {
                     if (drop_first && m == 0) continue;
-                    if (m >= issued - S)
-                        mbar_wait(bar_rfull + 8 * (m % S), (m / S) & 1, p.timeout_ns, p.status, &no_abort);
+                    mbar_wait(bar_rfull + 8 * (m % S), (m / S) & 1, p.timeout_ns, p.status, &no_abort);
+                }
+                for (int m = max(0, mx - SX); m < mx; ++m) {
+                    if (drop_first && m == 0) continue;
                     mbar_wait(bar_xfull + 8 * (m % SX), (m / SX) & 1, p.timeout_ns, p.status, &no_abort);
                 }
             }
