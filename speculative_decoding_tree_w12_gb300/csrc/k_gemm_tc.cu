@@ -131,6 +131,8 @@ __device__ __forceinline__ void named_arrive(int id, int threads)
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// kChunk: records the MMA warp takes per tensor-memory fence (see the MMA warp)
+template <int kChunk>
 __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_constant__ CUtensorMap xmap, const TcParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -399,52 +401,132 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
         const uint32_t idesc = idesc_bf16_f32(128, NR);
         int tcount = 0, dcur = 0;
         int kt = (int)(rec_begin - nt_first * KT);
-        // group g, A buffer ab, A-buffer done slot aq and activation pair slot
-        // xsl (fill parity xph) of record i, advanced without divisions
-        int g = 0, ab = 0, aq = 0, xsl = 0;
-        uint32_t xph = 0;
-        for (int i = 0; i < nrec; ++i) {
-            if (i > 0) {
-                if (++g == GR) {
-                    g = 0;
-                    if (++ab == NAG) ab = 0;
+        if constexpr (kChunk == 1) {
+            // group g, A buffer ab, A-buffer done slot aq and activation pair slot
+            // xsl (fill parity xph) of record i, advanced without divisions
+            int g = 0, ab = 0, aq = 0, xsl = 0;
+            uint32_t xph = 0;
+            for (int i = 0; i < nrec; ++i) {
+                if (i > 0) {
+                    if (++g == GR) {
+                        g = 0;
+                        if (++ab == NAG) ab = 0;
+                    }
+                    if (++aq == Q) aq = 0;
                 }
-                if (++aq == Q) aq = 0;
-            }
-            named_bar(kBarA0 + g * NAG + ab, 160);
-            // the whole warp runs this part (it stays converged); one elected
-            // lane issues the tensor-core instructions
-            tc_fence_after();
-            const bool first = (i == 0) || kt == 0;
-            const bool last = (i == nrec - 1) || kt == KT - 1;
-            const bool pair_end = (i & 1) || i == nrec - 1;
-            bool go = !*abort_flag;
-            if (go && (i & 1) == 0) go = mbar_wait(bar_xfull + 8 * xsl, xph, p.timeout_ns, p.status, abort_flag);
-            go = __all_sync(0xffffffffu, go);
-            if (first) {
-                dcur = tcount % DB;
-                if (go && tcount >= DB)
-                    go = mbar_wait(bar_accempty + 8 * dcur, ((tcount / DB) - 1) & 1, p.timeout_ns, p.status,
-                                   abort_flag);
-                go = __all_sync(0xffffffffu, go);
+                named_bar(kBarA0 + g * NAG + ab, 160);
+                // the whole warp runs this part (it stays converged); one elected
+                // lane issues the tensor-core instructions
                 tc_fence_after();
-            }
-            if (elect_one()) {
-                if (go) {
-                    const uint32_t d_t = tmem + d_col(dcur), a_t = tmem + a_col(g, ab);
-                    const uint64_t bd = smem_desc_sw128(x_s + (uint32_t)(xsl * 2 + (i & 1)) * xb);
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        tc_mma_ts(d_t, a_t + ks * 8, bd + (uint64_t)(ks * 2), idesc, (first && ks == 0) ? 0u : 1u);
+                const bool first = (i == 0) || kt == 0;
+                const bool last = (i == nrec - 1) || kt == KT - 1;
+                const bool pair_end = (i & 1) || i == nrec - 1;
+                bool go = !*abort_flag;
+                if (go && (i & 1) == 0) go = mbar_wait(bar_xfull + 8 * xsl, xph, p.timeout_ns, p.status, abort_flag);
+                go = __all_sync(0xffffffffu, go);
+                if (first) {
+                    dcur = tcount % DB;
+                    if (go && tcount >= DB)
+                        go = mbar_wait(bar_accempty + 8 * dcur, ((tcount / DB) - 1) & 1, p.timeout_ns, p.status,
+                                       abort_flag);
+                    go = __all_sync(0xffffffffu, go);
+                    tc_fence_after();
                 }
-                tc_commit(bar_done + 8 * aq);                 // always: frees the A buffer
-                if (pair_end) tc_commit(bar_xdone + 8 * xsl);   // always: frees the activation slot
-                if (last && go) tc_commit(bar_accfull + 8 * dcur);
+                if (elect_one()) {
+                    if (go) {
+                        const uint32_t d_t = tmem + d_col(dcur), a_t = tmem + a_col(g, ab);
+                        const uint64_t bd = smem_desc_sw128(x_s + (uint32_t)(xsl * 2 + (i & 1)) * xb);
+    #pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            tc_mma_ts(d_t, a_t + ks * 8, bd + (uint64_t)(ks * 2), idesc, (first && ks == 0) ? 0u : 1u);
+                    }
+                    tc_commit(bar_done + 8 * aq);                 // always: frees the A buffer
+                    if (pair_end) tc_commit(bar_xdone + 8 * xsl);   // always: frees the activation slot
+                    if (last && go) tc_commit(bar_accfull + 8 * dcur);
+                }
+                __syncwarp();
+                if (last) ++tcount;
+                if (pair_end && ++xsl == SX) xsl = 0, xph ^= 1u;
+                if (++kt == KT) kt = 0;
             }
-            __syncwarp();
-            if (last) ++tcount;
-            if (pair_end && ++xsl == SX) xsl = 0, xph ^= 1u;
-            if (++kt == KT) kt = 0;
+        } else {
+            // group g, A buffer ab, A-buffer done slot aq and activation pair slot
+            // xsl (fill parity xph) of the next record, advanced without divisions.
+            // The records are taken in chunks of up to kChunk within one tile: one
+            // tensor-memory fence per chunk, after the chunk's named-barrier syncs.
+            // Up to 64 rows the host picks 4 (LM head at 32 rows 269 -> 252 us);
+            // wider MMAs want each record issued as soon as it is decoded, so
+            // there it picks 1 (a separate instantiation: sharing one with the
+            // chunked loop made the wide launches 1.5x slower).
+            int g = 0, ab = 0, aq = 0, xsl = 0;
+            uint32_t xph = 0;
+            for (int i = 0; i < nrec;) {
+                int n = min(kChunk, nrec - i);
+                n = min(n, KT - kt);   // a chunk never crosses a tile boundary
+                n = min(n, Q);         // record r's buffer waits for record r - Q's commit
+                int cg[kChunk], cab[kChunk], caq[kChunk], cxs[kChunk];
+                uint32_t cxp[kChunk];
+                bool cpe[kChunk];
+    #pragma unroll
+                for (int j = 0; j < kChunk; ++j) {
+                    if (j < n) {
+                        const int r = i + j;
+                        if (r > 0) {
+                            if (++g == GR) {
+                                g = 0;
+                                if (++ab == NAG) ab = 0;
+                            }
+                            if (++aq == Q) aq = 0;
+                            if ((r & 1) == 0 && ++xsl == SX) xsl = 0, xph ^= 1u;   // a new pair starts
+                        }
+                        cg[j] = g, cab[j] = ab, caq[j] = aq, cxs[j] = xsl, cxp[j] = xph;
+                        cpe[j] = (r & 1) || r == nrec - 1;
+                        named_bar(kBarA0 + g * NAG + ab, 160);
+                    }
+                }
+                // the whole warp runs this part (it stays converged); one elected
+                // lane issues the tensor-core instructions
+                tc_fence_after();
+                const bool first = (i == 0) || kt == 0;
+                const bool last = (i + n == nrec) || kt + n == KT;
+                bool go = !*abort_flag;
+    #pragma unroll
+                for (int j = 0; j < kChunk; ++j)
+                    if (j < n && go && ((i + j) & 1) == 0)
+                        go = mbar_wait(bar_xfull + 8 * cxs[j], cxp[j], p.timeout_ns, p.status, abort_flag);
+                go = __all_sync(0xffffffffu, go);
+                if (first) {
+                    dcur = tcount % DB;
+                    if (go && tcount >= DB)
+                        go = mbar_wait(bar_accempty + 8 * dcur, ((tcount / DB) - 1) & 1, p.timeout_ns, p.status,
+                                       abort_flag);
+                    go = __all_sync(0xffffffffu, go);
+                    tc_fence_after();
+                }
+                if (elect_one()) {
+    #pragma unroll
+                    for (int j = 0; j < kChunk; ++j) {
+                        if (j < n) {
+                            if (go) {
+                                const uint32_t d_t = tmem + d_col(dcur), a_t = tmem + a_col(cg[j], cab[j]);
+                                const uint64_t bd = smem_desc_sw128(x_s + (uint32_t)(cxs[j] * 2 + ((i + j) & 1)) * xb);
+    #pragma unroll
+                                for (int ks = 0; ks < 4; ++ks)
+                                    tc_mma_ts(d_t, a_t + ks * 8, bd + (uint64_t)(ks * 2), idesc,
+                                              (first && j == 0 && ks == 0) ? 0u : 1u);
+                            }
+                            tc_commit(bar_done + 8 * caq[j]);                    // always: frees the A buffer
+                            if (cpe[j]) tc_commit(bar_xdone + 8 * cxs[j]);       // always: frees the activation slot
+                        }
+                    }
+                    if (last && go) tc_commit(bar_accfull + 8 * dcur);
+                }
+                __syncwarp();
+                if (last) ++tcount;
+                kt += n;
+                if (kt == KT) kt = 0;
+                i += n;
+            }
         }
         // tensor memory is released only after every issued MMA finished
         if (nrec > 0) {
@@ -692,7 +774,9 @@ int launch_gemm_tc(const GemmArgs &a, void *stream)
         return (int)cudaErrorInvalidConfiguration;
     const int smem = plan(p.stages, p.groups * p.a_bufs, p.x_slots, nr, p.max_recs, p.esc_cap, p.base_tiles).total;
     if (smem > budget) return (int)cudaErrorInvalidConfiguration;
-    cudaError_t e = cudaFuncSetAttribute(k_w12_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // chunks of four records per fence up to 64 rows with two accumulators
+    const auto kern = (nr <= 64 && p.d_bufs == 2) ? k_w12_gemm_tc<4> : k_w12_gemm_tc<1>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return (int)e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(G);
@@ -704,7 +788,7 @@ int launch_gemm_tc(const GemmArgs &a, void *stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 1 : 0;
-    return (int)cudaLaunchKernelEx(&cfg, k_w12_gemm_tc, xmap, p);
+    return (int)cudaLaunchKernelEx(&cfg, kern, xmap, p);
 }
 
 }  // namespace w12i
