@@ -131,8 +131,10 @@ __device__ __forceinline__ void named_arrive(int id, int threads)
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// kChunk: records the MMA warp takes per tensor-memory fence (see the MMA warp)
-template <int kChunk>
+// kChunk: records the MMA warp takes per tensor-memory fence (see the MMA warp);
+// QV: the quick pass (only the 8 KB view plane of each record is copied; the low
+// mantissa bits of in-window weights are taken as the midpoint 0b1000)
+template <int kChunk, bool QV>
 __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_constant__ CUtensorMap xmap, const TcParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -201,10 +203,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
             const uint64_t pol = policy_evict_first();
             auto issue = [&](int m, int sl) {
                 const int n = min(2, nrec - 2 * m);
-                mbar_expect_tx(bar_rfull + 8 * sl, (uint32_t)(n * w12i::kRecBytes));
-                if (!(drop_first && m == 0))
-                    bulk_g2s(rec_s + sl * kRecPair, p.rec + (rec_begin + 2 * m) * (int64_t)w12i::kRecBytes,
-                             (uint32_t)(n * w12i::kRecBytes), bar_rfull + 8 * sl, pol);
+                if constexpr (QV) {
+                    // the view plane of each record: its first 8 KB, at the record's place in the slot
+                    mbar_expect_tx(bar_rfull + 8 * sl, (uint32_t)(n * w12i::kViewBytes));
+                    if (!(drop_first && m == 0))
+                        for (int r = 0; r < n; ++r)
+                            bulk_g2s(rec_s + sl * kRecPair + r * w12i::kRecBytes,
+                                     p.rec + (rec_begin + 2 * m + r) * (int64_t)w12i::kRecBytes,
+                                     (uint32_t)w12i::kViewBytes, bar_rfull + 8 * sl, pol);
+                } else {
+                    mbar_expect_tx(bar_rfull + 8 * sl, (uint32_t)(n * w12i::kRecBytes));
+                    if (!(drop_first && m == 0))
+                        bulk_g2s(rec_s + sl * kRecPair, p.rec + (rec_begin + 2 * m) * (int64_t)w12i::kRecBytes,
+                                 (uint32_t)(n * w12i::kRecBytes), bar_rfull + 8 * sl, pol);
+                }
             };
             // activation blocks of pair m (k-tile kt0 for its first record) into
             // pair slot xsl, right behind the pair's records in the copy queue
@@ -360,7 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
                     for (int q = 0; q < 4; ++q) v[q] = *reinterpret_cast<const uint4 *>(rb + (q * 128 + c) * 16);
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
-                        nb[h] = *reinterpret_cast<const uint4 *>(rb + w12i::kViewBytes + (h * 128 + c) * 16);
+                        nb[h] = QV ? make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u)
+                                   : *reinterpret_cast<const uint4 *>(rb + w12i::kViewBytes + (h * 128 + c) * 16);
                     // the record is in registers: hand the slot back to the producer
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_rempty + 8 * s);
@@ -775,7 +788,9 @@ int launch_gemm_tc(const GemmArgs &a, void *stream)
     const int smem = plan(p.stages, p.groups * p.a_bufs, p.x_slots, nr, p.max_recs, p.esc_cap, p.base_tiles).total;
     if (smem > budget) return (int)cudaErrorInvalidConfiguration;
     // chunks of four records per fence up to 64 rows with two accumulators
-    const auto kern = (nr <= 64 && p.d_bufs == 2) ? k_w12_gemm_tc<4> : k_w12_gemm_tc<1>;
+    const bool chunked = nr <= 64 && p.d_bufs == 2;
+    const auto kern = a.qview ? (chunked ? k_w12_gemm_tc<4, true> : k_w12_gemm_tc<1, true>)
+                              : (chunked ? k_w12_gemm_tc<4, false> : k_w12_gemm_tc<1, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return (int)e;
     cudaLaunchConfig_t cfg{};

@@ -178,7 +178,7 @@ w12_status ws_check(void *ws, size_t ws_bytes, const WsLayout &L)
 int gemm_slices(const DevWeight &dw, const uint16_t *x, int32_t R, int mode, uint16_t *y, const Ws &ws, int &slot,
                 bool pdl, cudaStream_t st, bool qview = false)
 {
-    const bool tc = !qview && use_tc(R, (int64_t)dw.n_tiles * dw.k_tiles);
+    const bool tc = use_tc(R, (int64_t)dw.n_tiles * dw.k_tiles);
     const int32_t step = tc ? R : kPartialRows;
     for (int32_t r0 = 0; r0 < R; r0 += step) {
         GemmArgs a{};

@@ -191,7 +191,7 @@ QUICK_GEMM_CASES = [
 
 
 @pytest.mark.parametrize("n,k,R,outl,zero", QUICK_GEMM_CASES)
-def test_gemm_quick_matches_oracle(w12, n, k, R, outl, zero):
+def test_gemm_quick_matches_oracle(w12, path, n, k, R, outl, zero):
     w = synth.weights(n, k, n + k + R, 21, outl, zero)
     x = synth.activations(R, k, n + k + R, 22)
     pk = oracle.w12_pack(w)
@@ -207,8 +207,8 @@ def test_gemm_quick_matches_oracle(w12, n, k, R, outl, zero):
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))   # deterministic
 
 
-@pytest.mark.parametrize("V,K,R", [(4096, 512, 8), (8192, 1024, 33), (2048, 384, 70)])
-def test_lmhead_argmax_quick_matches_oracle(w12, V, K, R):
+@pytest.mark.parametrize("V,K,R", [(4096, 512, 8), (8192, 1024, 33), (2048, 384, 70), (4096, 640, 200)])
+def test_lmhead_argmax_quick_matches_oracle(w12, path, V, K, R):
     wh = synth.weights(V, K, V + K, 23)
     pk = oracle.w12_pack(wh)
     wq = oracle.w12_unpack_q(pk)
