@@ -160,6 +160,37 @@ def head_argmax(h: np.ndarray, w_head: np.ndarray, bias: Optional[np.ndarray] = 
     return am, t1, mg
 
 
+def _bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    return (np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def certified_head(h: np.ndarray, p: Packed):
+    """Certified LM head (explainer "4.1"/"4.3": a cheap pass over the head,
+    a per-row Cauchy-Schwarz error bound that discards tokens proven unable
+    to be the argmax, exact rescoring of the survivors; the argmax equals the
+    dense one).  Reading: the cheap pass reads each record's 8-bit view (the
+    quick-pass weights w^), not a separate INT8 copy, so the bound for row r
+    and token v is ||h_r|| * ||w_v - w^_v||.  All in FP64.
+
+    Returns (argmax per row, survivors per row, the per-token norms
+    ||w_v - w^_v|| and ||w^_v||)."""
+    hf = _bf16_to_f64(h)
+    w = _bf16_to_f64(w12_unpack(p))
+    wq = _bf16_to_f64(w12_unpack_q(p))
+    err = np.sqrt(((w - wq) ** 2).sum(axis=1))
+    qn = np.sqrt((wq ** 2).sum(axis=1))
+    sq = hf @ wq.T
+    eps = np.sqrt((hf ** 2).sum(axis=1))[:, None] * err[None, :]
+    low = (sq - eps).max(axis=1)
+    surv = (sq + eps) >= low[:, None]
+    am = np.empty(hf.shape[0], dtype=np.int32)
+    for r in range(hf.shape[0]):
+        idx = np.nonzero(surv[r])[0]
+        s = w[idx] @ hf[r]
+        am[r] = idx[int(np.argmax(s))]          # first maximum: lowest index on ties
+    return am, surv.sum(axis=1).astype(np.int64), err, qn
+
+
 # ---------------------------------------------------------------------------
 # Best-first tree (explainer "4.2", "4.4") and acceptance ("1.1")
 # ---------------------------------------------------------------------------

@@ -440,3 +440,50 @@ def test_planted_defect_is_caught():
     assert gated.sum() > 32
     assert (am_bad[gated] != am[gated]).mean() > 0.5
     assert (am_bad % 7 == 0).mean() > 0.9
+
+
+# ---------------------------------------------------------------------------
+# Certified LM head (explainer "4.1"/"4.3": cheap pass, per-row Cauchy-Schwarz
+# bound, exact rescoring of the survivors; the argmax never changes)
+# ---------------------------------------------------------------------------
+
+def test_certified_head_equals_dense_argmax():
+    w = synth.weights(640, 256, 3, 41, 0.002, 0.002)      # Gaussian, with escapes
+    h = synth.activations(24, 256, 3, 42)
+    p = oracle.w12_pack(w)
+    am, surv, err, qn = oracle.certified_head(h, p)
+    dense, _, _ = oracle.head_argmax(h, oracle.w12_unpack(p))
+    assert np.array_equal(am, dense)
+    assert (surv >= 1).all() and (surv < 640).all()
+    assert (err >= 0).all() and (qn > 0).all()
+
+
+def test_certified_head_bound_holds():
+    """|h.w_v - h.w^_v| <= ||h|| ||w_v - w^_v|| for every row and token
+    (Cauchy-Schwarz), checked on logits computed separately."""
+    w = synth.weights(384, 192, 4, 43, 0.003, 0.003)
+    h = synth.activations(16, 192, 4, 44)
+    p = oracle.w12_pack(w)
+    _, _, err, _ = oracle.certified_head(h, p)
+    s = oracle.gemm_f64(h, oracle.w12_unpack(p))
+    sq = oracle.gemm_f64(h, oracle.w12_unpack_q(p))
+    hn = np.sqrt((synth.bf16_bits_to_f32(h).astype(np.float64) ** 2).sum(axis=1))
+    assert (np.abs(s - sq) <= hn[:, None] * err[None, :] * (1 + 1e-9) + 1e-12).all()
+
+
+def test_certified_head_separates_tokens_the_view_cannot():
+    """Token 1 is token 0 with other low mantissa nibbles: the two share their
+    view bytes, so the cheap pass scores them alike.  With h = w_1 the exact
+    argmax is token 1; the cheap argmax (lowest index on its tie) is token 0;
+    the certified head keeps both and returns token 1."""
+    base = synth.weights(128, 128, 5, 45)
+    g = np.random.default_rng(46)
+    w = base.copy()
+    w[1] = (w[0] & np.uint16(0xFFF0)) | g.integers(0, 16, size=128).astype(np.uint16)
+    h = np.ascontiguousarray(np.vstack([w[1], w[1]]))
+    p = oracle.w12_pack(w)
+    dense, _, _ = oracle.head_argmax(h, oracle.w12_unpack(p))
+    quick, _, _ = oracle.head_argmax(h, oracle.w12_unpack_q(p))
+    am, surv, _, _ = oracle.certified_head(h, p)
+    assert (dense == 1).all() and (quick == 0).all()
+    assert np.array_equal(am, dense) and (surv >= 2).all()
