@@ -459,6 +459,50 @@ def quick_pass(wk: "Workload", K: int, W: int):
             "top1_agreement": round(agree, 4), "rows": int(wk.R)}
 
 
+def certified_head(wk: "Workload", K: int, W: int):
+    """The LM head through the certified head (quick-pass logits of every
+    token, per-row Cauchy-Schwarz bound, exact FP64 rescoring of the
+    survivors): graph-timed launch sequence, survivor counts, and the top-1
+    agreement with the exact head's argmax on the step's rows."""
+    import torch
+    w12 = wk.w12
+    norms = w12.w12_head_cert_norms(wk.head)
+    cws = w12.CertWorkspace(wk.R, wk.head.n)
+    cam = torch.empty_like(wk.argmax)
+    surv = torch.empty(wk.R, dtype=torch.int32, device=wk.argmax.device)
+    fn = lambda: w12.w12_lmhead_argmax_certified(wk.head, norms, wk.h, wk.ws, cws, argmax=cam, survivors=surv)
+    for _ in range(W):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        fn()
+    for _ in range(W):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    if wk.ws.status() != 0:
+        raise RuntimeError(f"device status {w12.status_str(wk.ws.status())}")
+    wk.step()
+    torch.cuda.synchronize()
+    n = surv.cpu().numpy()
+    return {"head_us": round(1e3 * ms, 2), "survivors_mean": round(float(n.mean()), 2),
+            "survivors_max": int(n.max()), "top1_agreement": round(float((cam == wk.argmax).float().mean().item()), 4),
+            "rows": int(wk.R)}
+
+
 # ---------------------------------------------------------------------------
 # step time vs tree rows
 # ---------------------------------------------------------------------------
@@ -657,6 +701,13 @@ def main():
     except Exception as ex:  # reported, never hidden
         quick = {"error": str(ex)[:200]}
 
+    # ------------------------------------------------- certified head
+    cert = None
+    try:
+        cert = certified_head(wk, K, W)
+    except Exception as ex:  # reported, never hidden
+        cert = {"error": str(ex)[:200]}
+
     # --------------------------------------------------- step time vs rows
     sweep = None
     spec = args.rows_sweep
@@ -698,6 +749,7 @@ def main():
             "gpu_launches": K * wk.gpu_launches_per_step(per_weight),
             "rows_sweep": sweep,
             "quick_pass": quick,
+            "certified_head": cert,
         }
         if sweep and len(sweep) > 1 and all("step_us" in e for e in sweep):
             line["rows_sweep_flatness"] = round(sweep[-1]["step_us"] / sweep[0]["step_us"], 4)

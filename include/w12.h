@@ -216,13 +216,42 @@ w12_status w12_lmhead_argmax(const w12_weight *head, const uint16_t *h, int32_t 
  * the quick weights: every in-window weight keeps its sign, exponent and
  * three high mantissa bits and takes 0b1000 as its four low mantissa bits;
  * escaped weights keep their exact value.  Only the 8 KB view plane of each
- * record is read (about 2/3 of the W12 bytes).  Runs on the warp-level MMA
- * path for every row count (row slices of up to 64).
+ * record is read (about 2/3 of the W12 bytes).  Takes the same GEMM path as
+ * the exact pass for the same weight and row count.
  */
 w12_status w12_gemm_q(const w12_weight *w, const uint16_t *x, int32_t R, uint16_t *y, void *ws, size_t ws_bytes,
                       w12_stream_t stream);
 w12_status w12_lmhead_argmax_q(const w12_weight *head, const uint16_t *h, int32_t R, int32_t *argmax,
                                float *maxlogit, void *ws, size_t ws_bytes, w12_stream_t stream);
+
+/*
+ * Certified LM head (explainer 4.1 and 4.3: a cheap pass, a per-row
+ * Cauchy-Schwarz error bound that discards every token proven unable to be
+ * the argmax, exact rescoring of the survivors; the argmax never changes).
+ * The cheap pass is the quick pass above (the 8-bit view in each record,
+ * where the pages keep a separate INT8 copy), so nothing extra is stored.
+ *
+ * w12_head_cert_norms: load time.  norms (device, float[2][head->n]) gets
+ * per token v, rounded up: norms[v] = ||w_v - w^_v|| and
+ * norms[n + v] = ||w^_v||, with w^ the quick weights.  Asynchronous.
+ *
+ * w12_lmhead_argmax_certified: per row r, with s^ the quick logits (BF16)
+ * and eps_v = ||h_r|| (norms[v] + tau norms[n + v]) + 2^-8 |s^_v|
+ * (tau = k * 2^-22 covers the FP32 accumulation of the cheap pass):
+ * L = max_v (s^_v - eps_v); survivors are the tokens with s^_v + eps_v >= L;
+ * their exact logits (W12 decoded exactly, FP64 accumulation) decide
+ * argmax[r] (lowest index on ties); maxlogit[r] (nullable) gets that logit
+ * in FP32; n_survivors[r] (device, nullable) the survivor count.
+ * ws: the w12_lmhead_argmax workspace for R rows and n = vocab; cws: device,
+ * 256-byte aligned, w12_cert_workspace_bytes(R, vocab) bytes.  More than
+ * 1024 survivors in a row records W12_E_WORKSPACE in the device status word
+ * (that row's argmax is then taken over the first 1024 found).
+ */
+w12_status w12_head_cert_norms(const w12_weight *head, float *norms, w12_stream_t stream);
+size_t w12_cert_workspace_bytes(int32_t R, int64_t vocab);
+w12_status w12_lmhead_argmax_certified(const w12_weight *head, const float *norms, const uint16_t *h, int32_t R,
+                                       int32_t *argmax, float *maxlogit, int32_t *n_survivors, void *ws,
+                                       size_t ws_bytes, void *cws, size_t cws_bytes, w12_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Draft tree

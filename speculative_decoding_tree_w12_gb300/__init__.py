@@ -95,6 +95,9 @@ def lib():
             "w12_lmhead_argmax": ([p, p, i32, p, p, p, sz, p], C.c_int),
             "w12_gemm_q": ([p, p, i32, p, p, sz, p], C.c_int),
             "w12_lmhead_argmax_q": ([p, p, i32, p, p, p, sz, p], C.c_int),
+            "w12_head_cert_norms": ([p, p, p], C.c_int),
+            "w12_cert_workspace_bytes": ([i32, i64], sz),
+            "w12_lmhead_argmax_certified": ([p, p, p, i32, p, p, p, p, sz, p, sz, p], C.c_int),
             "w12_tree_build": ([p, i32, p, p, sz, p], C.c_int),
             "w12_tree_accept": ([p, i32, i32, p, p, p, p, p], C.c_int),
             "w12_verify_step": ([p, p, i32, i32, p, p, p, p, sz, p], C.c_int),
@@ -259,6 +262,50 @@ def w12_lmhead_argmax(head: DeviceWeight, h, ws: Workspace, argmax=None, maxlogi
     _check(fn(C.byref(head.c), C.c_void_p(h.data_ptr()), R, C.c_void_p(argmax.data_ptr()),
               C.c_void_p(_dp(maxlogit)) if maxlogit is not None else None, ws.ptr, ws.nbytes,
               _stream(stream)), name)
+    return argmax
+
+
+def w12_head_cert_norms(head: DeviceWeight, out=None, stream=None):
+    """Per token: ||w_v - w^_v|| and ||w^_v|| (w^: quick weights) -> float32
+    [2][n] on the device (load time, for the certified head)."""
+    import torch
+    if out is None:
+        out = torch.empty((2, head.n), dtype=torch.float32, device="cuda")
+    _check(lib().w12_head_cert_norms(C.byref(head.c), C.c_void_p(out.data_ptr()), _stream(stream)),
+           "w12_head_cert_norms")
+    return out
+
+
+class CertWorkspace:
+    """Device buffer for the certified head's quick logits and survivor lists."""
+
+    def __init__(self, R: int, vocab: int, device="cuda"):
+        import torch
+        self.nbytes = int(lib().w12_cert_workspace_bytes(int(R), int(vocab)))
+        if self.nbytes == 0:
+            raise W12Error(W12_E_INVAL, "w12_cert_workspace_bytes")
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+
+    @property
+    def ptr(self):
+        return C.c_void_p(self.buf.data_ptr())
+
+
+def w12_lmhead_argmax_certified(head: DeviceWeight, norms, h, ws: Workspace, cws: CertWorkspace, argmax=None,
+                                maxlogit=None, survivors=None, stream=None):
+    """Certified argmax over ``h . W_head^T`` per row -> int32 [R]: quick-pass
+    logits, per-row Cauchy-Schwarz bound, exact FP64 rescoring of the
+    survivors.  ``survivors`` (int32 [R], optional) gets the survivor counts."""
+    import torch
+    R = h.shape[0]
+    if argmax is None:
+        argmax = torch.empty(R, dtype=torch.int32, device=h.device)
+    _check(lib().w12_lmhead_argmax_certified(C.byref(head.c), C.c_void_p(norms.data_ptr()), C.c_void_p(h.data_ptr()),
+                                             R, C.c_void_p(argmax.data_ptr()),
+                                             C.c_void_p(_dp(maxlogit)) if maxlogit is not None else None,
+                                             C.c_void_p(_dp(survivors)) if survivors is not None else None,
+                                             ws.ptr, ws.nbytes, cws.ptr, cws.nbytes, _stream(stream)),
+           "w12_lmhead_argmax_certified")
     return argmax
 
 

@@ -1,0 +1,222 @@
+// Certified LM head (sm_103a).
+//
+// SpecPilot explainer, sections 4.1 and 4.3: a cheap pass over the head, a
+// per-row Cauchy-Schwarz error bound that discards every token proven unable
+// to be the argmax, and exact rescoring of the survivors, so the argmax never
+// changes.  The pages' cheap pass reads an INT8 copy of the head; here it is
+// the quick pass over the 8-bit view already in every W12 record (w^: view
+// byte, low mantissa nibble 0b1000, escapes exact), so nothing extra is
+// stored.  For row r and token v the bound is ||h_r|| * ||w_v - w^_v||, with
+// slack for the FP32 accumulation and the BF16 output of the cheap pass.
+//
+//   k_cert_norms    load time: ||w_v - w^_v|| and ||w^_v|| per token (FP64
+//                   sums over the decoded record rows, rounded up to FP32)
+//   k_cert_select   per row: ||h_r||, the best lower bound L = max(s^ - eps)
+//                   and the survivors s^ + eps >= L (an unordered list)
+//   k_cert_rescore  per row: exact FP64 logits of the survivors from the W12
+//                   records (exact decode, escapes patched), the argmax with
+//                   the lowest index on ties
+#include <cuda_runtime.h>
+
+#include <cfloat>
+#include <climits>
+
+#include "w12_device.cuh"
+
+using namespace w12d;
+
+namespace {
+
+__device__ __forceinline__ float bf16f(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+// the 16 weights of channel c in the 16-K group kg of a record, exact (nib =
+// the record's low-nibble word) or quick (nib = 0x88888888); escaped slots
+// of the group take their exact value
+__device__ __forceinline__ void decode16(const uint8_t *r, int c, int kg, ChanConst cc, bool quick,
+                                         const int32_t *esc_off, const uint32_t *esc, int64_t t, float (&w)[16])
+{
+    const uint4 v4 = __ldg(reinterpret_cast<const uint4 *>(r + (kg * 128 + c) * 16));
+    const uint32_t vw[4] = {v4.x, v4.y, v4.z, v4.w};
+    uint32_t nw[4] = {0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u};
+    if (!quick) {
+        const uint4 n4 = __ldg(reinterpret_cast<const uint4 *>(r + w12i::kViewBytes + ((kg >> 1) * 128 + c) * 16));
+        nw[0] = n4.x >> ((kg & 1) * 4), nw[1] = n4.y >> ((kg & 1) * 4);
+        nw[2] = n4.z >> ((kg & 1) * 4), nw[3] = n4.w >> ((kg & 1) * 4);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t pp, pq;
+        decode_word(vw[i], nw[i], cc, 16u, pp, pq);
+        w[2 * i] = bf16f(pp & 0xFFFFu), w[2 * i + 1] = bf16f(pp >> 16);
+        w[2 * i + 8] = bf16f(pq & 0xFFFFu), w[2 * i + 9] = bf16f(pq >> 16);
+    }
+    const int32_t e0 = __ldg(esc_off + t), e1 = __ldg(esc_off + t + 1);
+    for (int32_t e = e0; e < e1; ++e) {
+        const uint32_t en = __ldg(esc + e);
+        const int nl = (en >> 22) & 0x7F, kl = (en >> 16) & 0x3F;
+        if (nl != c || (kl >> 4) != kg) continue;
+        const float x = bf16f(en & 0xFFFFu);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (j == (kl & 15)) w[j] = x;
+    }
+}
+
+__global__ void __launch_bounds__(128) k_cert_norms(const uint8_t *__restrict__ rec, const uint8_t *__restrict__ base,
+                                                    const int32_t *__restrict__ esc_off,
+                                                    const uint32_t *__restrict__ esc, int32_t k_tiles, float *err,
+                                                    float *qnorm)
+{
+    const int nt = blockIdx.x, c = threadIdx.x;
+    const ChanConst cc = chan_const(__ldg(base + nt * w12i::kTileN + c));
+    double d2 = 0.0, q2 = 0.0;
+    for (int kt = 0; kt < k_tiles; ++kt) {
+        const int64_t t = (int64_t)nt * k_tiles + kt;
+        const uint8_t *r = rec + t * w12i::kRecBytes;
+        for (int kg = 0; kg < 4; ++kg) {
+            float we[16], wq[16];
+            decode16(r, c, kg, cc, false, esc_off, esc, t, we);
+            decode16(r, c, kg, cc, true, esc_off, esc, t, wq);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const double d = (double)we[j] - (double)wq[j];
+                d2 += d * d;
+                q2 += (double)wq[j] * (double)wq[j];
+            }
+        }
+    }
+    // round up: the bound must not shrink
+    err[nt * w12i::kTileN + c] = __double2float_ru(sqrt(d2) * (1.0 + 1e-12));
+    qnorm[nt * w12i::kTileN + c] = __double2float_ru(sqrt(q2) * (1.0 + 1e-12));
+}
+
+template <typename T, typename Op>
+__device__ T block_reduce(T v, Op op, T *scratch)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, off));
+    __syncthreads();
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    T r = scratch[0];
+    for (int i = 1; i < nw; ++i) r = op(r, scratch[i]);
+    return r;
+}
+
+__global__ void __launch_bounds__(256) k_cert_select(const uint16_t *__restrict__ shat, const uint16_t *__restrict__ h,
+                                                     const float *__restrict__ err, const float *__restrict__ qnorm,
+                                                     int64_t V, int64_t K, double tau, int32_t cap, int32_t *surv,
+                                                     int32_t *cnt, int32_t *cnt_out, int32_t *status)
+{
+    __shared__ double scratch[32];
+    __shared__ int n_s;
+    const int r = blockIdx.x, tid = threadIdx.x;
+    double s = 0.0;
+    for (int64_t k = tid; k < K; k += blockDim.x) {
+        const double x = bf16f(__ldg(h + r * K + k));
+        s += x * x;
+    }
+    s = block_reduce(s, [](double a, double b) { return a + b; }, scratch);
+    const double hn = sqrt(s) * (1.0 + 1e-12);
+    const uint16_t *sr = shat + r * V;
+    // eps: the Cauchy-Schwarz bound, the FP32 accumulation of the cheap pass
+    // (tau ||h|| ||w^||) and its BF16 output (2^-8 |s^|)
+    auto eps_of = [&](int64_t v, double sh) { return hn * ((double)err[v] + tau * (double)qnorm[v]) + 0x1p-8 * fabs(sh); };
+    double lo = -DBL_MAX;
+    for (int64_t v = tid; v < V; v += blockDim.x) {
+        const double sh = bf16f(__ldg(sr + v));
+        lo = fmax(lo, sh - eps_of(v, sh));
+    }
+    lo = block_reduce(lo, [](double a, double b) { return fmax(a, b); }, scratch);
+    if (tid == 0) n_s = 0;
+    __syncthreads();
+    for (int64_t v = tid; v < V; v += blockDim.x) {
+        const double sh = bf16f(__ldg(sr + v));
+        if (sh + eps_of(v, sh) >= lo) {
+            const int i = atomicAdd(&n_s, 1);
+            if (i < cap) surv[(int64_t)r * cap + i] = (int32_t)v;
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        cnt[r] = n_s;
+        if (cnt_out) cnt_out[r] = n_s;
+        if (n_s > cap) atomicCAS(status, 0, (int32_t)W12_E_WORKSPACE);
+    }
+}
+
+__global__ void __launch_bounds__(256) k_cert_rescore(const uint8_t *__restrict__ rec, const uint8_t *__restrict__ base,
+                                                      const int32_t *__restrict__ esc_off,
+                                                      const uint32_t *__restrict__ esc, int32_t k_tiles, int64_t K,
+                                                      const uint16_t *__restrict__ h, const int32_t *__restrict__ surv,
+                                                      const int32_t *__restrict__ cnt, int32_t cap, int32_t *argmax,
+                                                      float *maxlogit)
+{
+    __shared__ double best_s[8];
+    __shared__ int32_t besti_s[8];
+    const int r = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int n = min(cnt[r], cap);
+    const uint16_t *hr = h + r * K;
+    double bv = -DBL_MAX;
+    int32_t bi = INT_MAX;
+    for (int i = warp; i < n; i += 8) {
+        const int32_t v = surv[(int64_t)r * cap + i];
+        const int nt = v >> 7, c = v & 127;
+        const ChanConst cc = chan_const(__ldg(base + v));
+        double acc = 0.0;
+        for (int j = lane; j < 4 * k_tiles; j += 32) {
+            const int kt = j >> 2, kg = j & 3;
+            const int64_t t = (int64_t)nt * k_tiles + kt;
+            float w[16];
+            decode16(rec + t * w12i::kRecBytes, c, kg, cc, false, esc_off, esc, t, w);
+            const uint16_t *hk = hr + kt * 64 + kg * 16;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) acc += (double)w[q] * (double)bf16f(__ldg(hk + q));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (acc > bv || (acc == bv && v < bi)) bv = acc, bi = v;
+    }
+    if (lane == 0) best_s[warp] = bv, besti_s[warp] = bi;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < 8; ++w)
+            if (best_s[w] > bv || (best_s[w] == bv && besti_s[w] < bi)) bv = best_s[w], bi = besti_s[w];
+        argmax[r] = (bi == INT_MAX) ? 0 : bi;
+        if (maxlogit) maxlogit[r] = (float)bv;
+    }
+}
+
+}  // namespace
+
+namespace w12i {
+
+int launch_cert_norms(const DevWeight &w, float *err, float *qnorm, void *stream)
+{
+    k_cert_norms<<<w.n_tiles, 128, 0, static_cast<cudaStream_t>(stream)>>>(w.rec, w.base, w.esc_off, w.esc,
+                                                                           w.k_tiles, err, qnorm);
+    return (int)cudaGetLastError();
+}
+
+int launch_cert_select(const uint16_t *shat, const uint16_t *h, const float *err, const float *qnorm, int32_t R,
+                       int64_t V, int64_t K, int32_t cap, int32_t *surv, int32_t *cnt, int32_t *cnt_out,
+                       int32_t *status, void *stream)
+{
+    // FP32 accumulation of K products: |error| <= K * 2^-23 * ||h|| ||w^|| with
+    // room to spare (2^-22 per product)
+    const double tau = (double)K * 0x1p-22;
+    k_cert_select<<<R, 256, 0, static_cast<cudaStream_t>(stream)>>>(shat, h, err, qnorm, V, K, tau, cap, surv, cnt,
+                                                                     cnt_out, status);
+    return (int)cudaGetLastError();
+}
+
+int launch_cert_rescore(const DevWeight &w, const uint16_t *h, int32_t R, const int32_t *surv, const int32_t *cnt,
+                        int32_t cap, int32_t *argmax, float *maxlogit, void *stream)
+{
+    k_cert_rescore<<<R, 256, 0, static_cast<cudaStream_t>(stream)>>>(w.rec, w.base, w.esc_off, w.esc, w.k_tiles, w.k,
+                                                                      h, surv, cnt, cap, argmax, maxlogit);
+    return (int)cudaGetLastError();
+}
+
+}  // namespace w12i

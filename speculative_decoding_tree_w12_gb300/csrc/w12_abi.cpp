@@ -415,6 +415,59 @@ w12_status w12_lmhead_argmax_q(const w12_weight *head, const uint16_t *h, int32_
     return head_entry(head, h, R, argmax, maxlogit, ws, ws_bytes, stream, true);
 }
 
+// ---------------------------------------------------------------------------
+// certified LM head
+// ---------------------------------------------------------------------------
+
+w12_status w12_head_cert_norms(const w12_weight *head, float *norms, w12_stream_t stream)
+{
+    w12_status s = weight_ok(head);
+    if (s != W12_OK) return s;
+    if (!norms || !aligned(norms, 4)) return W12_E_INVAL;
+    const DevWeight dw = dev_weight(head);
+    return cuda_status(launch_cert_norms(dw, norms, norms + head->n, stream));
+}
+
+size_t w12_cert_workspace_bytes(int32_t R, int64_t vocab)
+{
+    if (R < 1 || vocab < 1) return 0;
+    const size_t shat = ((size_t)R * (size_t)vocab * 2 + 255) / 256 * 256;
+    const size_t surv = ((size_t)R * kCertCap * 4 + 255) / 256 * 256;
+    const size_t cnt = ((size_t)R * 4 + 255) / 256 * 256;
+    return shat + surv + cnt;
+}
+
+w12_status w12_lmhead_argmax_certified(const w12_weight *head, const float *norms, const uint16_t *h, int32_t R,
+                                       int32_t *argmax, float *maxlogit, int32_t *n_survivors, void *ws,
+                                       size_t ws_bytes, void *cws, size_t cws_bytes, w12_stream_t stream)
+{
+    w12_status s = weight_ok(head);
+    if (s != W12_OK) return s;
+    if (!norms || !h || !argmax || !aligned(h, 16) || !cws || !aligned(cws, 256)) return W12_E_INVAL;
+    if (R < 1) return W12_E_INVAL;
+    if (R > kMaxRows) return W12_E_UNSUPPORTED;
+    if (cws_bytes < w12_cert_workspace_bytes(R, head->n)) return W12_E_WORKSPACE;
+    const WsLayout L = layout_for(R, head->n, 0, 0);
+    if ((s = ws_check(ws, ws_bytes, L)) != W12_OK) return s;
+    Ws W{static_cast<uint8_t *>(ws), L};
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (int ce = W.clear_counters(st)) return cuda_status(ce);
+    uint8_t *c = static_cast<uint8_t *>(cws);
+    uint16_t *shat = reinterpret_cast<uint16_t *>(c);
+    int32_t *surv = reinterpret_cast<int32_t *>(c + ((size_t)R * head->n * 2 + 255) / 256 * 256);
+    int32_t *cnt = surv + ((size_t)R * kCertCap * 4 + 255) / 256 * 256 / 4;
+    const DevWeight dw = dev_weight(head);
+    int slot = 0;
+    // 1. cheap pass: the quick-pass logits of every token, BF16 [R][V]
+    if (int e = gemm_slices(dw, h, R, kModeLinear, shat, W, slot, false, st, true)) return cuda_status(e);
+    // 2. per row: the bound and the survivors
+    if (int e = launch_cert_select(shat, h, norms, norms + head->n, R, head->n, head->k, kCertCap, surv, cnt,
+                                   n_survivors, W.status(), st))
+        return cuda_status(e);
+    // 3. exact FP64 rescoring of the survivors
+    return cuda_status(launch_cert_rescore(dw, h, R, surv, cnt, kCertCap, argmax, maxlogit, st));
+}
+
 w12_status w12_tree_build(const w12_lattice *lat, int32_t budget, w12_tree *out, void *ws, size_t ws_bytes,
                           w12_stream_t stream)
 {

@@ -225,6 +225,66 @@ def test_lmhead_argmax_quick_matches_oracle(w12, path, V, K, R):
 
 
 # ---------------------------------------------------------------------------
+# certified LM head: the argmax of exact FP64 logits, on every row
+# ---------------------------------------------------------------------------
+
+def _planted_rows(wh, R, seed, alpha=8.0):
+    g = np.random.default_rng(seed)
+    t = g.integers(0, wh.shape[0], size=R)
+    hf = alpha * synth.bf16_bits_to_f32(wh[t]) + g.standard_normal((R, wh.shape[1]), dtype=np.float32)
+    return synth.f32_to_bf16_bits(hf.astype(np.float32))
+
+
+@pytest.mark.parametrize("V,K,R,planted", [(4096, 512, 8, True), (8192, 1024, 33, True), (2048, 384, 70, False),
+                                           (4096, 640, 200, True), (1024, 256, 5, False)])
+def test_lmhead_certified_matches_dense_fp64(w12, path, V, K, R, planted):
+    wh = synth.weights(V, K, V + K, 31, 0.001, 0.001)
+    pk = oracle.w12_pack(wh)
+    h = _planted_rows(wh, R, V + R) if planted else synth.activations(R, K, V + K, 32)
+    dense, _, _ = oracle.head_argmax(h, oracle.w12_unpack(pk))
+    _, surv_ref, err_ref, qn_ref = oracle.certified_head(h, pk)
+    dw = _packed(w12, wh)
+    norms = w12.w12_head_cert_norms(dw)
+    ws = w12.Workspace(R, V, V)
+    cws = w12.CertWorkspace(R, V)
+    surv = torch.empty(R, dtype=torch.int32, device="cuda")
+    got = w12.w12_lmhead_argmax_certified(dw, norms, _dev_bf16(h), ws, cws, survivors=surv)
+    got2 = w12.w12_lmhead_argmax_certified(dw, norms, _dev_bf16(h), ws, cws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    assert np.array_equal(got.cpu().numpy(), dense)               # every row, no margin gate
+    assert torch.equal(got, got2)
+    n = surv.cpu().numpy()
+    assert (n >= 1).all() and (n <= 1024).all()
+    nm = norms.cpu().numpy().astype(np.float64)
+    assert (nm[0] >= err_ref * (1 - 1e-6)).all() and np.allclose(nm[0], err_ref, rtol=1e-5, atol=1e-12)
+    assert (nm[1] >= qn_ref * (1 - 1e-6)).all() and np.allclose(nm[1], qn_ref, rtol=1e-5)
+
+
+def test_lmhead_certified_separates_tokens_the_view_cannot(w12):
+    """Token 1 is token 0 with other low mantissa nibbles (same view bytes):
+    the quick argmax takes token 0, the certified and dense argmax token 1."""
+    base = synth.weights(256, 256, 5, 45)
+    g = np.random.default_rng(46)
+    wh = base.copy()
+    wh[1] = (wh[0] & np.uint16(0xFFF0)) | g.integers(0, 16, size=256).astype(np.uint16)
+    h = np.ascontiguousarray(np.vstack([wh[1]] * 4))
+    pk = oracle.w12_pack(wh)
+    dense, _, _ = oracle.head_argmax(h, oracle.w12_unpack(pk))
+    dw = _packed(w12, wh)
+    norms = w12.w12_head_cert_norms(dw)
+    ws = w12.Workspace(4, 256, 256)
+    cws = w12.CertWorkspace(4, 256)
+    surv = torch.empty(4, dtype=torch.int32, device="cuda")
+    got = w12.w12_lmhead_argmax_certified(dw, norms, _dev_bf16(h), ws, cws, survivors=surv)
+    quick = w12.w12_lmhead_argmax(dw, _dev_bf16(h), ws, quick=True)
+    torch.cuda.synchronize()
+    assert (dense == 1).all()
+    assert (got.cpu().numpy() == 1).all() and (surv.cpu().numpy() >= 2).all()
+    assert (quick.cpu().numpy() == 0).all()
+
+
+# ---------------------------------------------------------------------------
 # tree build and acceptance
 # ---------------------------------------------------------------------------
 
