@@ -243,9 +243,11 @@ w12_status w12_lmhead_argmax_q(const w12_weight *head, const uint16_t *h, int32_
  * argmax[r] (lowest index on ties); maxlogit[r] (nullable) gets that logit
  * in FP32; n_survivors[r] (device, nullable) the survivor count.
  * ws: the w12_lmhead_argmax workspace for R rows and n = vocab; cws: device,
- * 256-byte aligned, w12_cert_workspace_bytes(R, vocab) bytes.  More than
- * 1024 survivors in a row records W12_E_WORKSPACE in the device status word
- * (that row's argmax is then taken over the first 1024 found).
+ * 256-byte aligned, w12_cert_workspace_bytes(R, vocab) bytes (room for every
+ * token of every row to survive).  The rescoring costs one exact row decode
+ * and a K-long FP64 dot product per survivor: cheap when a row's top logit
+ * stands out, slow (but still exact) when the view's bound keeps much of the
+ * vocabulary, as for unstructured rows.
  */
 w12_status w12_head_cert_norms(const w12_weight *head, float *norms, w12_stream_t stream);
 size_t w12_cert_workspace_bytes(int32_t R, int64_t vocab);

@@ -11,11 +11,14 @@
 //
 //   k_cert_norms    load time: ||w_v - w^_v|| and ||w^_v|| per token (FP64
 //                   sums over the decoded record rows, rounded up to FP32)
-//   k_cert_select   per row: ||h_r||, the best lower bound L = max(s^ - eps)
-//                   and the survivors s^ + eps >= L (an unordered list)
-//   k_cert_rescore  per row: exact FP64 logits of the survivors from the W12
-//                   records (exact decode, escapes patched), the argmax with
-//                   the lowest index on ties
+//   k_cert_lo/surv  64 CTAs per row: ||h_r||, the best lower bound
+//                   L = max(s^ - eps) and the survivors s^ + eps >= L (FP32
+//                   with directed rounding; an unordered list with room for
+//                   the whole vocabulary)
+//   k_cert_rescore  64 CTAs per row: exact FP64 logits of the survivors from
+//                   the W12 records (exact decode, escapes patched), each
+//                   CTA's best; k_cert_final: the row's argmax (lowest index
+//                   on ties)
 #include <cuda_runtime.h>
 
 #include <cfloat>
@@ -104,63 +107,87 @@ __device__ T block_reduce(T v, Op op, T *scratch)
     return r;
 }
 
-__global__ void __launch_bounds__(256) k_cert_select(const uint16_t *__restrict__ shat, const uint16_t *__restrict__ h,
-                                                     const float *__restrict__ err, const float *__restrict__ qnorm,
-                                                     int64_t V, int64_t K, double tau, int32_t cap, int32_t *surv,
-                                                     int32_t *cnt, int32_t *cnt_out, int32_t *status)
+// grid R: hn[r] = ||h_r|| rounded up to FP32 (FP64 sum)
+__global__ void __launch_bounds__(256) k_cert_hnorm(const uint16_t *__restrict__ h, int64_t K, float *hn)
 {
     __shared__ double scratch[32];
-    __shared__ int n_s;
-    const int r = blockIdx.x, tid = threadIdx.x;
+    const uint16_t *hr = h + blockIdx.x * K;
     double s = 0.0;
-    for (int64_t k = tid; k < K; k += blockDim.x) {
-        const double x = bf16f(__ldg(h + r * K + k));
+    for (int64_t k = threadIdx.x; k < K; k += blockDim.x) {
+        const double x = bf16f(__ldg(hr + k));
         s += x * x;
     }
     s = block_reduce(s, [](double a, double b) { return a + b; }, scratch);
-    const double hn = sqrt(s) * (1.0 + 1e-12);
+    if (threadIdx.x == 0) hn[blockIdx.x] = __double2float_ru(sqrt(s) * (1.0 + 1e-12));
+}
+
+// eps of token v, rounded up: the Cauchy-Schwarz bound, the FP32
+// accumulation of the cheap pass (tau ||h|| ||w^||) and its BF16 output
+// (2^-8 |s^|)
+__device__ __forceinline__ float eps_up(float hn, float e, float q, float tau, float sh)
+{
+    return __fadd_ru(__fmul_ru(hn, __fadd_ru(e, __fmul_ru(tau, q))), __fmul_ru(0x1p-8f, fabsf(sh)));
+}
+
+// grid (R, parts): part_lo[r][b] = max over CTA b's tokens of s^ - eps (rounded down)
+__global__ void __launch_bounds__(256) k_cert_lo(const uint16_t *__restrict__ shat, const float *__restrict__ hnorm,
+                                                 const float *__restrict__ err, const float *__restrict__ qnorm,
+                                                 int64_t V, float tau, float *part_lo, int32_t *cnt)
+{
+    __shared__ float fscratch[32];
+    const int r = blockIdx.x, b = blockIdx.y, parts = gridDim.y;
+    const float hn = hnorm[r];
     const uint16_t *sr = shat + r * V;
-    // eps: the Cauchy-Schwarz bound, the FP32 accumulation of the cheap pass
-    // (tau ||h|| ||w^||) and its BF16 output (2^-8 |s^|)
-    auto eps_of = [&](int64_t v, double sh) { return hn * ((double)err[v] + tau * (double)qnorm[v]) + 0x1p-8 * fabs(sh); };
-    double lo = -DBL_MAX;
-    for (int64_t v = tid; v < V; v += blockDim.x) {
-        const double sh = bf16f(__ldg(sr + v));
-        lo = fmax(lo, sh - eps_of(v, sh));
+    float lo = -FLT_MAX;
+    for (int64_t v = (int64_t)b * blockDim.x + threadIdx.x; v < V; v += (int64_t)parts * blockDim.x) {
+        const float sh = bf16f(__ldg(sr + v));
+        lo = fmaxf(lo, __fsub_rd(sh, eps_up(hn, __ldg(err + v), __ldg(qnorm + v), tau, sh)));
     }
-    lo = block_reduce(lo, [](double a, double b) { return fmax(a, b); }, scratch);
-    if (tid == 0) n_s = 0;
-    __syncthreads();
-    for (int64_t v = tid; v < V; v += blockDim.x) {
-        const double sh = bf16f(__ldg(sr + v));
-        if (sh + eps_of(v, sh) >= lo) {
-            const int i = atomicAdd(&n_s, 1);
-            if (i < cap) surv[(int64_t)r * cap + i] = (int32_t)v;
-        }
-    }
-    __syncthreads();
-    if (tid == 0) {
-        cnt[r] = n_s;
-        if (cnt_out) cnt_out[r] = n_s;
-        if (n_s > cap) atomicCAS(status, 0, (int32_t)W12_E_WORKSPACE);
+    lo = block_reduce(lo, [](float x, float y) { return fmaxf(x, y); }, fscratch);
+    if (threadIdx.x == 0) {
+        part_lo[(int64_t)r * parts + b] = lo;
+        if (b == 0) cnt[r] = 0;
     }
 }
 
+// grid (R, parts): the survivors s^ + eps >= L (L = the row's best lower bound)
+__global__ void __launch_bounds__(256) k_cert_surv(const uint16_t *__restrict__ shat, const float *__restrict__ hnorm,
+                                                   const float *__restrict__ err, const float *__restrict__ qnorm,
+                                                   int64_t V, float tau, const float *part_lo, int32_t *surv,
+                                                   int32_t *cnt)
+{
+    const int r = blockIdx.x, b = blockIdx.y, parts = gridDim.y;
+    const float hn = hnorm[r];
+    float L = -FLT_MAX;
+    for (int i = 0; i < parts; ++i) L = fmaxf(L, part_lo[(int64_t)r * parts + i]);
+    const uint16_t *sr = shat + r * V;
+    for (int64_t v = (int64_t)b * blockDim.x + threadIdx.x; v < V; v += (int64_t)parts * blockDim.x) {
+        const float sh = bf16f(__ldg(sr + v));
+        if (__fadd_ru(sh, eps_up(hn, __ldg(err + v), __ldg(qnorm + v), tau, sh)) >= L) {
+            const int i = atomicAdd(cnt + r, 1);
+            surv[(int64_t)r * V + i] = (int32_t)v;   // at most V survivors: the list never overflows
+        }
+    }
+}
+
+// grid (R, parts): CTA (r, b) rescores survivors b*8 + warp, b*8 + warp + 8*parts, ...
+// of row r and writes its best (logit, token) to part_v/part_i[r][b]
 __global__ void __launch_bounds__(256) k_cert_rescore(const uint8_t *__restrict__ rec, const uint8_t *__restrict__ base,
                                                       const int32_t *__restrict__ esc_off,
                                                       const uint32_t *__restrict__ esc, int32_t k_tiles, int64_t K,
                                                       const uint16_t *__restrict__ h, const int32_t *__restrict__ surv,
-                                                      const int32_t *__restrict__ cnt, int32_t cap, int32_t *argmax,
-                                                      float *maxlogit)
+                                                      const int32_t *__restrict__ cnt, int64_t cap, double *part_v,
+                                                      int32_t *part_i)
 {
     __shared__ double best_s[8];
     __shared__ int32_t besti_s[8];
     const int r = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int n = min(cnt[r], cap);
+    const int parts = gridDim.y, b = blockIdx.y;
+    const int64_t n = min((int64_t)cnt[r], cap);
     const uint16_t *hr = h + r * K;
     double bv = -DBL_MAX;
     int32_t bi = INT_MAX;
-    for (int i = warp; i < n; i += 8) {
+    for (int64_t i = (int64_t)b * 8 + warp; i < n; i += 8 * (int64_t)parts) {
         const int32_t v = surv[(int64_t)r * cap + i];
         const int nt = v >> 7, c = v & 127;
         const ChanConst cc = chan_const(__ldg(base + v));
@@ -183,9 +210,27 @@ __global__ void __launch_bounds__(256) k_cert_rescore(const uint8_t *__restrict_
     if (threadIdx.x == 0) {
         for (int w = 1; w < 8; ++w)
             if (best_s[w] > bv || (best_s[w] == bv && besti_s[w] < bi)) bv = best_s[w], bi = besti_s[w];
-        argmax[r] = (bi == INT_MAX) ? 0 : bi;
-        if (maxlogit) maxlogit[r] = (float)bv;
+        part_v[(int64_t)r * parts + b] = bv;
+        part_i[(int64_t)r * parts + b] = bi;
     }
+}
+
+// per row: the best of the parts (lowest token on ties)
+__global__ void k_cert_final(const double *part_v, const int32_t *part_i, int32_t R, int32_t parts, int32_t *argmax,
+                             float *maxlogit, const int32_t *cnt, int32_t *cnt_out)
+{
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= R) return;
+    if (cnt_out) cnt_out[r] = cnt[r];
+    double bv = -DBL_MAX;
+    int32_t bi = INT_MAX;
+    for (int b = 0; b < parts; ++b) {
+        const double v = part_v[(int64_t)r * parts + b];
+        const int32_t i = part_i[(int64_t)r * parts + b];
+        if (v > bv || (v == bv && i < bi)) bv = v, bi = i;
+    }
+    argmax[r] = (bi == INT_MAX) ? 0 : bi;
+    if (maxlogit) maxlogit[r] = (float)bv;
 }
 
 }  // namespace
@@ -200,22 +245,30 @@ int launch_cert_norms(const DevWeight &w, float *err, float *qnorm, void *stream
 }
 
 int launch_cert_select(const uint16_t *shat, const uint16_t *h, const float *err, const float *qnorm, int32_t R,
-                       int64_t V, int64_t K, int32_t cap, int32_t *surv, int32_t *cnt, int32_t *cnt_out,
-                       int32_t *status, void *stream)
+                       int64_t V, int64_t K, int32_t *surv, int32_t *cnt, float *part_lo, void *stream)
 {
     // FP32 accumulation of K products: |error| <= K * 2^-23 * ||h|| ||w^|| with
     // room to spare (2^-22 per product)
-    const double tau = (double)K * 0x1p-22;
-    k_cert_select<<<R, 256, 0, static_cast<cudaStream_t>(stream)>>>(shat, h, err, qnorm, V, K, tau, cap, surv, cnt,
-                                                                     cnt_out, status);
+    const float tau = (float)K * 0x1p-22f;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float *hn = part_lo + (size_t)R * kCertParts;   // R more floats after the partial bounds
+    k_cert_hnorm<<<R, 256, 0, st>>>(h, K, hn);
+    if (cudaError_t e = cudaGetLastError()) return (int)e;
+    k_cert_lo<<<dim3(R, kCertParts), 256, 0, st>>>(shat, hn, err, qnorm, V, tau, part_lo, cnt);
+    if (cudaError_t e = cudaGetLastError()) return (int)e;
+    k_cert_surv<<<dim3(R, kCertParts), 256, 0, st>>>(shat, hn, err, qnorm, V, tau, part_lo, surv, cnt);
     return (int)cudaGetLastError();
 }
 
 int launch_cert_rescore(const DevWeight &w, const uint16_t *h, int32_t R, const int32_t *surv, const int32_t *cnt,
-                        int32_t cap, int32_t *argmax, float *maxlogit, void *stream)
+                        double *part_v, int32_t *part_i, int32_t *argmax, float *maxlogit, int32_t *cnt_out,
+                        void *stream)
 {
-    k_cert_rescore<<<R, 256, 0, static_cast<cudaStream_t>(stream)>>>(w.rec, w.base, w.esc_off, w.esc, w.k_tiles, w.k,
-                                                                      h, surv, cnt, cap, argmax, maxlogit);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    k_cert_rescore<<<dim3(R, kCertParts), 256, 0, st>>>(w.rec, w.base, w.esc_off, w.esc, w.k_tiles, w.k, h, surv, cnt,
+                                                        w.n, part_v, part_i);
+    if (cudaError_t e = cudaGetLastError()) return (int)e;
+    k_cert_final<<<(R + 127) / 128, 128, 0, st>>>(part_v, part_i, R, kCertParts, argmax, maxlogit, cnt, cnt_out);
     return (int)cudaGetLastError();
 }
 

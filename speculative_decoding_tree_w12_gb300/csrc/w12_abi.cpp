@@ -432,9 +432,10 @@ size_t w12_cert_workspace_bytes(int32_t R, int64_t vocab)
 {
     if (R < 1 || vocab < 1) return 0;
     const size_t shat = ((size_t)R * (size_t)vocab * 2 + 255) / 256 * 256;
-    const size_t surv = ((size_t)R * kCertCap * 4 + 255) / 256 * 256;
+    const size_t surv = ((size_t)R * (size_t)vocab * 4 + 255) / 256 * 256;
     const size_t cnt = ((size_t)R * 4 + 255) / 256 * 256;
-    return shat + surv + cnt;
+    const size_t part = ((size_t)R * kCertParts * 16 + (size_t)R * 4 + 255) / 256 * 256;
+    return shat + surv + cnt + part;
 }
 
 w12_status w12_lmhead_argmax_certified(const w12_weight *head, const float *norms, const uint16_t *h, int32_t R,
@@ -455,17 +456,19 @@ w12_status w12_lmhead_argmax_certified(const w12_weight *head, const float *norm
     uint8_t *c = static_cast<uint8_t *>(cws);
     uint16_t *shat = reinterpret_cast<uint16_t *>(c);
     int32_t *surv = reinterpret_cast<int32_t *>(c + ((size_t)R * head->n * 2 + 255) / 256 * 256);
-    int32_t *cnt = surv + ((size_t)R * kCertCap * 4 + 255) / 256 * 256 / 4;
+    int32_t *cnt = surv + ((size_t)R * head->n * 4 + 255) / 256 * 256 / 4;
+    double *part_v = reinterpret_cast<double *>(reinterpret_cast<uint8_t *>(cnt) + ((size_t)R * 4 + 255) / 256 * 256);
+    int32_t *part_i = reinterpret_cast<int32_t *>(part_v + (size_t)R * kCertParts);
+    float *part_lo = reinterpret_cast<float *>(part_i + (size_t)R * kCertParts);
     const DevWeight dw = dev_weight(head);
     int slot = 0;
     // 1. cheap pass: the quick-pass logits of every token, BF16 [R][V]
     if (int e = gemm_slices(dw, h, R, kModeLinear, shat, W, slot, false, st, true)) return cuda_status(e);
     // 2. per row: the bound and the survivors
-    if (int e = launch_cert_select(shat, h, norms, norms + head->n, R, head->n, head->k, kCertCap, surv, cnt,
-                                   n_survivors, W.status(), st))
+    if (int e = launch_cert_select(shat, h, norms, norms + head->n, R, head->n, head->k, surv, cnt, part_lo, st))
         return cuda_status(e);
     // 3. exact FP64 rescoring of the survivors
-    return cuda_status(launch_cert_rescore(dw, h, R, surv, cnt, kCertCap, argmax, maxlogit, st));
+    return cuda_status(launch_cert_rescore(dw, h, R, surv, cnt, part_v, part_i, argmax, maxlogit, n_survivors, st));
 }
 
 w12_status w12_tree_build(const w12_lattice *lat, int32_t budget, w12_tree *out, void *ws, size_t ws_bytes,

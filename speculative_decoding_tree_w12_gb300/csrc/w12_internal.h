@@ -97,13 +97,13 @@ struct TreeArgs {
 int launch_tree_build(const TreeArgs &a, void *stream);
 
 // certified LM head (k_cert.cu)
-constexpr int kCertCap = 1024;   // survivors per row
+constexpr int kCertParts = 64;   // CTAs rescoring one row's survivors
 int launch_cert_norms(const DevWeight &w, float *err, float *qnorm, void *stream);
 int launch_cert_select(const uint16_t *shat, const uint16_t *h, const float *err, const float *qnorm, int32_t R,
-                       int64_t V, int64_t K, int32_t cap, int32_t *surv, int32_t *cnt, int32_t *cnt_out,
-                       int32_t *status, void *stream);
+                       int64_t V, int64_t K, int32_t *surv, int32_t *cnt, float *part_lo, void *stream);
 int launch_cert_rescore(const DevWeight &w, const uint16_t *h, int32_t R, const int32_t *surv, const int32_t *cnt,
-                        int32_t cap, int32_t *argmax, float *maxlogit, void *stream);
+                        double *part_v, int32_t *part_i, int32_t *argmax, float *maxlogit, int32_t *cnt_out,
+                        void *stream);
 int launch_tree_accept(const int32_t *parent, const int32_t *token, const uint8_t *depth,
                        const int32_t *req_row_off, int32_t R, int32_t n_req, int32_t p_max, const int32_t *argmax,
                        int32_t *acc_tok, int32_t *acc_len, int32_t *acc_node, bool pdl, void *stream);
