@@ -9,7 +9,10 @@ lists the readings taken where the pages are silent.
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (exhaustive round trip, hand-computed window cases, NumPy cross-check,
 exact integer GEMM, brute-force tree and acceptance enumeration, the greedy
-autoregressive invariant and the planted-defect mutation).
+autoregressive invariant and the planted-defect mutation); the TLV chain and
+splice by ``tests/test_oracle_tlv.py`` (hand-built trees, greedy
+autoregressive decoding through the combined tree under any Q-pass argmax,
+tree invariants).
 """
 from __future__ import annotations
 
@@ -232,3 +235,80 @@ def tree_accept(tree: Tree, argmax: np.ndarray, n_req: int, p_max: int):
                                  _ptr(tree.req_row_off), n_req, p_max, _ptr(am), _ptr(acc_tok),
                                  _ptr(acc_len), _ptr(acc_node)), "tree_accept")
     return acc_tok, acc_len, acc_node
+
+
+# ---------------------------------------------------------------------------
+# TLV: commit chain and splice (explainer "4.3")
+# ---------------------------------------------------------------------------
+
+BONUS_RANK = 255     # rank of the chain's bonus token: not a drafted candidate
+
+
+def tlv_chain(c_len: np.ndarray, t1_row_off: np.ndarray, budget: int):
+    """Commit chain lengths and the fresh subtree's budget (explainer "4.3").
+
+    The Q pass's greedy acceptance over the first tree gives, per request q,
+    the chain C_q: its accepted draft tokens and the bonus token, c_len[q] of
+    them.  Reading: the exact pass keeps the first tree's budget N; request
+    q commits m_q = min(c_len[q], N_q - 1) chain tokens, N_q being its row
+    count in the first tree (the cap only ever drops the bonus, when the
+    request's whole share was accepted), so every request keeps one row for
+    its subtree root.  The fresh subtrees, drafted from the chain ends, share
+    N - sum(m_q) rows counting their roots, which are the chain ends: for one
+    request that is the pages' N - |C|."""
+    n_req = len(c_len)
+    m = np.zeros(n_req, np.int32)
+    for q in range(n_req):
+        rows_q = int(t1_row_off[q + 1]) - int(t1_row_off[q])
+        m[q] = max(0, min(int(c_len[q]), rows_q - 1))
+    return m, int(budget) - int(m.sum())
+
+
+def tlv_splice(t1: Tree, c_tok: np.ndarray, c_len: np.ndarray, c_node: np.ndarray, m: np.ndarray,
+               t2: Tree, n_req: int) -> Tree:
+    """The combined tree of one TLV cycle (explainer "4.3"): per request the
+    first tree's root, then the first m_q tokens of the commit chain as a
+    path, then the fresh subtree (drafted from the chain end, its root being
+    that end) attached under the chain's last row.
+
+    Rows stay grouped by request, parents before children.  Chain rows copy
+    the first tree's rank and score along the Q-accepted path; the bonus row
+    takes rank BONUS_RANK and its parent's score; a subtree row's depth is
+    m_q plus its own and its score is the chain end's plus its own (FP32)."""
+    par, tok, dep, req, sc, rk = [], [], [], [], [], []
+    off = [0]
+    for q in range(n_req):
+        base = len(par)
+        path = []
+        j = int(c_node[q])
+        while j >= 0:
+            path.append(j)
+            j = int(t1.parent[j])
+        path.reverse()
+        if len(path) != int(c_len[q]) or not 0 <= int(m[q]) <= int(c_len[q]):
+            raise ValueError("commit chain of request %d does not match the first tree" % q)
+        root = path[0]
+        par.append(-1); tok.append(int(t1.token[root])); dep.append(0); req.append(q)
+        sc.append(np.float32(t1.score[root])); rk.append(int(t1.rank[root]))
+        for i in range(1, int(m[q]) + 1):
+            t = int(c_tok[q][i - 1])
+            if i < len(path):
+                if t != int(t1.token[path[i]]):
+                    raise ValueError("chain token %d of request %d is not the tree's" % (i, q))
+                s, r = np.float32(t1.score[path[i]]), int(t1.rank[path[i]])
+            else:
+                s, r = sc[-1], BONUS_RANK
+            par.append(base + i - 1); tok.append(t); dep.append(i); req.append(q); sc.append(s); rk.append(r)
+        end = base + int(m[q])
+        lo, hi = int(t2.req_row_off[q]), int(t2.req_row_off[q + 1])
+        if hi <= lo or int(t2.token[lo]) != tok[end]:
+            raise ValueError("subtree of request %d is not rooted at the chain end" % q)
+        for j in range(lo + 1, hi):
+            par.append(end + int(t2.parent[j]) - lo); tok.append(int(t2.token[j]))
+            dep.append(int(m[q]) + int(t2.depth[j])); req.append(q)
+            sc.append(np.float32(sc[end] + np.float32(t2.score[j]))); rk.append(int(t2.rank[j]))
+        off.append(len(par))
+    R = len(par)
+    return Tree(R, np.asarray(par, np.int32), np.asarray(tok, np.int32), np.asarray(dep, np.uint8),
+                np.asarray(req, np.int32), np.asarray(sc, np.float32), np.asarray(rk, np.uint8),
+                np.asarray(off, np.int32))

@@ -193,14 +193,21 @@ def _log_softmax_sorted(g: np.random.Generator, shape) -> np.ndarray:
     return (cand - lse).astype(np.float32)
 
 
-def lattice(w: Workload, seed: Optional[int] = None) -> Lattice:
+def lattice(w: Workload, seed: Optional[int] = None, truth: Optional[np.ndarray] = None,
+            root_tok: Optional[np.ndarray] = None) -> Lattice:
+    """Drafter lattice of workload ``w``.  ``truth`` ([n_req][p_max + 1]) and
+    ``root_tok`` ([n_req]) replace the drawn continuation and roots when given
+    (a second draft from the end of a committed chain); the random streams are
+    consumed the same way either way."""
     seed = w.seed if seed is None else seed
     g = rng(seed, STREAM_LATTICE)
     gt = rng(seed, STREAM_TRUTH)
     n_req, p_max, V = w.n_req, w.p_max, w.vocab
     p_r = g.choice(np.asarray(w.positions), size=n_req).astype(np.int32)
-    truth = gt.integers(0, V, size=(n_req, p_max + 1)).astype(np.int32)
-    root_tok = gt.integers(0, V, size=n_req).astype(np.int32)
+    drawn_truth = gt.integers(0, V, size=(n_req, p_max + 1)).astype(np.int32)
+    drawn_root = gt.integers(0, V, size=n_req).astype(np.int32)
+    truth = drawn_truth if truth is None else np.ascontiguousarray(truth, np.int32).reshape(n_req, p_max + 1)
+    root_tok = drawn_root if root_tok is None else np.ascontiguousarray(root_tok, np.int32).reshape(n_req)
     cand_tok = np.zeros((n_req, p_max, 16), dtype=np.int32)
     if w.conditional:
         logp = _log_softmax_sorted(g, (n_req, p_max, 16))

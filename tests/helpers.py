@@ -166,3 +166,60 @@ def accepted_parity(acc_tok, acc_len, ref_tok, ref_len, ref_node, parent, margin
         if int(acc_len[r]) != n or not np.array_equal(np.asarray(acc_tok[r][:n]), np.asarray(ref_tok[r][:n])):
             mismatched.append(r)
     return compared, mismatched, near
+
+
+# ---------------------------------------------------------------------------
+# TLV cycle inputs (explainer 4.3): a long true continuation per request, the
+# first lattice over its start, a toy target that prefers the true next token
+# on the true path, a Q-pass argmax that may disagree with it, and the second
+# lattice drafted from each chain end
+# ---------------------------------------------------------------------------
+
+def tlv_truth(w: synth.Workload, p2: int, seed: int) -> np.ndarray:
+    g = np.random.default_rng(seed * 7 + 3)
+    return g.integers(0, w.vocab, size=(w.n_req, w.p_max + p2 + 2)).astype(np.int32)
+
+
+def target_argmax(tree, truth_long: np.ndarray, vocab: int, seed: int) -> np.ndarray:
+    """The toy target's greedy token at every row: a function of the row's
+    (request, root path) only."""
+    paths = synth.tree_paths(tree.parent, tree.token)
+    return np.asarray([synth.planted_token(int(tree.req[j]), paths[j], truth_long, vocab, seed)
+                       for j in range(len(paths))], np.int32)
+
+
+def q_argmax(exact: np.ndarray, err: float, vocab: int, seed: int) -> np.ndarray:
+    """A Q-pass argmax that differs from the exact one at a fraction ``err``
+    of the rows."""
+    g = np.random.default_rng(seed * 11 + 5)
+    q = exact.copy()
+    bad = g.random(len(q)) < err
+    q[bad] = g.integers(0, vocab, size=int(bad.sum()))
+    return q
+
+
+def greedy_ar(req: int, truth_long: np.ndarray, vocab: int, seed: int, n: int) -> List[int]:
+    """n tokens of greedy autoregressive decoding under the toy target."""
+    out: List[int] = []
+    for _ in range(n):
+        out.append(synth.planted_token(req, out, truth_long, vocab, seed))
+    return out
+
+
+def second_lattice(w2: synth.Workload, lat1: synth.Lattice, c_tok: np.ndarray, m: np.ndarray,
+                   truth_long: np.ndarray, seed: int) -> synth.Lattice:
+    """The lattice drafted from each request's chain end: its root is the
+    last committed chain token (the first tree's root when m = 0); where the
+    chain follows the true continuation the drafter is offered the rest of
+    it, elsewhere a drawn one."""
+    p2 = w2.p_max
+    g = np.random.default_rng(seed * 13 + 7)
+    truth2 = g.integers(0, w2.vocab, size=(w2.n_req, p2 + 1)).astype(np.int32)
+    root2 = np.asarray(lat1.root_tok, np.int32).copy()
+    for q in range(w2.n_req):
+        mq = int(m[q])
+        if mq:
+            root2[q] = int(c_tok[q][mq - 1])
+        if np.array_equal(np.asarray(c_tok[q][:mq]), truth_long[q, :mq]):
+            truth2[q] = truth_long[q, mq:mq + p2 + 1]
+    return synth.lattice(w2, seed + 101, truth=truth2, root_tok=root2)
