@@ -302,6 +302,8 @@ w12_status w12_tree_build(const w12_lattice *lat, int32_t budget, w12_tree *out,
  * parent.  acc_tok[n_req][p_max + 1] gets the deepest accepted node's draft
  * tokens followed by the bonus token (argmax at that node), padded with -1;
  * acc_len[n_req] = tau = depth + 1; acc_node[n_req] (nullable) the row.
+ * p_max: the tree's deepest row depth or more (<= 33, which covers a
+ * spliced TLV tree); the row stride of acc_tok is p_max + 1.
  */
 w12_status w12_tree_accept(const w12_tree *tree, int32_t n_req, int32_t p_max, const int32_t *argmax,
                            int32_t *acc_tok, int32_t *acc_len, int32_t *acc_node, w12_stream_t stream);
@@ -329,6 +331,63 @@ typedef struct {
 w12_status w12_verify_step(const w12_step *step, const w12_tree *tree, int32_t n_req, int32_t p_max,
                            int32_t *acc_tok, int32_t *acc_len, int32_t *acc_node, void *ws, size_t ws_bytes,
                            w12_stream_t stream);
+
+/*
+ * The Q pass of TLV (explainer 4.3): the same pass on the quick weights
+ * (w12_gemm_q semantics for every linear and the head).  Its acceptance
+ * output is the commit chain C: per request the Q-accepted draft tokens and
+ * the Q bonus token (acc_tok), their count (acc_len) and the deepest
+ * Q-accepted row (acc_node).  Same arguments and workspace as
+ * w12_verify_step.
+ */
+w12_status w12_verify_step_q(const w12_step *step, const w12_tree *tree, int32_t n_req, int32_t p_max,
+                             int32_t *acc_tok, int32_t *acc_len, int32_t *acc_node, void *ws, size_t ws_bytes,
+                             w12_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * TLV: two-level verification (explainer 4.3)
+ *
+ *   tree T1 --w12_verify_step_q--> chain C (device)
+ *   C lengths + T1 row offsets (read to the host) --w12_tlv_chain--> m, subtree budget
+ *   lattice drafted from each chain end --w12_tree_build(budget)--> subtree T2
+ *   T1 + C + T2 --w12_tlv_splice--> combined tree --w12_verify_step--> accepted tokens
+ *
+ * Only the exact pass over the combined tree accepts tokens; C is a
+ * proposal, so the output is lossless whatever the Q pass chose.
+ * ---------------------------------------------------------------------- */
+
+/*
+ * Host only, no device work.  c_len[n_req]: the chain lengths (acc_len of
+ * the Q pass); t1_row_off[n_req + 1]: T1's req_row_off; budget: the node
+ * budget N the exact pass keeps.  Request q commits
+ * m[q] = min(c_len[q], N_q - 1) chain tokens, N_q being its rows in T1 (the
+ * cap only drops the bonus, when the whole share was accepted, so every
+ * request keeps a row for its subtree root); *sub_budget = N - sum(m): the
+ * budget of the fresh subtrees, counting their roots, which are the chain
+ * ends (for one request: N - |C|).  W12_E_INVAL if c_len[q] is not in
+ * [1, N_q] or the offsets are not those of a tree of at most N rows.
+ */
+w12_status w12_tlv_chain(const int32_t *c_len, const int32_t *t1_row_off, int32_t n_req, int32_t budget, int32_t *m,
+                         int32_t *sub_budget);
+
+/*
+ * The combined tree (device, asynchronous).  t1: the first tree (R set);
+ * c_tok[n_req][p1_max + 1], c_len[n_req], c_node[n_req]: the Q pass's
+ * acceptance outputs for t1 (device); m: HOST [n_req] from w12_tlv_chain;
+ * t2: the subtree built with the lattice whose roots are the chain ends
+ * (R set, req required).  Per request the rows are t1's root, the first m[q]
+ * tokens of the chain as a path (draft rows keep t1's rank and score; the
+ * bonus row takes rank 255 and its parent's score), then t2's non-root rows
+ * of q under the chain end (depth + m[q], FP32 score + the chain end's).
+ * out->R = sum(m) + t2->R is set on the host; out's arrays hold that many
+ * rows, req_row_off n_req + 1.  Device check: a chain that is not t1's path
+ * from the root to c_node, a t2 root that is not the chain end, or
+ * inconsistent row offsets set W12_E_INVAL in the status word (ws as for
+ * w12_tree_build); no write goes past out->R rows.
+ */
+w12_status w12_tlv_splice(const w12_tree *t1, const int32_t *c_tok, const int32_t *c_len, const int32_t *c_node,
+                          int32_t n_req, int32_t p1_max, const int32_t *m, const w12_tree *t2, w12_tree *out,
+                          void *ws, size_t ws_bytes, w12_stream_t stream);
 
 #ifdef __cplusplus
 }

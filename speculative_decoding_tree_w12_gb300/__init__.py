@@ -8,7 +8,8 @@ below raises -- there is no fallback.
 
 Entry points (same names as the C ABI): ``w12_pack``, ``w12_unpack``,
 ``w12_load_check``, ``w12_gemm``, ``w12_lmhead_argmax``, ``w12_tree_build``,
-``w12_tree_accept``, ``w12_verify_step``, plus the workspace helpers.
+``w12_tree_accept``, ``w12_verify_step``, the TLV calls (``w12_verify_step_q``,
+``w12_tlv_chain``, ``w12_tlv_splice``), plus the workspace helpers.
 """
 from __future__ import annotations
 
@@ -101,6 +102,9 @@ def lib():
             "w12_tree_build": ([p, i32, p, p, sz, p], C.c_int),
             "w12_tree_accept": ([p, i32, i32, p, p, p, p, p], C.c_int),
             "w12_verify_step": ([p, p, i32, i32, p, p, p, p, sz, p], C.c_int),
+            "w12_verify_step_q": ([p, p, i32, i32, p, p, p, p, sz, p], C.c_int),
+            "w12_tlv_chain": ([p, p, i32, i32, p, p], C.c_int),
+            "w12_tlv_splice": ([p, p, p, p, i32, i32, p, p, p, p, sz, p], C.c_int),
             "w12_debug_set": ([i32, C.c_uint64], None),
             "w12_debug_num_sms": ([], i32),
             "w12_debug_profile": ([i32], None),
@@ -386,6 +390,42 @@ def w12_verify_step(step: VerifyStep, tree: DeviceTree, n_req: int, p_max: int, 
     _check(lib().w12_verify_step(C.byref(step.c), C.byref(tree.c), n_req, p_max, C.c_void_p(acc_tok.data_ptr()),
                                  C.c_void_p(acc_len.data_ptr()), C.c_void_p(_dp(acc_node)) if acc_node is not None
                                  else None, ws.ptr, ws.nbytes, _stream(stream)), "w12_verify_step")
+
+
+def w12_verify_step_q(step: VerifyStep, tree: DeviceTree, n_req: int, p_max: int, ws: Workspace, acc_tok,
+                      acc_len, acc_node=None, stream=None):
+    """The TLV Q pass: ``w12_verify_step`` on the quick weights; its
+    acceptance outputs are the commit chain."""
+    _check(lib().w12_verify_step_q(C.byref(step.c), C.byref(tree.c), n_req, p_max, C.c_void_p(acc_tok.data_ptr()),
+                                   C.c_void_p(acc_len.data_ptr()), C.c_void_p(_dp(acc_node)) if acc_node is not None
+                                   else None, ws.ptr, ws.nbytes, _stream(stream)), "w12_verify_step_q")
+
+
+def w12_tlv_chain(c_len_host, t1_row_off_host, budget: int):
+    """Host call: chain tokens committed per request and the subtree budget."""
+    c_len = np.ascontiguousarray(c_len_host, np.int32)
+    off = np.ascontiguousarray(t1_row_off_host, np.int32)
+    n_req = len(c_len)
+    if len(off) != n_req + 1:
+        raise ValueError("t1_row_off needs n_req + 1 entries")
+    m = np.empty(n_req, np.int32)
+    sub = C.c_int32(0)
+    _check(lib().w12_tlv_chain(_np(c_len), _np(off), n_req, int(budget), _np(m), C.byref(sub)), "w12_tlv_chain")
+    return m, int(sub.value)
+
+
+def w12_tlv_splice(t1: DeviceTree, c_tok, c_len, c_node, m_host, t2: DeviceTree, ws: Workspace,
+                   out: Optional[DeviceTree] = None, stream=None) -> DeviceTree:
+    """The combined tree of one TLV cycle (device)."""
+    m = np.ascontiguousarray(m_host, np.int32)
+    n_req = len(m)
+    p1_max = int(c_tok.shape[1]) - 1
+    if out is None:
+        out = DeviceTree(max(1, int(m.sum()) + t2.R), n_req, device=c_tok.device)
+    _check(lib().w12_tlv_splice(C.byref(t1.c), C.c_void_p(c_tok.data_ptr()), C.c_void_p(c_len.data_ptr()),
+                                C.c_void_p(c_node.data_ptr()), n_req, p1_max, _np(m), C.byref(t2.c),
+                                C.byref(out.c), ws.ptr, ws.nbytes, _stream(stream)), "w12_tlv_splice")
+    return out
 
 
 def debug_set(flags: int = 0, timeout_ns: int = 0):

@@ -529,13 +529,18 @@ w12_status w12_tree_accept(const w12_tree *tree, int32_t n_req, int32_t p_max, c
     if (s != W12_OK) return s;
     if (!argmax || !acc_tok || !acc_len) return W12_E_INVAL;
     if (n_req < 1 || p_max < 0) return W12_E_INVAL;
-    if (n_req > kMaxBudget || p_max > kMaxPositions) return W12_E_UNSUPPORTED;
+    if (n_req > kMaxBudget || p_max > kMaxDepth) return W12_E_UNSUPPORTED;
     return cuda_status(launch_tree_accept(tree->parent, tree->token, tree->depth, tree->req_row_off, tree->R, n_req,
                                           p_max, argmax, acc_tok, acc_len, acc_node, false, stream));
 }
 
-w12_status w12_verify_step(const w12_step *step, const w12_tree *tree, int32_t n_req, int32_t p_max, int32_t *acc_tok,
-                           int32_t *acc_len, int32_t *acc_node, void *ws, size_t ws_bytes, w12_stream_t stream)
+}  // extern "C"
+
+namespace {
+
+w12_status verify_step_entry(const w12_step *step, const w12_tree *tree, int32_t n_req, int32_t p_max,
+                             int32_t *acc_tok, int32_t *acc_len, int32_t *acc_node, void *ws, size_t ws_bytes,
+                             w12_stream_t stream, bool qview)
 {
     if (!step || step->n_linear < 0 || (step->n_linear > 0 && (!step->lin || !step->x || !step->y)))
         return W12_E_INVAL;
@@ -543,7 +548,7 @@ w12_status w12_verify_step(const w12_step *step, const w12_tree *tree, int32_t n
     if (s != W12_OK) return s;
     if (!acc_tok || !acc_len || !step->h || !step->argmax || !aligned(step->h, 16)) return W12_E_INVAL;
     if (n_req < 1 || p_max < 0) return W12_E_INVAL;
-    if (n_req > kMaxBudget || p_max > kMaxPositions) return W12_E_UNSUPPORTED;
+    if (n_req > kMaxBudget || p_max > kMaxDepth) return W12_E_UNSUPPORTED;
     const int32_t R = tree->R;
     if (R > kMaxRows) return W12_E_UNSUPPORTED;
     if ((s = weight_ok(step->head)) != W12_OK) return s;
@@ -562,10 +567,11 @@ w12_status w12_verify_step(const w12_step *step, const w12_tree *tree, int32_t n
     if (prof_mark(st)) return W12_E_CUDA;
     int slot = 0;
     for (int32_t l = 0; l < step->n_linear; ++l)
-        if (int e = gemm_slices(dev_weight(&step->lin[l]), step->x[l], R, kModeLinear, step->y[l], W, slot, true, st))
+        if (int e = gemm_slices(dev_weight(&step->lin[l]), step->x[l], R, kModeLinear, step->y[l], W, slot, true, st,
+                                qview))
             return cuda_status(e);
     const DevWeight hw = dev_weight(step->head);
-    if (int e = gemm_slices(hw, step->h, R, kModeHead, nullptr, W, slot, true, st)) return cuda_status(e);
+    if (int e = gemm_slices(hw, step->h, R, kModeHead, nullptr, W, slot, true, st, qview)) return cuda_status(e);
     if (int e = launch_argmax_stage2(W.s1_val(), W.s1_idx(), R, hw.n_tiles, step->argmax, nullptr, true, st))
         return cuda_status(e);
     if (prof_mark(st)) return W12_E_CUDA;
@@ -573,6 +579,96 @@ w12_status w12_verify_step(const w12_step *step, const w12_tree *tree, int32_t n
                                    step->argmax, acc_tok, acc_len, acc_node, true, stream))
         return cuda_status(e);
     return prof_mark(st) ? W12_E_CUDA : W12_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+w12_status w12_verify_step(const w12_step *step, const w12_tree *tree, int32_t n_req, int32_t p_max, int32_t *acc_tok,
+                           int32_t *acc_len, int32_t *acc_node, void *ws, size_t ws_bytes, w12_stream_t stream)
+{
+    return verify_step_entry(step, tree, n_req, p_max, acc_tok, acc_len, acc_node, ws, ws_bytes, stream, false);
+}
+
+w12_status w12_verify_step_q(const w12_step *step, const w12_tree *tree, int32_t n_req, int32_t p_max,
+                             int32_t *acc_tok, int32_t *acc_len, int32_t *acc_node, void *ws, size_t ws_bytes,
+                             w12_stream_t stream)
+{
+    return verify_step_entry(step, tree, n_req, p_max, acc_tok, acc_len, acc_node, ws, ws_bytes, stream, true);
+}
+
+w12_status w12_tlv_chain(const int32_t *c_len, const int32_t *t1_row_off, int32_t n_req, int32_t budget, int32_t *m,
+                         int32_t *sub_budget)
+{
+    if (!c_len || !t1_row_off || !m || !sub_budget || n_req < 1 || budget < 1) return W12_E_INVAL;
+    if (n_req > kMaxBudget || budget > kMaxBudget) return W12_E_UNSUPPORTED;
+    if (t1_row_off[0] != 0 || t1_row_off[n_req] > budget) return W12_E_INVAL;
+    int64_t used = 0;
+    for (int32_t q = 0; q < n_req; ++q) {
+        const int32_t rows = t1_row_off[q + 1] - t1_row_off[q];
+        if (rows < 1 || c_len[q] < 1 || c_len[q] > rows) return W12_E_INVAL;
+        m[q] = std::min(c_len[q], rows - 1);
+        used += m[q];
+    }
+    *sub_budget = static_cast<int32_t>(budget - used);
+    return W12_OK;
+}
+
+w12_status w12_tlv_splice(const w12_tree *t1, const int32_t *c_tok, const int32_t *c_len, const int32_t *c_node,
+                          int32_t n_req, int32_t p1_max, const int32_t *m, const w12_tree *t2, w12_tree *out,
+                          void *ws, size_t ws_bytes, w12_stream_t stream)
+{
+    w12_status s = tree_ok(t1, true);
+    if (s != W12_OK) return s;
+    if ((s = tree_ok(t2, true)) != W12_OK) return s;
+    if (!t1->score || !t1->rank || !t2->req || !t2->score || !t2->rank) return W12_E_INVAL;
+    if (!out || !out->parent || !out->token || !out->depth || !out->req || !out->score || !out->rank ||
+        !out->req_row_off)
+        return W12_E_INVAL;
+    if (!c_tok || !c_len || !c_node || !m || n_req < 1 || p1_max < 0) return W12_E_INVAL;
+    if (n_req > kMaxBudget || p1_max > kMaxPositions) return W12_E_UNSUPPORTED;
+    int64_t R = t2->R;
+    for (int32_t q = 0; q < n_req; ++q) {
+        if (m[q] < 0 || m[q] > p1_max + 1) return W12_E_INVAL;
+        R += m[q];
+    }
+    if (R > kMaxBudget) return W12_E_UNSUPPORTED;
+    const WsLayout L = layout_for(1, 0, 0, n_req);
+    if ((s = ws_check(ws, ws_bytes, L)) != W12_OK) return s;
+    Ws W{static_cast<uint8_t *>(ws), L};
+    out->R = static_cast<int32_t>(R);
+    SpliceArgs a{};
+    a.n_req = n_req;
+    a.p1_max = p1_max;
+    a.t1_R = t1->R;
+    a.t2_R = t2->R;
+    a.R = out->R;
+    a.m_host = m;
+    a.t1_parent = t1->parent;
+    a.t1_token = t1->token;
+    a.t1_off = t1->req_row_off;
+    a.t1_rank = t1->rank;
+    a.t1_score = t1->score;
+    a.c_tok = c_tok;
+    a.c_len = c_len;
+    a.c_node = c_node;
+    a.t2_parent = t2->parent;
+    a.t2_token = t2->token;
+    a.t2_req = t2->req;
+    a.t2_off = t2->req_row_off;
+    a.t2_depth = t2->depth;
+    a.t2_rank = t2->rank;
+    a.t2_score = t2->score;
+    a.parent = out->parent;
+    a.token = out->token;
+    a.req = out->req;
+    a.off = out->req_row_off;
+    a.depth = out->depth;
+    a.rank = out->rank;
+    a.score = out->score;
+    a.status = W.status();
+    return cuda_status(launch_tlv_splice(a, stream));
 }
 
 }  // extern "C"

@@ -15,6 +15,7 @@ constexpr int kViewBytes = 8192;
 constexpr int kMaxRows = 256;
 constexpr int kMaxBudget = 512;
 constexpr int kMaxPositions = 16;
+constexpr int kMaxDepth = 2 * kMaxPositions + 1;   // deepest row of a spliced tree
 constexpr int kCands = 16;
 constexpr int kGemmSlots = 2;        // consecutive GEMMs alternate workspace slots
 
@@ -104,6 +105,24 @@ int launch_cert_select(const uint16_t *shat, const uint16_t *h, const float *err
 int launch_cert_rescore(const DevWeight &w, const uint16_t *h, int32_t R, const int32_t *surv, const int32_t *cnt,
                         double *part_v, int32_t *part_i, int32_t *argmax, float *maxlogit, int32_t *cnt_out,
                         void *stream);
+// TLV splice (k_tlv.cu)
+struct SpliceArgs {
+    int32_t n_req, p1_max, t1_R, t2_R, R;
+    const int32_t *m_host;       // [n_req], host memory (copied into the launch parameters)
+    const int32_t *t1_parent, *t1_token, *t1_off;
+    const uint8_t *t1_rank;
+    const float *t1_score;
+    const int32_t *c_tok, *c_len, *c_node;
+    const int32_t *t2_parent, *t2_token, *t2_req, *t2_off;
+    const uint8_t *t2_depth, *t2_rank;
+    const float *t2_score;
+    int32_t *parent, *token, *req, *off;
+    uint8_t *depth, *rank;
+    float *score;
+    int32_t *status;
+};
+int launch_tlv_splice(const SpliceArgs &a, void *stream);
+
 int launch_tree_accept(const int32_t *parent, const int32_t *token, const uint8_t *depth,
                        const int32_t *req_row_off, int32_t R, int32_t n_req, int32_t p_max, const int32_t *argmax,
                        int32_t *acc_tok, int32_t *acc_len, int32_t *acc_node, bool pdl, void *stream);

@@ -136,3 +136,45 @@ def test_refusals_before_launch(L):
     assert L.w12_workspace_bytes(0, 128, 0, 1) == 0
     assert L.w12_workspace_bytes(257, 128, 0, 1) == 0
     assert w12.status_str(w12.W12_E_TIMEOUT) == "W12_E_TIMEOUT"
+
+
+def test_tlv_chain_equals_oracle(L):
+    """The library's host-side TLV chain rule against the oracle's, on random
+    first-tree shares and chain lengths (no device work)."""
+    g = np.random.default_rng(5)
+    for _ in range(300):
+        n_req = int(g.integers(1, 20))
+        rows = g.integers(1, 12, size=n_req)
+        off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+        budget = int(off[-1] + g.integers(0, 5))
+        c_len = np.asarray([g.integers(1, r + 1) for r in rows], np.int32)
+        m, sub = w12.w12_tlv_chain(c_len, off, budget)
+        m_ref, sub_ref = oracle.tlv_chain(c_len, off, budget)
+        assert np.array_equal(m, m_ref) and sub == sub_ref
+        assert sub >= n_req
+
+
+def test_tlv_refusals_before_launch(L):
+    m = np.zeros(1, np.int32)
+    sub = C.c_int32(0)
+    c_len = np.asarray([3], np.int32)
+    off = np.asarray([0, 2], np.int32)   # a chain longer than the request's rows
+    assert L.w12_tlv_chain(c_len.ctypes.data, off.ctypes.data, 1, 4, m.ctypes.data, C.byref(sub)) == w12.W12_E_INVAL
+    off_big = np.asarray([0, 9], np.int32)   # more rows than the budget
+    assert L.w12_tlv_chain(c_len.ctypes.data, off_big.ctypes.data, 1, 4, m.ctypes.data,
+                           C.byref(sub)) == w12.W12_E_INVAL
+    fake = C.c_void_p(0x1000)
+    ws = C.c_void_p(0x100000)
+    t = w12.TreeC(4, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000)
+    out = w12.TreeC(0, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000)
+    mm = np.asarray([2], np.int32)
+    assert L.w12_tlv_splice(C.byref(t), None, fake, fake, 1, 4, mm.ctypes.data, C.byref(t), C.byref(out), ws,
+                            1 << 30, None) == w12.W12_E_INVAL
+    m_bad = np.asarray([6], np.int32)   # more than p1_max + 1 chain tokens
+    assert L.w12_tlv_splice(C.byref(t), fake, fake, fake, 1, 4, m_bad.ctypes.data, C.byref(t), C.byref(out), ws,
+                            1 << 30, None) == w12.W12_E_INVAL
+    t_big = w12.TreeC(510, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000)
+    m5 = np.asarray([5], np.int32)      # 510 + 5 rows: over the 512-row cap
+    assert L.w12_tlv_splice(C.byref(t), fake, fake, fake, 1, 4, m5.ctypes.data, C.byref(t_big), C.byref(out), ws,
+                            1 << 30, None) == w12.W12_E_UNSUPPORTED
+    assert L.w12_tree_accept(C.byref(t), 1, 34, fake, fake, fake, None, None) == w12.W12_E_UNSUPPORTED

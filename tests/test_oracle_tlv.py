@@ -115,11 +115,11 @@ def test_splice_refuses_inconsistent_inputs():
 
 
 CASES = [
-    ("single", dict(n_req=1, positions=(8,), budget=24, vocab=64), 6),
-    ("single_deep", dict(n_req=1, positions=(16,), budget=32, vocab=64), 16),
-    ("batched", dict(n_req=5, positions=(2, 4, 6), budget=40, vocab=64), 5),
+    ("single", dict(n_req=1, positions=(8,), budget=24, vocab=64, n_cand=16), 6),
+    ("single_deep", dict(n_req=1, positions=(16,), budget=32, vocab=64, n_cand=16), 16),
+    ("batched", dict(n_req=5, positions=(2, 4, 6), budget=40, vocab=64, n_cand=16), 5),
     ("chain", dict(n_req=3, positions=(6,), budget=12, vocab=64, n_cand=1), 4),
-    ("roots_only_left", dict(n_req=4, positions=(3,), budget=8, vocab=64), 3),
+    ("roots_only_left", dict(n_req=4, positions=(3,), budget=8, vocab=64, n_cand=16), 3),
 ]
 
 
