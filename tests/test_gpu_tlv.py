@@ -137,7 +137,7 @@ def test_tlv_cycle_with_w12_gemms(w12, n_req, positions, budget, p2):
     """A whole cycle: Q pass (quick weights) over the first tree, chain,
     subtree, splice, exact pass over the combined tree; every stage against
     the oracle on margin-passing rows, and the accepted tokens against
-    greedy decoding of the planted target."""
+    greedy decoding of the same target."""
     seed = 9
     w = synth.scaled(synth.WORKLOADS["single_27b"], vocab=8192, hidden=512, linears=((1024, 512),), n_req=n_req,
                      positions=positions, budget=budget, hit_rate=0.9, seed=seed)
@@ -210,8 +210,22 @@ def test_tlv_cycle_with_w12_gemms(w12, n_req, positions, budget, p2):
                                              tc.parent, mg, w.n_req)
     assert not mism, (mism, near)
     assert len(compared) >= 0.75 * w.n_req
+    # greedy decoding of the same target (the FP64 argmax of each prefix's
+    # hidden row), one token at a time
     for q in compared:
         n = int(a_len[q])
-        assert list(e_tok.cpu().numpy()[q][:n]) == H.greedy_ar(q, truth, w.vocab, seed, n)
-    # the cycle commits at least the chain it verified (the Q pass agreed here)
-    assert np.all(e_len.cpu().numpy()[compared] >= m[compared] + 1)
+        ar = []
+        for _ in range(n):
+            hrow = synth.hidden_row(q, ar, truth, wh, n2, seed)
+            ar.append(int(oracle.head_argmax(hrow[None, :], wh)[0][0]))
+        assert list(e_tok.cpu().numpy()[q][:n]) == ar
+    # where the Q pass agreed with the exact one along the chain, the exact
+    # pass accepts the whole committed chain and one token more
+    am1, _, _ = oracle.head_argmax(h1, wh)
+    for q in compared:
+        rows, j = [], int(c_node[q])
+        while j >= 0:
+            rows.append(j)
+            j = int(t1.parent[j])
+        if all(qam[j] == am1[j] for j in rows):
+            assert int(e_len[q]) >= int(m[q]) + 1
