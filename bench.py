@@ -503,6 +503,114 @@ def certified_head(wk: "Workload", K: int, W: int):
             "rows": int(wk.R)}
 
 
+def tlv_cycle(wk: "Workload", K: int, W: int, seed: int = 0):
+    """One TLV cycle (explainer 4.3) on the step's first tree: the Q pass
+    (w12_verify_step_q: every linear and the head on the view planes, then
+    acceptance, giving the commit chain), the chain lengths read back to the
+    host (w12_tlv_chain), the fresh subtree from the chain ends
+    (w12_tree_build on a second synthetic lattice standing in for the
+    drafter's second draft, prepared once: the inputs repeat every cycle),
+    the splice (w12_tlv_splice) and the exact pass over the combined tree
+    (w12_verify_step).  Eager launches with one host synchronisation per
+    cycle (the chain lengths), timed with CUDA events; per-stage times from
+    events around each stage.  Accepted tokens per exact pass are reported
+    for the toy target of the synthetic rows, next to a single exact pass
+    over the first tree: a property of the synthetic inputs, not of a model."""
+    import torch
+    w12, synth, w = wk.w12, wk.synth, wk.wl
+    dev = wk.argmax.device
+    n_req, p1 = w.n_req, w.p_max
+    p2 = p1
+    p_comb = p1 + 1 + p2
+    i32 = torch.int32
+    c_tok = torch.empty((n_req, p1 + 1), dtype=i32, device=dev)
+    c_len = torch.empty(n_req, dtype=i32, device=dev)
+    c_node = torch.empty(n_req, dtype=i32, device=dev)
+    c_len_host = torch.empty(n_req, dtype=i32, pin_memory=True)
+    q_args = w12.VerifyStep(wk.lin, wk.xs, [torch.empty_like(y) for y in wk.ys], wk.head, wk.h,
+                            torch.empty_like(wk.argmax))
+    row_off = wk.tree.req_row_off.cpu().numpy()
+    # the second draft: rooted at each chain end, offered the rest of the true
+    # continuation where the chain follows it
+    w12.w12_verify_step_q(q_args, wk.tree, n_req, p1, wk.ws, c_tok, c_len, c_node)
+    torch.cuda.synchronize()
+    m, sub = w12.w12_tlv_chain(c_len.cpu().numpy(), row_off, w.budget)
+    g = np.random.default_rng(seed + 977)
+    truth_long = np.concatenate([wk.lat.truth, g.integers(0, w.vocab, size=(n_req, p2 + 1)).astype(np.int32)], 1)
+    ct = c_tok.cpu().numpy()
+    truth2 = g.integers(0, w.vocab, size=(n_req, p2 + 1)).astype(np.int32)
+    root2 = np.asarray(wk.lat.root_tok, np.int32).copy()
+    for q in range(n_req):
+        mq = int(m[q])
+        if mq:
+            root2[q] = int(ct[q][mq - 1])
+        if np.array_equal(ct[q][:mq], truth_long[q, :mq]):
+            truth2[q] = truth_long[q, mq:mq + p2 + 1]
+    lat2 = synth.lattice(synth.scaled(w, positions=(p2,)), seed + 101, truth=truth2, root_tok=root2)
+    dlat2 = w12.DeviceLattice(lat2, dev)
+    t2 = w12.DeviceTree(w.budget, n_req, dev)
+    comb = w12.DeviceTree(w.budget, n_req, dev)
+    w12.w12_tree_build(dlat2, sub, wk.ws, tree=t2)
+    w12.w12_tlv_splice(wk.tree, c_tok, c_len, c_node, m, t2, wk.ws, out=comb)
+    torch.cuda.synchronize()
+    th = comb.host()
+    Rc = comb.R
+    hc = synth.hidden_rows(th["req"], th["parent"], th["token"], truth_long, wk.head_bits, seed,
+                           head_norm2=wk.head_n2)
+    tobf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    xc_layer = [tobf(synth.activations(Rc, k, seed, synth.STREAM_X + i)) for i, (n, k) in enumerate(w.linears)]
+    xc = [xc_layer[j % len(w.linears)] for j in range(len(wk.lin))]
+    yc = [torch.empty((Rc, dw.n), dtype=torch.bfloat16, device=dev) for dw in wk.lin]
+    step_c = w12.VerifyStep(wk.lin, xc, yc, wk.head, tobf(hc), torch.empty(Rc, dtype=i32, device=dev))
+    e_tok = torch.empty((n_req, p_comb + 1), dtype=i32, device=dev)
+    e_len = torch.empty(n_req, dtype=i32, device=dev)
+    e_node = torch.empty(n_req, dtype=i32, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+
+    def cycle(events):
+        if events:
+            events[0].record()
+        w12.w12_verify_step_q(q_args, wk.tree, n_req, p1, wk.ws, c_tok, c_len, c_node)
+        c_len_host.copy_(c_len, non_blocking=True)
+        if events:
+            events[1].record()
+        torch.cuda.current_stream().synchronize()
+        mm, sb = w12.w12_tlv_chain(c_len_host.numpy(), row_off, w.budget)
+        w12.w12_tree_build(dlat2, sb, wk.ws, tree=t2)
+        w12.w12_tlv_splice(wk.tree, c_tok, c_len, c_node, mm, t2, wk.ws, out=comb)
+        if events:
+            events[2].record()
+        w12.w12_verify_step(step_c, comb, n_req, p_comb, wk.ws, e_tok, e_len, e_node)
+        if events:
+            events[3].record()
+
+    for _ in range(W):
+        cycle(None)
+    torch.cuda.synchronize()
+    q_ms = ops_ms = ex_ms = 0.0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        cycle(ev)
+        torch.cuda.synchronize()
+        q_ms += ev[0].elapsed_time(ev[1])
+        ops_ms += ev[1].elapsed_time(ev[2])
+        ex_ms += ev[2].elapsed_time(ev[3])
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    if wk.ws.status() != 0:
+        raise RuntimeError(f"device status {w12.status_str(wk.ws.status())}")
+    wk.step()
+    torch.cuda.synchronize()
+    return {"cycle_us": round(1e3 * ms, 2), "q_pass_us": round(1e3 * q_ms / K, 2),
+            "chain_subtree_splice_us": round(1e3 * ops_ms / K, 2), "exact_pass_us": round(1e3 * ex_ms / K, 2),
+            "rows_q": int(wk.R), "rows_exact": int(Rc), "committed_chain_tokens": int(m.sum()),
+            "synthetic_tokens_per_exact_pass": round(float(e_len.float().mean().item()), 3),
+            "synthetic_tokens_single_pass": round(float(wk.acc_len.float().mean().item()), 3),
+            "timing": "eager launches, one host sync per cycle for the chain lengths, CUDA events"}
+
+
 # ---------------------------------------------------------------------------
 # step time vs tree rows
 # ---------------------------------------------------------------------------
@@ -708,6 +816,13 @@ def main():
     except Exception as ex:  # reported, never hidden
         cert = {"error": str(ex)[:200]}
 
+    # ------------------------------------------------------------ TLV cycle
+    tlv = None
+    try:
+        tlv = tlv_cycle(wk, max(10, min(K, 50)), W)
+    except Exception as ex:  # reported, never hidden
+        tlv = {"error": str(ex)[:200]}
+
     # --------------------------------------------------- step time vs rows
     sweep = None
     spec = args.rows_sweep
@@ -750,6 +865,7 @@ def main():
             "rows_sweep": sweep,
             "quick_pass": quick,
             "certified_head": cert,
+            "tlv_cycle": tlv,
         }
         if sweep and len(sweep) > 1 and all("step_us" in e for e in sweep):
             line["rows_sweep_flatness"] = round(sweep[-1]["step_us"] / sweep[0]["step_us"], 4)
