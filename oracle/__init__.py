@@ -12,7 +12,10 @@ exact integer GEMM, brute-force tree and acceptance enumeration, the greedy
 autoregressive invariant and the planted-defect mutation); the TLV chain and
 splice by ``tests/test_oracle_tlv.py`` (hand-built trees, greedy
 autoregressive decoding through the combined tree under any Q-pass argmax,
-tree invariants).
+tree invariants); the recurrent-layer tree functions by
+``tests/test_oracle_gdn.py`` (closed forms for pure decay and for a unit key
+written at full strength, independence from rows off the root path, an
+independent WY-form restatement, the commit state).
 """
 from __future__ import annotations
 
@@ -312,3 +315,66 @@ def tlv_splice(t1: Tree, c_tok: np.ndarray, c_len: np.ndarray, c_node: np.ndarra
     return Tree(R, np.asarray(par, np.int32), np.asarray(tok, np.int32), np.asarray(dep, np.uint8),
                 np.asarray(req, np.int32), np.asarray(sc, np.float32), np.asarray(rk, np.uint8),
                 np.asarray(off, np.int32))
+
+
+# ---------------------------------------------------------------------------
+# Gated DeltaNet layer over a draft tree (explainer "4.2": a recurrent head
+# keeps a fixed-size state updated once per token; the tree recomputes the
+# state along each root path from the committed state)
+# ---------------------------------------------------------------------------
+
+def gdn_tree_path(S0: np.ndarray, q: np.ndarray, k: np.ndarray, v: np.ndarray, alpha: np.ndarray,
+                  beta: np.ndarray, tree: Tree):
+    """Per-node outputs of one GDN layer over a tree, in FP64, by walking every
+    node's root path from its request's committed state.
+
+    Reading (the pages name the layer and its rank-one updates; the update is
+    the published gated delta rule): per head, with state S (d_v x d_k), a
+    token with gate a, strength b, key k, value v, query q does
+        S <- a * S (I - b k k^T) + b v k^T,      output o = S q.
+    Every row of the tree is a token: the root applies its update to the
+    committed state S0[request], a child to its parent's state.
+
+    S0: float [n_req][H][d_v][d_k]; q, k: BF16 bits [R][H][d_k]; v: BF16 bits
+    [R][H][d_v]; alpha, beta: float [R][H].  Returns o float64 [R][H][d_v]."""
+    qf, kf, vf = _bf16_to_f64(q), _bf16_to_f64(k), _bf16_to_f64(v)
+    a64, b64 = np.asarray(alpha, np.float64), np.asarray(beta, np.float64)
+    R, H, dk = qf.shape
+    dv = vf.shape[2]
+    out = np.empty((R, H, dv), np.float64)
+    for j in range(R):
+        path = []
+        i = j
+        while i >= 0:
+            path.append(i)
+            i = int(tree.parent[i])
+        path.reverse()
+        S = np.array(S0[int(tree.req[j])], np.float64)            # [H][d_v][d_k]
+        for i in path:
+            Sk = np.einsum("hvk,hk->hv", S, kf[i])
+            S = a64[i][:, None, None] * (S - b64[i][:, None, None] * Sk[:, :, None] * kf[i][:, None, :]) \
+                + b64[i][:, None, None] * vf[i][:, :, None] * kf[i][:, None, :]
+        out[j] = np.einsum("hvk,hk->hv", S, qf[j])
+    return out
+
+
+def gdn_commit(S0: np.ndarray, k: np.ndarray, v: np.ndarray, alpha: np.ndarray, beta: np.ndarray, tree: Tree,
+               acc_node: np.ndarray):
+    """The committed state after acceptance (FP64): each request's state
+    replayed along the root path of its deepest accepted row."""
+    kf, vf = _bf16_to_f64(k), _bf16_to_f64(v)
+    a64, b64 = np.asarray(alpha, np.float64), np.asarray(beta, np.float64)
+    out = np.array(S0, np.float64)
+    for r, node in enumerate(acc_node):
+        path = []
+        i = int(node)
+        while i >= 0:
+            path.append(i)
+            i = int(tree.parent[i])
+        S = out[r]
+        for i in reversed(path):
+            Sk = np.einsum("hvk,hk->hv", S, kf[i])
+            S = a64[i][:, None, None] * (S - b64[i][:, None, None] * Sk[:, :, None] * kf[i][:, None, :]) \
+                + b64[i][:, None, None] * vf[i][:, :, None] * kf[i][:, None, :]
+        out[r] = S
+    return out

@@ -319,3 +319,38 @@ def hidden_rows(req: np.ndarray, parent: np.ndarray, token: np.ndarray,
         rows[j] = hidden_row(int(req[j]), path, truth, w_head_bits, head_norm2,
                              seed, plant_logit, noise_std)
     return rows
+
+
+# --------------------------------------------------------------------------
+# recurrent (Gated DeltaNet) layer inputs over a draft tree
+# --------------------------------------------------------------------------
+
+STREAM_GDN = 6000
+
+
+@dataclasses.dataclass
+class GdnInputs:
+    S0: np.ndarray       # float32 [n_req][H][d_v][d_k]: committed states
+    q: np.ndarray        # BF16 bits [R][H][d_k]
+    k: np.ndarray        # BF16 bits [R][H][d_k], rows of unit L2 norm before rounding
+    v: np.ndarray        # BF16 bits [R][H][d_v]
+    alpha: np.ndarray    # float32 [R][H], gates in [0.85, 1)
+    beta: np.ndarray     # float32 [R][H], write strengths in [0.05, 0.95]
+
+
+def gdn_inputs(R: int, n_req: int, H: int, d: int = 128, seed: int = 0, state_std: float = 0.05) -> GdnInputs:
+    """Seeded synthetic inputs of one recurrent layer for R tree rows: keys
+    and queries of unit norm (as the layer normalises them), N(0, 1) values,
+    gates near 1 and write strengths spread over (0, 1), committed states
+    N(0, state_std)."""
+    g = rng(seed, STREAM_GDN)
+    S0 = (g.standard_normal((n_req, H, d, d)) * state_std).astype(np.float32)
+    k = g.standard_normal((R, H, d))
+    k /= np.linalg.norm(k, axis=2, keepdims=True)
+    q = g.standard_normal((R, H, d))
+    q /= np.linalg.norm(q, axis=2, keepdims=True)
+    v = g.standard_normal((R, H, d)).astype(np.float32)
+    alpha = g.uniform(0.85, 1.0, size=(R, H)).astype(np.float32)
+    beta = g.uniform(0.05, 0.95, size=(R, H)).astype(np.float32)
+    return GdnInputs(S0=S0, q=f32_to_bf16_bits(q.astype(np.float32)), k=f32_to_bf16_bits(k.astype(np.float32)),
+                     v=f32_to_bf16_bits(v), alpha=alpha, beta=beta)
