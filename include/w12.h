@@ -309,6 +309,50 @@ w12_status w12_tree_accept(const w12_tree *tree, int32_t n_req, int32_t p_max, c
                            int32_t *acc_tok, int32_t *acc_len, int32_t *acc_node, w12_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Recurrent (Gated DeltaNet) layer over a draft tree (explainer 4.2)
+ *
+ * A GDN head keeps a d x d state S per request, updated by each token with
+ * gate a, write strength b, key k, value v:  S <- a S (I - b k k^T) + b v k^T,
+ * and outputs o = S q.  Every tree row is a token; the root applies its
+ * update to the request's committed state, a child to its parent's state.
+ * No per-node state is stored: the outputs are recomputed along root paths.
+ * ---------------------------------------------------------------------- */
+
+typedef struct {
+    int32_t n_heads;             /* H (>= 1) */
+    int32_t head_dim;            /* d = d_k = d_v; must be 128 */
+    const float *S0;             /* device [n_req][H][d][d] FP32, S0[r][h][v][k]; 16-byte aligned */
+    const uint16_t *q, *k;       /* device BF16 [R][H][d], 4-byte aligned */
+    const uint16_t *v;           /* device BF16 [R][H][d] */
+    const float *alpha, *beta;   /* device [R][H] */
+} w12_gdn_layer;
+
+#define W12_GDN_WY 0     /* WY form: one triangular solve per request and head, state products on tensor cores */
+#define W12_GDN_PATH 1   /* path walk: every row replays its root path on a copy of the committed state */
+
+/*
+ * Per-row outputs o (device FP32 [R][H][d]) of one layer over a tree
+ * (tree->R rows; parent and req_row_off used; rows of a request list every
+ * parent before its children, at most 64 rows per request).  W12_GDN_WY
+ * multiplies the FP32 state as three BF16 pieces that add up to it exactly,
+ * with FP32 accumulation; both methods match the FP64 path walk to FP32
+ * rounding.  Device checks: a request with more than 64 rows sets
+ * W12_E_UNSUPPORTED, a parent outside its request or after its child
+ * W12_E_INVAL in the status word (ws as for w12_tree_build).
+ */
+w12_status w12_gdn_tree_verify(const w12_gdn_layer *layer, const w12_tree *tree, int32_t n_req, int32_t method,
+                               float *o, void *ws, size_t ws_bytes, w12_stream_t stream);
+
+/*
+ * The committed states after acceptance: state[r] (device FP32, same layout
+ * as S0; may be S0 itself) = S0[r] replayed along the root path of row
+ * acc_node[r] (device [n_req], from w12_tree_accept).  Device check: a row
+ * outside the request sets W12_E_INVAL (the state is then left as S0[r]).
+ */
+w12_status w12_gdn_commit(const w12_gdn_layer *layer, const w12_tree *tree, int32_t n_req, const int32_t *acc_node,
+                          float *state, void *ws, size_t ws_bytes, w12_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * The verify step
  * ---------------------------------------------------------------------- */
 

@@ -104,6 +104,8 @@ def lib():
             "w12_verify_step": ([p, p, i32, i32, p, p, p, p, sz, p], C.c_int),
             "w12_verify_step_q": ([p, p, i32, i32, p, p, p, p, sz, p], C.c_int),
             "w12_tlv_chain": ([p, p, i32, i32, p, p], C.c_int),
+            "w12_gdn_tree_verify": ([p, p, i32, i32, p, p, sz, p], C.c_int),
+            "w12_gdn_commit": ([p, p, i32, p, p, p, sz, p], C.c_int),
             "w12_tlv_splice": ([p, p, p, p, i32, i32, p, p, p, p, sz, p], C.c_int),
             "w12_debug_set": ([i32, C.c_uint64], None),
             "w12_debug_num_sms": ([], i32),
@@ -426,6 +428,46 @@ def w12_tlv_splice(t1: DeviceTree, c_tok, c_len, c_node, m_host, t2: DeviceTree,
                                 C.c_void_p(c_node.data_ptr()), n_req, p1_max, _np(m), C.byref(t2.c),
                                 C.byref(out.c), ws.ptr, ws.nbytes, _stream(stream)), "w12_tlv_splice")
     return out
+
+
+class GdnLayerC(C.Structure):
+    _fields_ = [("n_heads", C.c_int32), ("head_dim", C.c_int32), ("S0", C.c_void_p), ("q", C.c_void_p),
+                ("k", C.c_void_p), ("v", C.c_void_p), ("alpha", C.c_void_p), ("beta", C.c_void_p)]
+
+
+W12_GDN_WY, W12_GDN_PATH = 0, 1
+
+
+class GdnLayer:
+    """Device inputs of one recurrent layer over a tree: committed states
+    S0 (float32 [n_req][H][d][d]), q/k/v (bfloat16 [R][H][d]), alpha/beta
+    (float32 [R][H]); kept alive with the marshalled struct."""
+
+    def __init__(self, S0, q, k, v, alpha, beta):
+        self.S0, self.q, self.k, self.v, self.alpha, self.beta = S0, q, k, v, alpha, beta
+        self.H, self.d = int(q.shape[1]), int(q.shape[2])
+        self.c = GdnLayerC(self.H, self.d, S0.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                           alpha.data_ptr(), beta.data_ptr())
+
+
+def w12_gdn_tree_verify(layer: GdnLayer, tree: DeviceTree, n_req: int, ws: Workspace, method: int = W12_GDN_WY,
+                        out=None, stream=None):
+    import torch
+    if out is None:
+        out = torch.empty((tree.R, layer.H, layer.d), dtype=torch.float32, device=layer.q.device)
+    _check(lib().w12_gdn_tree_verify(C.byref(layer.c), C.byref(tree.c), int(n_req), int(method),
+                                     C.c_void_p(out.data_ptr()), ws.ptr, ws.nbytes, _stream(stream)),
+           "w12_gdn_tree_verify")
+    return out
+
+
+def w12_gdn_commit(layer: GdnLayer, tree: DeviceTree, n_req: int, acc_node, ws: Workspace, state=None, stream=None):
+    import torch
+    if state is None:
+        state = torch.empty_like(layer.S0)
+    _check(lib().w12_gdn_commit(C.byref(layer.c), C.byref(tree.c), int(n_req), C.c_void_p(acc_node.data_ptr()),
+                                C.c_void_p(state.data_ptr()), ws.ptr, ws.nbytes, _stream(stream)), "w12_gdn_commit")
+    return state
 
 
 def debug_set(flags: int = 0, timeout_ns: int = 0):

@@ -598,6 +598,68 @@ w12_status w12_verify_step_q(const w12_step *step, const w12_tree *tree, int32_t
     return verify_step_entry(step, tree, n_req, p_max, acc_tok, acc_len, acc_node, ws, ws_bytes, stream, true);
 }
 
+}  // extern "C"
+
+namespace {
+
+w12_status gdn_args(const w12_gdn_layer *L, const w12_tree *tree, int32_t n_req, GdnArgs &a)
+{
+    if (!L || !tree || !tree->parent || !tree->req_row_off || !L->S0 || !L->q || !L->k || !L->v || !L->alpha ||
+        !L->beta)
+        return W12_E_INVAL;
+    if (L->n_heads < 1 || n_req < 1 || tree->R < 1) return W12_E_INVAL;
+    if (L->head_dim != kGdnDim || L->n_heads > 65535 || n_req > kMaxBudget || tree->R > kMaxBudget)
+        return W12_E_UNSUPPORTED;
+    if (!aligned(L->S0, 16) || !aligned(L->q, 4) || !aligned(L->k, 4)) return W12_E_INVAL;
+    a = GdnArgs{};
+    a.H = L->n_heads;
+    a.n_req = n_req;
+    a.S0 = L->S0;
+    a.q = L->q;
+    a.k = L->k;
+    a.v = L->v;
+    a.alpha = L->alpha;
+    a.beta = L->beta;
+    a.parent = tree->parent;
+    a.req_row_off = tree->req_row_off;
+    return W12_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+w12_status w12_gdn_tree_verify(const w12_gdn_layer *layer, const w12_tree *tree, int32_t n_req, int32_t method,
+                               float *o, void *ws, size_t ws_bytes, w12_stream_t stream)
+{
+    GdnArgs a;
+    w12_status s = gdn_args(layer, tree, n_req, a);
+    if (s != W12_OK) return s;
+    if (!o || (method != W12_GDN_WY && method != W12_GDN_PATH)) return W12_E_INVAL;
+    const WsLayout L = layout_for(1, 0, 0, n_req);
+    if ((s = ws_check(ws, ws_bytes, L)) != W12_OK) return s;
+    Ws W{static_cast<uint8_t *>(ws), L};
+    a.out = o;
+    a.status = W.status();
+    return cuda_status(launch_gdn(a, method == W12_GDN_WY ? kGdnWy : kGdnPath, stream));
+}
+
+w12_status w12_gdn_commit(const w12_gdn_layer *layer, const w12_tree *tree, int32_t n_req, const int32_t *acc_node,
+                          float *state, void *ws, size_t ws_bytes, w12_stream_t stream)
+{
+    GdnArgs a;
+    w12_status s = gdn_args(layer, tree, n_req, a);
+    if (s != W12_OK) return s;
+    if (!acc_node || !state || !aligned(state, 16)) return W12_E_INVAL;
+    const WsLayout L = layout_for(1, 0, 0, n_req);
+    if ((s = ws_check(ws, ws_bytes, L)) != W12_OK) return s;
+    Ws W{static_cast<uint8_t *>(ws), L};
+    a.acc_node = acc_node;
+    a.out = state;
+    a.status = W.status();
+    return cuda_status(launch_gdn(a, kGdnCommit, stream));
+}
+
 w12_status w12_tlv_chain(const int32_t *c_len, const int32_t *t1_row_off, int32_t n_req, int32_t budget, int32_t *m,
                          int32_t *sub_budget)
 {

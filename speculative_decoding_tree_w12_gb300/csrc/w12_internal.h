@@ -105,6 +105,21 @@ int launch_cert_select(const uint16_t *shat, const uint16_t *h, const float *err
 int launch_cert_rescore(const DevWeight &w, const uint16_t *h, int32_t R, const int32_t *surv, const int32_t *cnt,
                         double *part_v, int32_t *part_i, int32_t *argmax, float *maxlogit, int32_t *cnt_out,
                         void *stream);
+// recurrent-layer tree verification (k_gdn.cu)
+constexpr int kGdnWy = 0, kGdnPath = 1, kGdnCommit = 2;
+constexpr int kGdnDim = 128;        // head dimension
+constexpr int kGdnMaxRows = 64;     // tree rows of one request
+struct GdnArgs {
+    int32_t H, n_req;
+    const float *S0;
+    const uint16_t *q, *k, *v;
+    const float *alpha, *beta;
+    const int32_t *parent, *req_row_off, *acc_node;
+    float *out;
+    int32_t *status;
+};
+int launch_gdn(const GdnArgs &a, int mode, void *stream);
+
 // TLV splice (k_tlv.cu)
 struct SpliceArgs {
     int32_t n_req, p1_max, t1_R, t2_R, R;
