@@ -611,6 +611,82 @@ def tlv_cycle(wk: "Workload", K: int, W: int, seed: int = 0):
             "timing": "eager launches, one host sync per cycle for the chain lengths, CUDA events"}
 
 
+GDN_LAYERS, GDN_HEADS, GDN_DIM = 48, 32, 128
+
+
+def gdn_stack(wk: "Workload", K: int, W: int, seed: int = 0):
+    """Recurrent-layer tree verification over the step's tree (explainer
+    4.2): 48 Gated DeltaNet layers of 32 heads of 128 (synthetic committed
+    states and q/k/v/gates, 4 distinct input sets, each layer with its own
+    device copy), one launch per layer as a real stack would need, captured
+    in a CUDA graph.  Times the WY kernel, the path-walk kernel and the
+    commit replay of one accepted row per request; bytes are the states read
+    (and written by the commit) plus q/k/v/gates in and outputs out."""
+    import torch
+    w12, synth = wk.w12, wk.synth
+    dev = wk.argmax.device
+    n_req, R = wk.wl.n_req, wk.R
+    tobf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    base = [synth.gdn_inputs(R, n_req, GDN_HEADS, GDN_DIM, seed=seed + i) for i in range(4)]
+    layers = []
+    for l in range(GDN_LAYERS):
+        x = base[l % 4]
+        layers.append(w12.GdnLayer(torch.from_numpy(x.S0).to(dev), tobf(x.q), tobf(x.k), tobf(x.v),
+                                   torch.from_numpy(x.alpha).to(dev), torch.from_numpy(x.beta).to(dev)))
+    outs = [torch.empty((R, GDN_HEADS, GDN_DIM), dtype=torch.float32, device=dev) for _ in range(GDN_LAYERS)]
+    states = [torch.empty_like(L.S0) for L in layers]
+    acc = (wk.tree.req_row_off[1:] - 1).contiguous()   # each request's last row: its deepest branch
+    ws = w12.Workspace(1, 0, 0, n_req, dev)
+
+    def run(method):
+        for L, o in zip(layers, outs):
+            w12.w12_gdn_tree_verify(L, wk.tree, n_req, ws, method, out=o)
+
+    def commit():
+        for L, st in zip(layers, states):
+            w12.w12_gdn_commit(L, wk.tree, n_req, acc, ws, state=st)
+
+    def timed(fn):
+        for _ in range(W):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fn()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            fn()
+        for _ in range(W):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(K):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / K
+
+    ms_wy = timed(lambda: run(w12.W12_GDN_WY))
+    ms_path = timed(lambda: run(w12.W12_GDN_PATH))
+    ms_commit = timed(commit)
+    if ws.status() != 0:
+        raise RuntimeError(f"device status {w12.status_str(ws.status())}")
+    state_b = n_req * GDN_HEADS * GDN_DIM * GDN_DIM * 4
+    io_b = R * GDN_HEADS * (3 * GDN_DIM * 2 + 2 * 4) + R * GDN_HEADS * GDN_DIM * 4
+    verify_bytes = GDN_LAYERS * (state_b + io_b)
+    commit_bytes = GDN_LAYERS * (2 * state_b + R * GDN_HEADS * (2 * GDN_DIM * 2 + 2 * 4))
+    return {"layers": GDN_LAYERS, "heads": GDN_HEADS, "head_dim": GDN_DIM, "rows": int(R), "requests": int(n_req),
+            "wy_us": round(1e3 * ms_wy, 2), "path_us": round(1e3 * ms_path, 2), "commit_us": round(1e3 * ms_commit, 2),
+            "verify_bytes": int(verify_bytes), "wy_gbs": round(verify_bytes / (ms_wy * 1e-3) / 1e9, 1),
+            "commit_gbs": round(commit_bytes / (ms_commit * 1e-3) / 1e9, 1),
+            "timing": "CUDA graph of the 48 per-layer launches, CUDA events",
+            "inputs": "synthetic: N(0, 0.05) states, unit-norm q/k, N(0, 1) v, gates U[0.85, 1), strengths U[0.05, 0.95]"}
+
+
 # ---------------------------------------------------------------------------
 # step time vs tree rows
 # ---------------------------------------------------------------------------
@@ -823,6 +899,13 @@ def main():
     except Exception as ex:  # reported, never hidden
         tlv = {"error": str(ex)[:200]}
 
+    # ------------------------------------------- recurrent-layer verification
+    gdn = None
+    try:
+        gdn = gdn_stack(wk, max(10, min(K, 50)), W)
+    except Exception as ex:  # reported, never hidden
+        gdn = {"error": str(ex)[:200]}
+
     # --------------------------------------------------- step time vs rows
     sweep = None
     spec = args.rows_sweep
@@ -866,6 +949,7 @@ def main():
             "quick_pass": quick,
             "certified_head": cert,
             "tlv_cycle": tlv,
+            "gdn_tree": gdn,
         }
         if sweep and len(sweep) > 1 and all("step_us" in e for e in sweep):
             line["rows_sweep_flatness"] = round(sweep[-1]["step_us"] / sweep[0]["step_us"], 4)

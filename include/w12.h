@@ -322,8 +322,8 @@ typedef struct {
     int32_t n_heads;             /* H (>= 1) */
     int32_t head_dim;            /* d = d_k = d_v; must be 128 */
     const float *S0;             /* device [n_req][H][d][d] FP32, S0[r][h][v][k]; 16-byte aligned */
-    const uint16_t *q, *k;       /* device BF16 [R][H][d], 4-byte aligned */
-    const uint16_t *v;           /* device BF16 [R][H][d] */
+    const uint16_t *q, *k;       /* device BF16 [R][H][d], 16-byte aligned */
+    const uint16_t *v;           /* device BF16 [R][H][d], 4-byte aligned */
     const float *alpha, *beta;   /* device [R][H] */
 } w12_gdn_layer;
 

@@ -93,6 +93,49 @@ __device__ __forceinline__ int request_rows(const GdnParams &p, int r, int &row0
     return n;
 }
 
+// Per-row tree data of one request and head, in shared memory.  Parents,
+// gates and strengths load in parallel; then every row walks up its own
+// parent chain (shared memory, <= 64 steps) for its ancestor set, depth and
+// cumulative gate.  A parent outside the request or not before its child
+// sets W12_E_INVAL and makes the row a root.
+struct TreeInfo {
+    float g[kNR], ginv[kNR], alpha[kNR], beta[kNR];
+    unsigned long long anc[kNR];
+    int32_t par[kNR], depth[kNR];
+};
+
+__device__ __forceinline__ void tree_info(const GdnParams &p, TreeInfo &t, int row0, int n, int h)
+{
+    const int H = p.H;
+    for (int j = threadIdx.x; j < n; j += blockDim.x) {
+        const int pr = p.parent[row0 + j];
+        int pl = pr < 0 ? -1 : pr - row0;
+        if (pr >= 0 && (pl < 0 || pl >= j)) {
+            atomicCAS(p.status, 0, (int32_t)W12_E_INVAL);
+            pl = -1;
+        }
+        t.par[j] = pl;
+        t.alpha[j] = p.alpha[(size_t)(row0 + j) * H + h];
+        t.beta[j] = p.beta[(size_t)(row0 + j) * H + h];
+    }
+    __syncthreads();
+    for (int j = threadIdx.x; j < n; j += blockDim.x) {
+        unsigned long long m = 0ull;
+        float g = t.alpha[j];
+        int d = 0;
+        for (int i = t.par[j]; i >= 0; i = t.par[i]) {   // strictly decreasing: ends within n steps
+            m |= 1ull << i;
+            g *= t.alpha[i];
+            ++d;
+        }
+        t.anc[j] = m;
+        t.g[j] = g;
+        t.ginv[j] = 1.0f / g;
+        t.depth[j] = d;
+    }
+    __syncthreads();
+}
+
 // ---------------------------------------------------------------------------
 // WY form
 // ---------------------------------------------------------------------------
@@ -100,13 +143,12 @@ __device__ __forceinline__ int request_rows(const GdnParams &p, int r, int &row0
 struct WyShared {
     __nv_bfloat16 K[kNR * kKS], Q[kNR * kKS];
     float S[kVS * kSS];
-    float P[kNR * kPS], Rq[kNR * kPS], V[kNR * kPS], U[kNR * kPS];
+    float P[kNR * kPS], Rq[kNR * kPS], U[kNR * kPS];
     float KK[kNR * kMS], QK[kNR * kMS];
-    float g[kNR], ginv[kNR], beta[kNR];
-    unsigned long long anc[kNR];
+    TreeInfo t;
     int8_t order[kNR];
     int8_t lvl_off[kNR + 2];
-    int32_t n_lvl;
+    int32_t maxd;
 };
 
 __global__ void __launch_bounds__(kThreads, 1) k_gdn_wy(const GdnParams p)
@@ -115,76 +157,66 @@ __global__ void __launch_bounds__(kThreads, 1) k_gdn_wy(const GdnParams p)
     WyShared &s = *reinterpret_cast<WyShared *>(smem_raw);
     const int r = blockIdx.x, h = blockIdx.y, vs = blockIdx.z * kVS;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int H = p.H;
     int row0;
     const int n = request_rows(p, r, row0);
     if (n <= 0) return;
-    const int H = p.H;
-
-    // K, Q rows (BF16, zero padding to 16-row tiles), the value slice, the state slice
     const int n16 = (n + 15) & ~15;
-    for (int e = tid; e < n16 * (kD / 2); e += kThreads) {
-        const int j = e / (kD / 2), c2 = (e % (kD / 2)) * 2;
-        uint32_t kw = 0, qw = 0;
-        if (j < n) {
-            const size_t base = ((size_t)(row0 + j) * H + h) * kD + c2;
-            kw = *reinterpret_cast<const uint32_t *>(p.k + base);
-            qw = *reinterpret_cast<const uint32_t *>(p.q + base);
-        }
-        *reinterpret_cast<uint32_t *>(&s.K[j * kKS + c2]) = kw;
-        *reinterpret_cast<uint32_t *>(&s.Q[j * kKS + c2]) = qw;
-    }
-    for (int e = tid; e < n * kVS; e += kThreads) {
-        const int j = e / kVS, c = e % kVS;
-        s.V[j * kPS + c] = bf(p.v[((size_t)(row0 + j) * H + h) * kD + vs + c]);
-    }
+    if (tid == 0) s.maxd = 0;
+
+    // every global read issued before the first shared-memory store: the
+    // state slice, K and Q rows (16-byte pieces, zero padding to 16-row
+    // tiles) and the value slice (kept in registers until the state slice's
+    // space is free)
     const float *S0 = p.S0 + (((size_t)r * H + h) * kD + vs) * kD;
-    for (int e = tid; e < kVS * kD / 4; e += kThreads) {
-        const int v = e / (kD / 4), c4 = (e % (kD / 4)) * 4;
-        const float4 x = *reinterpret_cast<const float4 *>(S0 + (size_t)v * kD + c4);
-        *reinterpret_cast<float4 *>(&s.S[v * kSS + c4]) = x;
+    float4 sv[kVS * kD / 4 / kThreads];
+#pragma unroll
+    for (int i = 0; i < kVS * kD / 4 / kThreads; ++i)
+        sv[i] = *reinterpret_cast<const float4 *>(S0 + (size_t)(tid + i * kThreads) * 4);
+    uint4 kv[kNR * 16 / kThreads], qv[kNR * 16 / kThreads];
+    uint32_t vv[kNR * 16 / kThreads];
+#pragma unroll
+    for (int i = 0; i < kNR * 16 / kThreads; ++i) {
+        const int e = tid + i * kThreads, j = e >> 4;
+        kv[i] = qv[i] = make_uint4(0, 0, 0, 0);
+        vv[i] = 0;
+        if (j < n) {
+            const size_t base = ((size_t)(row0 + j) * H + h) * kD;
+            kv[i] = *reinterpret_cast<const uint4 *>(p.k + base + (e & 15) * 8);
+            qv[i] = *reinterpret_cast<const uint4 *>(p.q + base + (e & 15) * 8);
+            vv[i] = *reinterpret_cast<const uint32_t *>(p.v + base + vs + (e & 15) * 2);
+        }
     }
-    // cumulative gates, ancestor sets and depth levels (rows list parents first)
-    if (tid == 0) {
-        int depth[kNR];
-        int cnt[kNR + 1];
-        for (int d = 0; d <= kNR; ++d) cnt[d] = 0;
-        int maxd = 0;
-        bool ok = true;
-        for (int j = 0; j < n; ++j) {
-            const int pr = p.parent[row0 + j];
-            const float a = p.alpha[(size_t)(row0 + j) * H + h];
-            s.beta[j] = p.beta[(size_t)(row0 + j) * H + h];
-            if (pr < 0) {
-                s.g[j] = a;
-                s.anc[j] = 0ull;
-                depth[j] = 0;
-            } else {
-                const int pl = pr - row0;
-                if (pl < 0 || pl >= j) {   // not a parent listed earlier in this request
-                    ok = false;
-                    s.g[j] = a;
-                    s.anc[j] = 0ull;
-                    depth[j] = 0;
-                } else {
-                    s.g[j] = a * s.g[pl];
-                    s.anc[j] = s.anc[pl] | (1ull << pl);
-                    depth[j] = depth[pl] + 1;
-                }
-            }
-            s.ginv[j] = 1.0f / s.g[j];
-            maxd = max(maxd, depth[j]);
-            ++cnt[depth[j]];
+#pragma unroll
+    for (int i = 0; i < kVS * kD / 4 / kThreads; ++i) {
+        const int e = tid + i * kThreads, v = e / (kD / 4), c4 = (e % (kD / 4)) * 4;
+        *reinterpret_cast<float4 *>(&s.S[v * kSS + c4]) = sv[i];
+    }
+#pragma unroll
+    for (int i = 0; i < kNR * 16 / kThreads; ++i) {
+        const int e = tid + i * kThreads, j = e >> 4;
+        if (j < n16) {
+            *reinterpret_cast<uint4 *>(&s.K[j * kKS + (e & 15) * 8]) = kv[i];
+            *reinterpret_cast<uint4 *>(&s.Q[j * kKS + (e & 15) * 8]) = qv[i];
         }
-        int o = 0;
-        for (int d = 0; d <= maxd; ++d) {
-            s.lvl_off[d] = (int8_t)o;
-            o += cnt[d];
-            cnt[d] = s.lvl_off[d];
+    }
+    // ancestor sets and cumulative gates, then rows ordered by depth level
+    tree_info(p, s.t, row0, n, h);
+    for (int j = tid; j < n; j += kThreads) {
+        const int dj = s.t.depth[j];
+        atomicMax(&s.maxd, dj);
+        int pos = 0;
+        for (int i = 0; i < n; ++i) {
+            const int di = s.t.depth[i];
+            pos += (di < dj) || (di == dj && i < j);
         }
-        s.lvl_off[maxd + 1] = (int8_t)o;
-        s.n_lvl = maxd + 1;
-        for (int j = 0; j < n; ++j) s.order[cnt[depth[j]]++] = (int8_t)j;
-        if (!ok) atomicCAS(p.status, 0, (int32_t)W12_E_INVAL);
+        s.order[pos] = (int8_t)j;
+    }
+    __syncthreads();
+    for (int L = tid; L <= s.maxd + 1; L += kThreads) {
+        int c = 0;
+        for (int i = 0; i < n; ++i) c += s.t.depth[i] < L;
+        s.lvl_off[L] = (int8_t)c;
     }
     __syncthreads();
 
@@ -283,21 +315,33 @@ __global__ void __launch_bounds__(kThreads, 1) k_gdn_wy(const GdnParams p)
     }
     __syncthreads();
 
+    // the value slice moves into the state slice's space, no longer read
+    float *Vf = s.S;
+#pragma unroll
+    for (int i = 0; i < kNR * 16 / kThreads; ++i) {
+        const int e = tid + i * kThreads, j = e >> 4;
+        if (j < n) {
+            Vf[j * kPS + (e & 15) * 2] = __uint_as_float(vv[i] << 16);
+            Vf[j * kPS + (e & 15) * 2 + 1] = __uint_as_float(vv[i] & 0xffff0000u);
+        }
+    }
+    __syncthreads();
     // forward substitution by depth level: U[j] = B[j] - b_j g_j sum_anc (k_i.k_j / g_i) U[i]
     const int c = tid & 31, slot = tid >> 5;
-    for (int L = 0; L < s.n_lvl; ++L) {
+    const int n_lvl = s.maxd + 1;
+    for (int L = 0; L < n_lvl; ++L) {
         const int lo = s.lvl_off[L], hi = s.lvl_off[L + 1];
         for (int t = lo + slot; t < hi; t += kThreads / 32) {
             const int j = s.order[t];
             float sum = 0.f;
-            unsigned long long m = s.anc[j];
+            unsigned long long m = s.t.anc[j];
             while (m) {
                 const int i = __ffsll((long long)m) - 1;
                 m &= m - 1;
-                sum = fmaf(s.KK[j * kMS + i] * s.ginv[i], s.U[i * kPS + c], sum);
+                sum = fmaf(s.KK[j * kMS + i] * s.t.ginv[i], s.U[i * kPS + c], sum);
             }
-            const float bj = s.beta[j], gj = s.g[j];
-            const float B = bj * (s.V[j * kPS + c] - gj * s.P[j * kPS + c]);
+            const float bj = s.t.beta[j], gj = s.t.g[j];
+            const float B = bj * (Vf[j * kPS + c] - gj * s.P[j * kPS + c]);
             s.U[j * kPS + c] = B - bj * gj * sum;
         }
         __syncthreads();
@@ -305,13 +349,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_gdn_wy(const GdnParams p)
     // outputs: o_j = g_j (S0 q_j + sum over the path (k_i.q_j / g_i) u_i)
     for (int j = slot; j < n; j += kThreads / 32) {
         float sum = s.Rq[j * kPS + c];
-        unsigned long long m = s.anc[j] | (1ull << j);
+        unsigned long long m = s.t.anc[j] | (1ull << j);
         while (m) {
             const int i = __ffsll((long long)m) - 1;
             m &= m - 1;
-            sum = fmaf(s.QK[j * kMS + i] * s.ginv[i], s.U[i * kPS + c], sum);
+            sum = fmaf(s.QK[j * kMS + i] * s.t.ginv[i], s.U[i * kPS + c], sum);
         }
-        p.out[((size_t)(row0 + j) * H + h) * kD + vs + c] = s.g[j] * sum;
+        p.out[((size_t)(row0 + j) * H + h) * kD + vs + c] = s.t.g[j] * sum;
     }
 }
 
@@ -320,28 +364,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_gdn_wy(const GdnParams p)
 // ---------------------------------------------------------------------------
 
 struct PathShared {
+    float S[kVS * kD];
     float K[kNR * kD];
     float V[kNR * kVS];
-    float alpha[kNR], beta[kNR];
-    int32_t par[kNR];
-    int32_t path[kNR + 1];
-    int32_t path_len;
+    TreeInfo t;
 };
 
 // One walk: a warp's 4 state rows (lane holds columns lane + 32 e) start from
-// the committed state and take every update on row `node`'s root path.
-__device__ __forceinline__ void walk(const PathShared &s, const float *S0, int vrow0, int lane, float w[4][4])
+// the committed state and take the update of every row in `path` (a row set
+// closed under parents; ascending row order is root first).
+__device__ __forceinline__ void walk(const PathShared &s, unsigned long long path, int vrow0, int lane, float w[4][4])
 {
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) w[r][e] = S0[(size_t)(vrow0 + r) * kD + lane + 32 * e];
-    for (int t = 0; t < s.path_len; ++t) {
-        const int i = s.path[t];
+        for (int e = 0; e < 4; ++e) w[r][e] = s.S[(vrow0 + r) * kD + lane + 32 * e];
+    while (path) {
+        const int i = __ffsll((long long)path) - 1;
+        path &= path - 1;
         float kk[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) kk[e] = s.K[i * kD + lane + 32 * e];
-        const float a = s.alpha[i], b = s.beta[i];
+        const float a = s.t.alpha[i], b = s.t.beta[i];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             float d = w[r][0] * kk[0];
@@ -364,10 +408,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_gdn_path(const GdnParams p)
     PathShared &s = *reinterpret_cast<PathShared *>(smem_raw);
     const int r = blockIdx.x, h = blockIdx.y, vs = blockIdx.z * kVS;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int H = p.H;
+    const float *S0 = p.S0 + (((size_t)r * H + h) * kD + vs) * kD;
+    for (int e = tid; e < kVS * kD / 4; e += kThreads)
+        *reinterpret_cast<float4 *>(&s.S[e * 4]) = *reinterpret_cast<const float4 *>(S0 + (size_t)e * 4);
     int row0;
     const int n = request_rows(p, r, row0);
     if (n <= 0) return;
-    const int H = p.H;
     for (int e = tid; e < n * kD; e += kThreads) {
         const int j = e / kD, c = e % kD;
         s.K[j * kD + c] = bf(p.k[((size_t)(row0 + j) * H + h) * kD + c]);
@@ -376,63 +423,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_gdn_path(const GdnParams p)
         const int j = e / kVS, c = e % kVS;
         s.V[j * kVS + c] = bf(p.v[((size_t)(row0 + j) * H + h) * kD + vs + c]);
     }
-    for (int j = tid; j < n; j += kThreads) {
-        s.alpha[j] = p.alpha[(size_t)(row0 + j) * H + h];
-        s.beta[j] = p.beta[(size_t)(row0 + j) * H + h];
-        const int pr = p.parent[row0 + j];
-        s.par[j] = pr < 0 ? -1 : (pr - row0 < 0 ? -2 : pr - row0);
-    }
-    __syncthreads();
-    const float *S0 = p.S0 + (((size_t)r * H + h) * kD + vs) * kD;
+    tree_info(p, s.t, row0, n, h);
     const int vrow = warp * 4;   // this warp's first row inside the slice
-    const int count = kCommit ? 1 : n;
-    for (int t = 0; t < count; ++t) {
-        const int node = kCommit ? p.acc_node[r] - row0 : t;
-        if (tid == 0) {
-            // root path of `node`, root first; a malformed parent ends it
-            int len = 0, j = node;
-            bool ok = node >= 0 && node < n;
-            while (ok && j >= 0 && len <= kNR) {
-                s.path[len++] = j;
-                const int pj = s.par[j];
-                if (pj >= j || pj < -1) ok = false;
-                j = pj;
-            }
-            if (!ok || len > kNR) {
-                atomicCAS(p.status, 0, (int32_t)W12_E_INVAL);
-                len = 0;
-            }
-            for (int a = 0, b = len - 1; a < b; ++a, --b) {
-                const int x = s.path[a];
-                s.path[a] = s.path[b];
-                s.path[b] = x;
-            }
-            s.path_len = len;
+    float w[4][4];
+    if constexpr (kCommit) {
+        const int node = p.acc_node[r] - row0;
+        unsigned long long path = 0ull;
+        if (node >= 0 && node < n) {
+            path = s.t.anc[node] | (1ull << node);
+        } else if (tid == 0) {
+            atomicCAS(p.status, 0, (int32_t)W12_E_INVAL);
         }
-        __syncthreads();
-        float w[4][4];
-        walk(s, S0, vrow, lane, w);
-        if (kCommit) {
-            float *dst = p.out + (((size_t)r * H + h) * kD + vs) * kD;
+        walk(s, path, vrow, lane, w);
+        __syncthreads();   // every warp has read its rows of S0 before any is overwritten in place
+        float *dst = p.out + (((size_t)r * H + h) * kD + vs) * kD;
 #pragma unroll
-            for (int rr = 0; rr < 4; ++rr)
+        for (int rr = 0; rr < 4; ++rr)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) dst[(size_t)(vrow + rr) * kD + lane + 32 * e] = w[rr][e];
-        } else {
-            float qq[4];
+            for (int e = 0; e < 4; ++e) dst[(size_t)(vrow + rr) * kD + lane + 32 * e] = w[rr][e];
+    } else {
+    for (int node = 0; node < n; ++node) {
+        walk(s, s.t.anc[node] | (1ull << node), vrow, lane, w);
+        float qq[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) qq[e] = bf(p.q[((size_t)(row0 + node) * H + h) * kD + lane + 32 * e]);
+        for (int e = 0; e < 4; ++e) qq[e] = bf(p.q[((size_t)(row0 + node) * H + h) * kD + lane + 32 * e]);
 #pragma unroll
-            for (int rr = 0; rr < 4; ++rr) {
-                float d = w[rr][0] * qq[0];
+        for (int rr = 0; rr < 4; ++rr) {
+            float d = w[rr][0] * qq[0];
 #pragma unroll
-                for (int e = 1; e < 4; ++e) d = fmaf(w[rr][e], qq[e], d);
+            for (int e = 1; e < 4; ++e) d = fmaf(w[rr][e], qq[e], d);
 #pragma unroll
-                for (int o = 16; o; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-                if (lane == 0) p.out[((size_t)(row0 + node) * H + h) * kD + vs + vrow + rr] = d;
-            }
+            for (int o = 16; o; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+            if (lane == 0) p.out[((size_t)(row0 + node) * H + h) * kD + vs + vrow + rr] = d;
         }
-        __syncthreads();
+    }
     }
 }
 
@@ -457,21 +481,25 @@ int launch_gdn(const GdnArgs &a, int mode, void *stream)
     p.acc_node = a.acc_node;
     p.out = a.out;
     p.status = a.status;
-    const dim3 grid(a.n_req, a.H, kD / kVS);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // plain launches: with an early start the next layer's CTAs would share
+    // SMs with this one's and leave others idle (one CTA per SM is the
+    // balanced placement of a 128-CTA layer)
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(a.n_req, a.H, kD / kVS);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = static_cast<cudaStream_t>(stream);
     if (mode == kGdnWy) {
-        const int bytes = (int)sizeof(WyShared);
-        cudaError_t e = cudaFuncSetAttribute(k_gdn_wy, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        cfg.dynamicSmemBytes = sizeof(WyShared);
+        cudaError_t e = cudaFuncSetAttribute(k_gdn_wy, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)cfg.dynamicSmemBytes);
         if (e != cudaSuccess) return (int)e;
-        k_gdn_wy<<<grid, kThreads, bytes, st>>>(p);
-    } else {
-        const int bytes = (int)sizeof(PathShared);
-        const auto kern = mode == kGdnCommit ? k_gdn_path<true> : k_gdn_path<false>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        if (e != cudaSuccess) return (int)e;
-        kern<<<grid, kThreads, bytes, st>>>(p);
+        return (int)cudaLaunchKernelEx(&cfg, k_gdn_wy, p);
     }
-    return (int)cudaGetLastError();
+    cfg.dynamicSmemBytes = sizeof(PathShared);
+    const auto kern = mode == kGdnCommit ? k_gdn_path<true> : k_gdn_path<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes);
+    if (e != cudaSuccess) return (int)e;
+    return (int)cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace w12i

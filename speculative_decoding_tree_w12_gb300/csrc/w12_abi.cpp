@@ -610,7 +610,7 @@ w12_status gdn_args(const w12_gdn_layer *L, const w12_tree *tree, int32_t n_req,
     if (L->n_heads < 1 || n_req < 1 || tree->R < 1) return W12_E_INVAL;
     if (L->head_dim != kGdnDim || L->n_heads > 65535 || n_req > kMaxBudget || tree->R > kMaxBudget)
         return W12_E_UNSUPPORTED;
-    if (!aligned(L->S0, 16) || !aligned(L->q, 4) || !aligned(L->k, 4)) return W12_E_INVAL;
+    if (!aligned(L->S0, 16) || !aligned(L->q, 16) || !aligned(L->k, 16) || !aligned(L->v, 4)) return W12_E_INVAL;
     a = GdnArgs{};
     a.H = L->n_heads;
     a.n_req = n_req;
