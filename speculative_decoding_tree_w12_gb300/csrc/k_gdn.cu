@@ -415,18 +415,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_gdn_path(const GdnParams p)
     int row0;
     const int n = request_rows(p, r, row0);
     if (n <= 0) return;
-    for (int e = tid; e < n * kD; e += kThreads) {
-        const int j = e / kD, c = e % kD;
-        s.K[j * kD + c] = bf(p.k[((size_t)(row0 + j) * H + h) * kD + c]);
-    }
-    for (int e = tid; e < n * kVS; e += kThreads) {
-        const int j = e / kVS, c = e % kVS;
-        s.V[j * kVS + c] = bf(p.v[((size_t)(row0 + j) * H + h) * kD + vs + c]);
-    }
-    tree_info(p, s.t, row0, n, h);
     const int vrow = warp * 4;   // this warp's first row inside the slice
     float w[4][4];
     if constexpr (kCommit) {
+        // the accepted row's path first, then only its rows' keys and values
+        tree_info(p, s.t, row0, n, h);
         const int node = p.acc_node[r] - row0;
         unsigned long long path = 0ull;
         if (node >= 0 && node < n) {
@@ -434,29 +427,47 @@ __global__ void __launch_bounds__(kThreads, 1) k_gdn_path(const GdnParams p)
         } else if (tid == 0) {
             atomicCAS(p.status, 0, (int32_t)W12_E_INVAL);
         }
+        for (int e = tid; e < n * kD; e += kThreads) {
+            const int j = e / kD, c = e % kD;
+            if ((path >> j) & 1ull) s.K[j * kD + c] = bf(p.k[((size_t)(row0 + j) * H + h) * kD + c]);
+        }
+        for (int e = tid; e < n * kVS; e += kThreads) {
+            const int j = e / kVS, c = e % kVS;
+            if ((path >> j) & 1ull) s.V[j * kVS + c] = bf(p.v[((size_t)(row0 + j) * H + h) * kD + vs + c]);
+        }
+        __syncthreads();
+        // every read of S0 happened before tree_info's barriers: writing in place is safe
         walk(s, path, vrow, lane, w);
-        __syncthreads();   // every warp has read its rows of S0 before any is overwritten in place
         float *dst = p.out + (((size_t)r * H + h) * kD + vs) * kD;
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr)
 #pragma unroll
             for (int e = 0; e < 4; ++e) dst[(size_t)(vrow + rr) * kD + lane + 32 * e] = w[rr][e];
     } else {
-    for (int node = 0; node < n; ++node) {
-        walk(s, s.t.anc[node] | (1ull << node), vrow, lane, w);
-        float qq[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) qq[e] = bf(p.q[((size_t)(row0 + node) * H + h) * kD + lane + 32 * e]);
-#pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-            float d = w[rr][0] * qq[0];
-#pragma unroll
-            for (int e = 1; e < 4; ++e) d = fmaf(w[rr][e], qq[e], d);
-#pragma unroll
-            for (int o = 16; o; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-            if (lane == 0) p.out[((size_t)(row0 + node) * H + h) * kD + vs + vrow + rr] = d;
+        for (int e = tid; e < n * kD; e += kThreads) {
+            const int j = e / kD, c = e % kD;
+            s.K[j * kD + c] = bf(p.k[((size_t)(row0 + j) * H + h) * kD + c]);
         }
-    }
+        for (int e = tid; e < n * kVS; e += kThreads) {
+            const int j = e / kVS, c = e % kVS;
+            s.V[j * kVS + c] = bf(p.v[((size_t)(row0 + j) * H + h) * kD + vs + c]);
+        }
+        tree_info(p, s.t, row0, n, h);
+        for (int node = 0; node < n; ++node) {
+            walk(s, s.t.anc[node] | (1ull << node), vrow, lane, w);
+            float qq[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) qq[e] = bf(p.q[((size_t)(row0 + node) * H + h) * kD + lane + 32 * e]);
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+                float d = w[rr][0] * qq[0];
+#pragma unroll
+                for (int e = 1; e < 4; ++e) d = fmaf(w[rr][e], qq[e], d);
+#pragma unroll
+                for (int o = 16; o; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+                if (lane == 0) p.out[((size_t)(row0 + node) * H + h) * kD + vs + vrow + rr] = d;
+            }
+        }
     }
 }
 
