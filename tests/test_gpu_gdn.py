@@ -53,6 +53,9 @@ CASES = [
     ("full_64", dict(n_req=1, positions=(16,), budget=64, n_cand=16), 2),
     ("many_small", dict(n_req=24, positions=(8, 12, 16), budget=192, n_cand=16), 2),
     ("roots_only", dict(n_req=5, positions=(4,), budget=5, n_cand=16), 3),
+    # the shapes the bench times: 32 heads over the single_27b and batched_27b trees
+    ("bench_single", dict(n_req=1, positions=(16,), budget=32, n_cand=16), 32),
+    ("bench_batched", dict(n_req=24, positions=(16, 12, 8), budget=192, n_cand=16), 32),
 ]
 
 

@@ -178,3 +178,22 @@ def test_tlv_refusals_before_launch(L):
     assert L.w12_tlv_splice(C.byref(t), fake, fake, fake, 1, 4, m5.ctypes.data, C.byref(t_big), C.byref(out), ws,
                             1 << 30, None) == w12.W12_E_UNSUPPORTED
     assert L.w12_tree_accept(C.byref(t), 1, 34, fake, fake, fake, None, None) == w12.W12_E_UNSUPPORTED
+
+
+def test_gdn_refusals_before_launch(L):
+    ws = C.c_void_p(0x100000)
+    tr = w12.TreeC(32, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000)
+    good = w12.GdnLayerC(4, 128, 0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000)
+    out = C.c_void_p(0x70000)
+    # head dimension other than 128
+    bad_d = w12.GdnLayerC(4, 64, 0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000)
+    assert L.w12_gdn_tree_verify(C.byref(bad_d), C.byref(tr), 1, 0, out, ws, 1 << 30, None) == w12.W12_E_UNSUPPORTED
+    # null state, misaligned keys, unknown method
+    no_s = w12.GdnLayerC(4, 128, None, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000)
+    assert L.w12_gdn_tree_verify(C.byref(no_s), C.byref(tr), 1, 0, out, ws, 1 << 30, None) == w12.W12_E_INVAL
+    mis = w12.GdnLayerC(4, 128, 0x10000, 0x20000, 0x30008, 0x40000, 0x50000, 0x60000)
+    assert L.w12_gdn_tree_verify(C.byref(mis), C.byref(tr), 1, 0, out, ws, 1 << 30, None) == w12.W12_E_INVAL
+    assert L.w12_gdn_tree_verify(C.byref(good), C.byref(tr), 1, 7, out, ws, 1 << 30, None) == w12.W12_E_INVAL
+    # workspace too small, commit without accepted rows
+    assert L.w12_gdn_tree_verify(C.byref(good), C.byref(tr), 1, 0, out, ws, 16, None) == w12.W12_E_WORKSPACE
+    assert L.w12_gdn_commit(C.byref(good), C.byref(tr), 1, None, out, ws, 1 << 30, None) == w12.W12_E_INVAL
