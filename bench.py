@@ -747,6 +747,9 @@ def main():
     ap.add_argument("--rows-sweep", default=None,
                     help="comma-separated node budgets timed after the headline (default: 1,8,32,64 for "
                          "single-request workloads, none otherwise; 'none' to skip)")
+    ap.add_argument("--extras", default="all", choices=["all", "none"],
+                    help="the measurements after the headline and its end-to-end pass (quick pass, certified "
+                         "head, TLV cycle, recurrent-layer stack): all, or none for a launch list of the step alone")
     ap.add_argument("--gemm", default="auto", choices=["auto", "tcgen05", "warp_mma"],
                     help="GEMM kernel: the library's choice by row count, or one forced")
     args = ap.parse_args()
@@ -881,28 +884,32 @@ def main():
     # ------------------------------------------------------- quick pass
     quick = None
     try:
-        quick = quick_pass(wk, K, W)
+        if args.extras == "all":
+            quick = quick_pass(wk, K, W)
     except Exception as ex:  # reported, never hidden
         quick = {"error": str(ex)[:200]}
 
     # ------------------------------------------------- certified head
     cert = None
     try:
-        cert = certified_head(wk, K, W)
+        if args.extras == "all":
+            cert = certified_head(wk, K, W)
     except Exception as ex:  # reported, never hidden
         cert = {"error": str(ex)[:200]}
 
     # ------------------------------------------------------------ TLV cycle
     tlv = None
     try:
-        tlv = tlv_cycle(wk, max(10, min(K, 50)), W)
+        if args.extras == "all":
+            tlv = tlv_cycle(wk, max(10, min(K, 50)), W)
     except Exception as ex:  # reported, never hidden
         tlv = {"error": str(ex)[:200]}
 
     # ------------------------------------------- recurrent-layer verification
     gdn = None
     try:
-        gdn = gdn_stack(wk, max(10, min(K, 50)), W)
+        if args.extras == "all":
+            gdn = gdn_stack(wk, max(10, min(K, 50)), W)
     except Exception as ex:  # reported, never hidden
         gdn = {"error": str(ex)[:200]}
 
