@@ -9,6 +9,12 @@
  *   rows    --w12_lmhead_argmax--> target argmax per row
  *   tree + argmax --w12_tree_accept--> accepted tokens + lengths
  *
+ * Around it: the quick pass on the 8-bit view planes (w12_gemm_q,
+ * w12_lmhead_argmax_q, w12_verify_step_q), the certified LM head
+ * (w12_head_cert_norms, w12_lmhead_argmax_certified), the TLV splice of two
+ * trees (w12_tlv_chain, w12_tlv_splice) and a recurrent (Gated DeltaNet)
+ * layer over a tree (w12_gdn_tree_verify, w12_gdn_commit).
+ *
  * Sources (SpecPilot explainer at jaehun.me, "SpecPilot: Autonomous Algorithm
  * Discovery and Systems Optimization for Speculative Decoding"; the summary
  * page at agihunt.info; the poot-llm speculative-decoding docs):
@@ -16,6 +22,8 @@
  *   - verify rows / greedy acceptance: explainer 1.1; poot-llm "What a round
  *     guarantees".
  *   - best-first tree / shared budget: explainer 4.2 and 4.4.
+ *   - quick pass, certified head, TLV: explainer 4.1 and 4.3.
+ *   - recurrent layers over a tree (path walk, WY form): explainer 4.2.
  *   - typed refusal before anything runs: poot-llm "What is refused".
  *
  * Conventions for every entry point:
