@@ -197,3 +197,24 @@ def test_gdn_refusals_before_launch(L):
     # workspace too small, commit without accepted rows
     assert L.w12_gdn_tree_verify(C.byref(good), C.byref(tr), 1, 0, out, ws, 16, None) == w12.W12_E_WORKSPACE
     assert L.w12_gdn_commit(C.byref(good), C.byref(tr), 1, None, out, ws, 1 << 30, None) == w12.W12_E_INVAL
+
+
+def test_binding_signatures_match_the_header(L):
+    """Every declared entry point that the binding marshals has as many
+    arguments there as in its C declaration."""
+    import ctypes
+    src = ""
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src += re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+    decl = {}
+    for m in re.finditer(r"\b(w12_\w+)\s*\(([^;{]*?)\)\s*;", src, flags=re.S):
+        args = m.group(2).strip()
+        decl[m.group(1)] = 0 if args in ("", "void") else args.count(",") + 1
+    checked = 0
+    for name, n in decl.items():
+        f = getattr(L, name)
+        if getattr(f, "argtypes", None) is None:
+            continue
+        assert len(f.argtypes) == n, (name, len(f.argtypes), n)
+        checked += 1
+    assert checked >= 25
