@@ -24,6 +24,15 @@ def w12():
     return m
 
 
+@pytest.fixture(params=["warp_mma", "tcgen05"])
+def path(request, w12):
+    """Run the test on one GEMM kernel: the warp-MMA kernel (flag 4) or the
+    tensor-memory kernel (flag 2)."""
+    w12.debug_set(4 if request.param == "warp_mma" else 2, 0)
+    yield request.param
+    w12.debug_set(0, 0)
+
+
 def _dev_bf16(bits: np.ndarray):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
 
@@ -133,7 +142,7 @@ def test_tlv_splice_flags_a_chain_that_is_not_the_tree_path(w12):
 
 
 @pytest.mark.parametrize("n_req,positions,budget,p2", [(1, (16,), 32, 16), (4, (4, 8), 48, 8)])
-def test_tlv_cycle_with_w12_gemms(w12, n_req, positions, budget, p2):
+def test_tlv_cycle_with_w12_gemms(w12, path, n_req, positions, budget, p2):
     """A whole cycle: Q pass (quick weights) over the first tree, chain,
     subtree, splice, exact pass over the combined tree; every stage against
     the oracle on margin-passing rows, and the accepted tokens against
