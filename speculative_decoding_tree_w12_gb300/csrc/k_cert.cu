@@ -15,10 +15,10 @@
 //                   L = max(s^ - eps) and the survivors s^ + eps >= L (FP32
 //                   with directed rounding; an unordered list with room for
 //                   the whole vocabulary)
-//   k_cert_rescore  64 CTAs per row: exact FP64 logits of the survivors from
-//                   the W12 records (exact decode, escapes patched), each
-//                   CTA's best; k_cert_final: the row's argmax (lowest index
-//                   on ties)
+//   k_cert_rescore  64 CTAs per row, one survivor at a time per CTA: exact
+//                   FP64 logits from the W12 records (exact decode, escapes
+//                   patched), each CTA's best; k_cert_final: one warp per
+//                   row, the row's argmax (lowest index on ties)
 #include <cuda_runtime.h>
 
 #include <cfloat>
@@ -172,6 +172,15 @@ __global__ void __launch_bounds__(256) k_cert_surv(const uint16_t *__restrict__ 
 
 // grid (R, parts): CTA (r, b) rescores survivors b*8 + warp, b*8 + warp + 8*parts, ...
 // of row r and writes its best (logit, token) to part_v/part_i[r][b]
+// better (logit, token): larger logit, then the lower token id
+__device__ __forceinline__ bool better(double v, int32_t i, double bv, int32_t bi)
+{
+    return v > bv || (v == bv && i < bi);
+}
+
+// grid (R, parts): CTA (r, b) rescores survivors b, b + parts, ... of row r,
+// each with all 256 threads (one 16-K group of the channel per thread and
+// step), and writes its best (logit, token) to part_v/part_i[r][b]
 __global__ void __launch_bounds__(256) k_cert_rescore(const uint8_t *__restrict__ rec, const uint8_t *__restrict__ base,
                                                       const int32_t *__restrict__ esc_off,
                                                       const uint32_t *__restrict__ esc, int32_t k_tiles, int64_t K,
@@ -179,20 +188,19 @@ __global__ void __launch_bounds__(256) k_cert_rescore(const uint8_t *__restrict_
                                                       const int32_t *__restrict__ cnt, int64_t cap, double *part_v,
                                                       int32_t *part_i)
 {
-    __shared__ double best_s[8];
-    __shared__ int32_t besti_s[8];
+    __shared__ double red[8];
     const int r = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int parts = gridDim.y, b = blockIdx.y;
     const int64_t n = min((int64_t)cnt[r], cap);
     const uint16_t *hr = h + r * K;
     double bv = -DBL_MAX;
     int32_t bi = INT_MAX;
-    for (int64_t i = (int64_t)b * 8 + warp; i < n; i += 8 * (int64_t)parts) {
+    for (int64_t i = b; i < n; i += parts) {   // uniform over the CTA
         const int32_t v = surv[(int64_t)r * cap + i];
         const int nt = v >> 7, c = v & 127;
         const ChanConst cc = chan_const(__ldg(base + v));
         double acc = 0.0;
-        for (int j = lane; j < 4 * k_tiles; j += 32) {
+        for (int j = threadIdx.x; j < 4 * k_tiles; j += 256) {
             const int kt = j >> 2, kg = j & 3;
             const int64_t t = (int64_t)nt * k_tiles + kt;
             float w[16];
@@ -203,34 +211,47 @@ __global__ void __launch_bounds__(256) k_cert_rescore(const uint8_t *__restrict_
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (acc > bv || (acc == bv && v < bi)) bv = acc, bi = v;
+        if (lane == 0) red[warp] = acc;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            double tot = red[0];
+            for (int w = 1; w < 8; ++w) tot += red[w];
+            if (better(tot, v, bv, bi)) bv = tot, bi = v;
+        }
+        __syncthreads();
     }
-    if (lane == 0) best_s[warp] = bv, besti_s[warp] = bi;
-    __syncthreads();
     if (threadIdx.x == 0) {
-        for (int w = 1; w < 8; ++w)
-            if (best_s[w] > bv || (best_s[w] == bv && besti_s[w] < bi)) bv = best_s[w], bi = besti_s[w];
         part_v[(int64_t)r * parts + b] = bv;
         part_i[(int64_t)r * parts + b] = bi;
     }
 }
 
-// per row: the best of the parts (lowest token on ties)
-__global__ void k_cert_final(const double *part_v, const int32_t *part_i, int32_t R, int32_t parts, int32_t *argmax,
-                             float *maxlogit, const int32_t *cnt, int32_t *cnt_out)
+// one warp per row: the best of the row's parts (lowest token id on ties)
+__global__ void __launch_bounds__(128) k_cert_final(const double *part_v, const int32_t *part_i, int32_t R,
+                                                    int32_t parts, int32_t *argmax, float *maxlogit,
+                                                    const int32_t *cnt, int32_t *cnt_out)
 {
-    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (r >= R) return;
-    if (cnt_out) cnt_out[r] = cnt[r];
     double bv = -DBL_MAX;
     int32_t bi = INT_MAX;
-    for (int b = 0; b < parts; ++b) {
+    for (int b = lane; b < parts; b += 32) {
         const double v = part_v[(int64_t)r * parts + b];
         const int32_t i = part_i[(int64_t)r * parts + b];
-        if (v > bv || (v == bv && i < bi)) bv = v, bi = i;
+        if (better(v, i, bv, bi)) bv = v, bi = i;
     }
-    argmax[r] = (bi == INT_MAX) ? 0 : bi;
-    if (maxlogit) maxlogit[r] = (float)bv;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const double ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int32_t oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (better(ov, oi, bv, bi)) bv = ov, bi = oi;
+    }
+    if (lane == 0) {
+        if (cnt_out) cnt_out[r] = cnt[r];
+        argmax[r] = (bi == INT_MAX) ? 0 : bi;
+        if (maxlogit) maxlogit[r] = (float)bv;
+    }
 }
 
 }  // namespace
@@ -268,7 +289,7 @@ int launch_cert_rescore(const DevWeight &w, const uint16_t *h, int32_t R, const 
     k_cert_rescore<<<dim3(R, kCertParts), 256, 0, st>>>(w.rec, w.base, w.esc_off, w.esc, w.k_tiles, w.k, h, surv, cnt,
                                                         w.n, part_v, part_i);
     if (cudaError_t e = cudaGetLastError()) return (int)e;
-    k_cert_final<<<(R + 127) / 128, 128, 0, st>>>(part_v, part_i, R, kCertParts, argmax, maxlogit, cnt, cnt_out);
+    k_cert_final<<<(R + 3) / 4, 128, 0, st>>>(part_v, part_i, R, kCertParts, argmax, maxlogit, cnt, cnt_out);
     return (int)cudaGetLastError();
 }
 
