@@ -20,8 +20,7 @@
 //    three BF16 pieces that add up to the FP32 value exactly, each piece is
 //    multiplied by the BF16 keys/queries (exact products) with FP32
 //    accumulation.  k.k and k.q are BF16 products too.  The triangular solve
-//    (by depth level, each warp on its own 4 columns) and the output sums run
-//    on the FP32 pipes.
+//    (by depth level) and the output sums run on the FP32 pipes.
 //
 // The committed-state update after acceptance (k_gdn_commit) replays the
 // accepted path, like the path kernel, and writes the state.
@@ -327,14 +326,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_gdn_wy(const GdnParams p)
         }
     }
     __syncthreads();
-    // forward substitution by depth level: U[j] = B[j] - b_j g_j sum_anc (k_i.k_j / g_i) U[i].
-    // A column only reads its own column of U, so each warp owns 4 columns
-    // (8 row slots x 4 columns) and the levels need only warp barriers.
-    const int c = warp * 4 + (lane & 3), slot = lane >> 2;
+    // forward substitution by depth level: U[j] = B[j] - b_j g_j sum_anc (k_i.k_j / g_i) U[i]
+    const int c = tid & 31, slot = tid >> 5;
     const int n_lvl = s.maxd + 1;
     for (int L = 0; L < n_lvl; ++L) {
         const int lo = s.lvl_off[L], hi = s.lvl_off[L + 1];
-        for (int t = lo + slot; t < hi; t += 8) {
+        for (int t = lo + slot; t < hi; t += kThreads / 32) {
             const int j = s.order[t];
             float sum = 0.f;
             unsigned long long m = s.t.anc[j];
@@ -347,10 +344,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gdn_wy(const GdnParams p)
             const float B = bj * (Vf[j * kPS + c] - gj * s.P[j * kPS + c]);
             s.U[j * kPS + c] = B - bj * gj * sum;
         }
-        __syncwarp();
+        __syncthreads();
     }
-    // outputs: o_j = g_j (S0 q_j + sum over the path (k_i.q_j / g_i) u_i), same columns
-    for (int j = slot; j < n; j += 8) {
+    // outputs: o_j = g_j (S0 q_j + sum over the path (k_i.q_j / g_i) u_i)
+    for (int j = slot; j < n; j += kThreads / 32) {
         float sum = s.Rq[j * kPS + c];
         unsigned long long m = s.t.anc[j] | (1ull << j);
         while (m) {
