@@ -218,3 +218,17 @@ def test_binding_signatures_match_the_header(L):
         assert len(f.argtypes) == n, (name, len(f.argtypes), n)
         checked += 1
     assert checked >= 25
+
+
+def test_tlv_chain_edge_cases(L):
+    # 512 requests holding one row each: nothing can be committed, every row is a subtree root
+    n = 512
+    off = np.arange(n + 1, dtype=np.int32)
+    m, sub = w12.w12_tlv_chain(np.ones(n, np.int32), off, 512)
+    assert not m.any() and sub == 512
+    # one request whose whole share (a 32-row chain) was accepted: the bonus is dropped
+    m, sub = w12.w12_tlv_chain(np.asarray([32], np.int32), np.asarray([0, 32], np.int32), 32)
+    assert list(m) == [31] and sub == 1
+    # the first tree held fewer rows than the budget (lattice exhausted): the rest goes to the subtrees
+    m, sub = w12.w12_tlv_chain(np.asarray([2, 1], np.int32), np.asarray([0, 3, 5], np.int32), 40)
+    assert list(m) == [2, 1] and sub == 37
