@@ -752,6 +752,9 @@ def main():
                          "head, TLV cycle, recurrent-layer stack): all, or none for a launch list of the step alone")
     ap.add_argument("--gemm", default="auto", choices=["auto", "tcgen05", "warp_mma"],
                     help="GEMM kernel: the library's choice by row count, or one forced")
+    ap.add_argument("--chain", default="auto", choices=["auto", "on", "off"],
+                    help="verify step as one persistent GEMM-chain launch (on), one launch per GEMM (off), "
+                         "or the library's choice")
     args = ap.parse_args()
     if args.warmup < 3:
         log("[bench] warmup raised to 3")
@@ -773,7 +776,7 @@ def main():
     if dist:
         dist.barrier()
     import speculative_decoding_tree_w12_gb300 as w12
-    w12.debug_set({"auto": 0, "tcgen05": 2, "warp_mma": 4}[args.gemm], 0)
+    w12.debug_set({"auto": 0, "tcgen05": 2, "warp_mma": 4}[args.gemm] | {"auto": 0, "on": 16, "off": 8}[args.chain], 0)
 
     wk = Workload(args.workload, args.rows, device)
     W, K = args.warmup, args.steps
@@ -851,11 +854,15 @@ def main():
     w12.profile(False)
     per_launch = per_launch / K
     n_gemm = len(per_launch) - 2                     # then the argmax reduction and acceptance
-    per_weight = n_gemm // (len(wk.lin) + 1)
+    n_weights = len(wk.lin) + 1
+    chain = n_gemm < n_weights                       # the whole GEMM chain in one or two launches
+    per_weight = 1 if chain else n_gemm // n_weights
     lb = wk.launch_bytes(per_weight)
     gemm_ms = per_launch[:n_gemm]
     gemm_bytes = float(sum(lb))
     achieved = gemm_bytes / (float(gemm_ms.sum()) * 1e-3) / 1e9
+    if chain:
+        lb = [gemm_bytes]
     peak, peak_kind = load_peaks()
     traffic = committed_traffic(args.workload)
     kernels = {
@@ -951,7 +958,7 @@ def main():
             "cublas_bf16": cublas,
             "cpu_baseline": cpu,
             "clocks": clocks,
-            "gpu_launches": K * wk.gpu_launches_per_step(per_weight),
+            "gpu_launches": K * (3 + n_gemm if chain else wk.gpu_launches_per_step(per_weight)),
             "rows_sweep": sweep,
             "quick_pass": quick,
             "certified_head": cert,

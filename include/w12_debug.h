@@ -23,6 +23,12 @@ extern "C" {
  *   flags bit 1: run every GEMM on the tensor-memory (tcgen05) kernel.
  *   flags bit 2: run every GEMM on the warp-MMA kernel (64 rows per pass).
  *                Without either bit the library picks by row count.
+ *   flags bit 3: w12_verify_step launches one kernel per GEMM (the default).
+ *   flags bit 4: w12_verify_step runs all its GEMMs (every linear, then the
+ *                LM head) as one persistent tensor-memory GEMM chain: one
+ *                launch per up to 144 GEMMs, each GEMM's activations read
+ *                once every CTA has finished the previous GEMM.  Bits 2 and
+ *                3 take precedence.
  *   timeout_ns:  limit of every bounded wait inside the kernels
  *                (0 restores the default of 2 seconds).
  * Not thread-safe; meant to be set between launches by a test.
@@ -50,6 +56,19 @@ int32_t w12_debug_last_cuda_error(char *buf, int32_t len);
 
 /* Number of SMs the kernels size their persistent grids for (current device). */
 int32_t w12_debug_num_sms(void);
+
+/*
+ * Per-GEMM timing inside the verify step's GEMM chain (one persistent launch
+ * for all linears and the LM head, split into w12_debug_chain_parts(n) launches
+ * for n GEMMs).  While dev_words (device, n_words 64-bit words) is set, every
+ * CTA of a chain launch covering GEMMs [j0, j0 + m) writes the global timer
+ * (ns) when it starts, at word ((j0 + part) + m) * S + cta, and when it has
+ * written its last output of GEMM j, at word (j + part) * S + cta, with S the
+ * SM count and part the launch's index.  GEMM j ends when the last CTA
+ * stamps it.  Too small a buffer disables the stamps.  NULL turns it off.
+ */
+void w12_debug_chain_trace(void *dev_words, size_t n_words);
+int32_t w12_debug_chain_parts(int32_t n_gemms);
 
 #ifdef __cplusplus
 }

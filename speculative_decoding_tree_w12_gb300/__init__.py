@@ -112,6 +112,8 @@ def lib():
             "w12_debug_profile": ([i32], None),
             "w12_debug_last_cuda_error": ([p, i32], i32),
             "w12_debug_profile_read": ([p, i32], i32),
+            "w12_debug_chain_trace": ([p, sz], None),
+            "w12_debug_chain_parts": ([i32], i32),
         }
         for name, (args, res) in sigs.items():
             f = getattr(L, name)
@@ -488,3 +490,41 @@ def profile_read(max_launches: int = 1024) -> List[float]:
 
 def num_sms() -> int:
     return int(lib().w12_debug_num_sms())
+
+
+class ChainTrace:
+    """Per-GEMM end times inside the verify step's GEMM chain (debug hook):
+    while enabled, each chain launch stamps the global timer per CTA at its
+    start and when the CTA has written its last output of each GEMM."""
+
+    def __init__(self, n_gemms: int, device="cuda"):
+        import torch
+        self.n = int(n_gemms)
+        self.parts = int(lib().w12_debug_chain_parts(self.n))
+        self.S = num_sms()
+        self.buf = torch.zeros(((self.n + self.parts) * self.S,), dtype=torch.int64, device=device)
+
+    def __enter__(self):
+        lib().w12_debug_chain_trace(C.c_void_p(self.buf.data_ptr()), self.buf.numel())
+        return self
+
+    def __exit__(self, *exc):
+        lib().w12_debug_chain_trace(None, 0)
+
+    def gemm_us(self) -> List[float]:
+        """Per GEMM: the time from the previous GEMM's end (for each launch's
+        first GEMM, from the launch's first CTA start) to the last CTA's stamp."""
+        t = self.buf.view(self.n + self.parts, self.S).cpu().numpy().astype(np.float64)
+        out, j0 = [], 0
+        for k in range(self.parts):
+            m = (self.n - j0) // (self.parts - k)
+            rows = t[j0 + k: j0 + k + m]
+            start = t[j0 + k + m]
+            starts = start[start > 0]
+            prev = starts.min() if starts.size else rows[0].max()
+            for r in rows:
+                end = r.max()
+                out.append((end - prev) / 1e3)
+                prev = end
+            j0 += m
+        return out

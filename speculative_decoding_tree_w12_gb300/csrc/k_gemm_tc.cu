@@ -719,7 +719,14 @@ bool tc_buffer_plan(int nr, int max_recs, int esc_cap, int base_tiles, int budge
         if (g * na * kACols + db * nr > (int)kTmemCols) continue;
         // the most record-pair slots, then an activation ring up to two pairs deeper
         int st = 0, sx = 0;
-        for (int s = 8; s >= 2 && st == 0; --s)
+        // Group g takes records g, g + G, ...; pair slot P % S last held pair
+        // P - S.  With 4 groups a group reads every other pair, with 3 groups
+        // two pairs in three, so an even S (4 groups) or a multiple of 3 (3
+        // groups) makes pair P - S one the group itself has already consumed:
+        // a group waiting on a slot is then never two fills ahead of it, where
+        // a parity wait would report the fill from two rounds back as done.
+        const int s_step = g == 4 ? 2 : g == 3 ? 3 : 1;
+        for (int s = 8 / s_step * s_step; s >= 2 && st == 0; s -= s_step)
             for (int x = s + 2; x >= s; --x)
                 if (plan(s, g * na, x, nr, max_recs, esc_cap, base_tiles).total <= budget) {
                     st = s, sx = x;

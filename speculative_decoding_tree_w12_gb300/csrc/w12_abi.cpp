@@ -9,6 +9,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <vector>
 
 #include "w12.h"
 #include "w12_debug.h"
@@ -63,6 +64,24 @@ bool use_tc(int32_t R, int64_t records)
     if (R <= 16) return false;
     const int64_t per_sm = records / num_sms();
     return R <= 32 ? per_sm >= 100 : per_sm >= 50;
+}
+
+// GEMM-chain timing hook (w12_debug_chain_trace)
+uint64_t *g_trace = nullptr;
+size_t g_trace_words = 0;
+
+int chain_parts(int n_jobs) { return (n_jobs + chain_max_jobs() - 1) / chain_max_jobs(); }
+
+// The verify step runs its GEMMs as one persistent chain (k_chain.cu) when
+// debug flag bit 4 asks for it, unless bit 2 (warp-MMA kernel) or bit 3 (one
+// launch per GEMM) is set or the step has more GEMMs than the workspace has
+// chain words for.  Measured on GB300, one launch per GEMM with the per-row-count
+// kernel choice is faster on the 27B-like shapes, so it is the default.
+bool use_chain(int n_jobs)
+{
+    if (g_debug_flags & (4 | 8)) return false;
+    if (!(g_debug_flags & 16)) return false;
+    return n_jobs + 1 <= kGridWords;
 }
 
 int num_sms()
@@ -137,6 +156,21 @@ struct Ws {
     {
         return (int)cudaMemsetAsync(base + L.counters, 0, static_cast<size_t>(kGemmSlots) * L.max_tiles_n * 4, st);
     }
+    // the same, plus the GEMM-chain words of n_jobs GEMMs (the region sits just
+    // before the counters, so one memset clears both)
+    int clear_chain(int n_jobs, cudaStream_t st) const
+    {
+        const size_t lead = static_cast<size_t>(1 + n_jobs) * 4;
+        return (int)cudaMemsetAsync(base + L.counters - lead, 0,
+                                    lead + static_cast<size_t>(kGemmSlots) * L.max_tiles_n * 4, st);
+    }
+    // a chain of n_jobs GEMMs uses the last 1 + n_jobs words of the region:
+    // its abort word, then one arrival word per GEMM
+    int32_t *grid_abort(int n_jobs) const
+    {
+        return reinterpret_cast<int32_t *>(base + L.counters - static_cast<size_t>(1 + n_jobs) * 4);
+    }
+    uint32_t *grid_bar(int n_jobs) const { return reinterpret_cast<uint32_t *>(grid_abort(n_jobs) + 1); }
     float *s1_val() const { return reinterpret_cast<float *>(base + L.stage1_val); }
     int32_t *s1_idx() const { return reinterpret_cast<int32_t *>(base + L.stage1_idx); }
     void *tree() const { return base + L.tree; }
@@ -155,6 +189,9 @@ WsLayout layout_for(int32_t R, int64_t max_n, int64_t vocab, int32_t n_req)
     size_t o = 0;
     L.status = o;
     o += 256;
+    // the chain words end exactly where the counters start
+    L.grid = o;
+    o += static_cast<size_t>(kGridWords) * 4;
     L.counters = o;
     o = align256(o + static_cast<size_t>(kGemmSlots) * L.max_tiles_n * 4);
     L.partial = o;
@@ -247,6 +284,14 @@ void w12_debug_set(int32_t flags, uint64_t timeout_ns)
 }
 
 int32_t w12_debug_num_sms(void) { return num_sms(); }
+
+void w12_debug_chain_trace(void *dev_words, size_t n_words)
+{
+    g_trace = static_cast<uint64_t *>(dev_words);
+    g_trace_words = dev_words ? n_words : 0;
+}
+
+int32_t w12_debug_chain_parts(int32_t n_gemms) { return n_gemms > 0 ? chain_parts(n_gemms) : 0; }
 
 int32_t w12_debug_last_cuda_error(char *buf, int32_t len)
 {
@@ -562,16 +607,47 @@ w12_status verify_step_entry(const w12_step *step, const w12_tree *tree, int32_t
     if ((s = ws_check(ws, ws_bytes, L)) != W12_OK) return s;
     Ws W{static_cast<uint8_t *>(ws), L};
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (int ce = W.clear_counters(st)) return cuda_status(ce);
-    g_prof_used = 0;
-    if (prof_mark(st)) return W12_E_CUDA;
-    int slot = 0;
-    for (int32_t l = 0; l < step->n_linear; ++l)
-        if (int e = gemm_slices(dev_weight(&step->lin[l]), step->x[l], R, kModeLinear, step->y[l], W, slot, true, st,
-                                qview))
-            return cuda_status(e);
     const DevWeight hw = dev_weight(step->head);
-    if (int e = gemm_slices(hw, step->h, R, kModeHead, nullptr, W, slot, true, st, qview)) return cuda_status(e);
+    const int n_jobs = step->n_linear + 1;
+    if (use_chain(n_jobs)) {
+        // every GEMM of the step in one persistent launch (two or more for
+        // steps beyond one launch's parameter block)
+        if (int ce = W.clear_chain(n_jobs, st)) return cuda_status(ce);
+        g_prof_used = 0;
+        if (prof_mark(st)) return W12_E_CUDA;
+        std::vector<ChainJob> jobs(static_cast<size_t>(n_jobs));
+        for (int32_t l = 0; l < step->n_linear; ++l)
+            jobs[l] = ChainJob{dev_weight(&step->lin[l]), step->x[l], kModeLinear, step->y[l], nullptr, nullptr};
+        jobs[step->n_linear] = ChainJob{hw, step->h, kModeHead, nullptr, W.s1_val(), W.s1_idx()};
+        ChainArgs ca{};
+        ca.jobs = jobs.data();
+        ca.n_jobs = n_jobs;
+        ca.R = R;
+        ca.partial = W.partial(0);
+        ca.counters = W.counters(0);
+        ca.status = W.status();
+        ca.grid_bar = W.grid_bar(n_jobs);
+        ca.grid_abort = W.grid_abort(n_jobs);
+        ca.num_sms = num_sms();
+        ca.pdl = true;
+        ca.qview = qview;
+        ca.debug_flags = g_debug_flags;
+        ca.timeout_ns = g_timeout_ns;
+        if (g_trace && g_trace_words >= (size_t)(n_jobs + chain_parts(n_jobs)) * (size_t)ca.num_sms)
+            ca.trace = g_trace;
+        if (int e = launch_chain(ca, st)) return cuda_status(e);
+        if (int pe = prof_mark(st)) return cuda_status(pe);
+    } else {
+        if (int ce = W.clear_counters(st)) return cuda_status(ce);
+        g_prof_used = 0;
+        if (prof_mark(st)) return W12_E_CUDA;
+        int slot = 0;
+        for (int32_t l = 0; l < step->n_linear; ++l)
+            if (int e = gemm_slices(dev_weight(&step->lin[l]), step->x[l], R, kModeLinear, step->y[l], W, slot, true,
+                                    st, qview))
+                return cuda_status(e);
+        if (int e = gemm_slices(hw, step->h, R, kModeHead, nullptr, W, slot, true, st, qview)) return cuda_status(e);
+    }
     if (int e = launch_argmax_stage2(W.s1_val(), W.s1_idx(), R, hw.n_tiles, step->argmax, nullptr, true, st))
         return cuda_status(e);
     if (prof_mark(st)) return W12_E_CUDA;

@@ -18,6 +18,7 @@ constexpr int kMaxPositions = 16;
 constexpr int kMaxDepth = 2 * kMaxPositions + 1;   // deepest row of a spliced tree
 constexpr int kCands = 16;
 constexpr int kGemmSlots = 2;        // consecutive GEMMs alternate workspace slots
+constexpr int kGridWords = 4096;     // GEMM-chain words: an abort word + one per GEMM of a step
 
 // Device status word values (first condition wins).
 constexpr int32_t kDevOk = 0;
@@ -25,6 +26,7 @@ constexpr int32_t kDevOk = 0;
 // Byte layout of the caller's workspace.  Every region is 256-byte aligned.
 struct WsLayout {
     size_t status;        // int32[64]: [0] status, [1] detail, [8] mismatch count (int64)
+    size_t grid;          // uint32[kGridWords]: [0] abort word of a GEMM chain, [1 + j] CTAs done with GEMM j
     size_t counters;      // int32[kGemmSlots][max_tiles_n]: split-tile arrival counters
     size_t partial;       // float[kGemmSlots][max_ctas][2][rows8][128]
     size_t stage1_val;    // float[rows][vocab_tiles]
@@ -73,6 +75,38 @@ struct GemmArgs {
     int32_t debug_flags;
     uint64_t timeout_ns;
 };
+
+// The verify pass's GEMM chain in one persistent launch per up to
+// chain_max_jobs() GEMMs (k_chain.cu): GEMM j + 1 reads its activations only
+// after every CTA has counted itself in grid_bar[j].
+struct ChainJob {
+    DevWeight w;
+    const uint16_t *x;       // [R][k] row-major BF16
+    int32_t mode;
+    uint16_t *y;             // linear: [R][n]
+    float *s1_val;           // head: [R][n_tiles]
+    int32_t *s1_idx;
+};
+
+struct ChainArgs {
+    const ChainJob *jobs;
+    int32_t n_jobs;
+    int32_t R;
+    float *partial;          // one partial slot (ws.partial(0))
+    int32_t *counters;       // one counter slot, zero on entry
+    int32_t *status;
+    uint32_t *grid_bar;      // [n_jobs], zero on entry (may be null for one GEMM)
+    int32_t *grid_abort;     // zero on entry
+    uint64_t *trace;         // optional timing stamps (w12_debug_chain_trace)
+    int num_sms;
+    bool pdl;
+    bool qview;
+    int32_t debug_flags;
+    uint64_t timeout_ns;
+};
+
+int launch_chain(const ChainArgs &a, void *stream);
+int chain_max_jobs();
 
 int launch_gemm(const GemmArgs &a, void *stream);      // warp-MMA path, R <= 64 per launch
 int launch_gemm_tc(const GemmArgs &a, void *stream);   // tensor-memory path, R <= 256
