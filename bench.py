@@ -8,9 +8,13 @@ metric is the effective W12 weight-stream bandwidth of the step (W12 bytes
 read per step / step time, GB/s), reported with the step time in
 microseconds and as a fraction of the HBM roofline.
 
-Default workload: one 27B-like decoder layer (QKV 5120->7168, O 5120->5120,
-gate/up 5120->34816, down 17408->5120) + LM head 5120x151936 in W12
-(1.66 GB), one request, a 32-row tree from a top-16 x 16-position lattice.
+Default workload: 64 stacked 27B-like decoder layers (QKV 5120->7168, O
+5120->5120, gate/up 5120->34816, down 17408->5120; 4 distinct weight sets,
+each layer streaming its own copy) + LM head 5120x151936 in W12 (32.9 GB
+resident), one request, a 32-row tree from a top-16 x 16-position lattice.
+After the headline, the same step is timed at 1, 8, 32, 64, 128 and 192
+rows (one request) and at 192 rows from 24 requests, each next to dense BF16
+cuBLAS on the same shapes.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--rows R] [--impl reference]
@@ -48,7 +52,9 @@ DESCRIPTIONS = {
     "b4_tree": "4B-like layer (2560->3584, 2560->2560, 2560->19456, 9728->2560) + head 2560x151936; "
                "32 requests, 256-node budget, trees",
     "b4_chain": "4B-like layer + head; 32 requests, 256-node budget, chains",
-    "full_depth_27b": "64 stacked 27B-like layers + LM head (32.9 GB W12 resident)",
+    "full_depth_27b": "64 stacked 27B-like layers (QKV 5120->7168, O 5120->5120, gate/up 5120->34816, "
+                      "down 17408->5120) + LM head 5120x151936, W12 (32.9 GB resident); 1 request, "
+                      "32-node tree from top-16 x 16 positions",
 }
 
 
@@ -108,16 +114,20 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def committed_traffic(workload):
-    """DRAM bytes per GEMM launch from a committed ncu summary, if it was taken
-    on the current kernel source."""
+def committed_traffic(gemms):
+    """DRAM bytes (read + written) of a step's GEMM launches from a committed
+    ncu capture, if it was taken on the current kernel source: `gemms` lists
+    the step's launches as (n, k, rows); every one must have a captured
+    launch of the same shape and rows (stacked layers reuse one layer's
+    capture: same kernel, shape and rows, so the same traffic)."""
     p = os.path.join(ROOT, "profiles", "w12_gemm_traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
         if d.get("kernel_source_hash") != kernel_source_hash():
             return None
-        return d.get("per_step_bytes", {}).get(workload)
+        per = {(l["n"], l["k"], l["rows"]): l["dram_read_bytes"] + l["dram_write_bytes"] for l in d["launches"]}
+        return int(sum(per[g] for g in gemms))
     except Exception:
         return None
 
@@ -181,11 +191,12 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 class Workload:
-    def __init__(self, name, rows, device, seed=0, share=None, one_request=False):
+    def __init__(self, name, rows, device, seed=0, share=None, one_request=False, variant=None):
         """`share`: another Workload of the same name whose packed device
         weights are reused (only the tree, its rows and the activations are
         rebuilt for the new node budget).  `one_request`: a single request
-        drafting 16 positions (the rows of one best-first tree)."""
+        drafting 16 positions (the rows of one best-first tree).  `variant`:
+        other request/lattice fields of the workload replaced."""
         import torch
         import speculative_decoding_tree_w12_gb300 as w12
         from speculative_decoding_tree_w12_gb300 import synth
@@ -194,6 +205,8 @@ class Workload:
         w = synth.WORKLOADS[name]
         if one_request:
             w = synth.scaled(w, n_req=1, positions=(16,))
+        if variant:
+            w = synth.scaled(w, **variant)
         if rows:
             w = synth.scaled(w, budget=int(rows))
         self.wl, self.name, self.device = w, name, device
@@ -276,6 +289,11 @@ class Workload:
     def gpu_launches_per_step(self, launches_per_weight):
         return 1 + launches_per_weight * (len(self.lin) + 1) + 2
 
+    def gemm_shapes(self):
+        """The step's GEMM launches as (n, k, rows), one row slice per launch
+        where the library splits a weight into slices of 64 rows."""
+        return [(d.n, d.k, self.R) for d in self.lin] + [(self.head.n, self.head.k, self.R)]
+
     # the step ------------------------------------------------------------
     def step(self):
         w, w12 = self.wl, self.w12
@@ -287,11 +305,14 @@ class Workload:
 # CPU baseline: the oracle, as it stands, on a bounded sample
 # ---------------------------------------------------------------------------
 
-def oracle_sample_runner(wk: Workload, frac: float):
+def oracle_sample_runner(wk: Workload, frac: float, nthreads: int = 0):
     """A callable that runs the oracle over the first `frac` of every weight's
     output channels (multiples of 128, all rows): W12 decode (oracle unpack),
     FP64 GEMM for the linears, FP64 logits + argmax for the head, then the
-    tree build and acceptance.  Returns (callable, sampled W12 bytes, text)."""
+    tree build and acceptance.  The linears are one layer's: stacked layers
+    repeat the same shapes, so bytes per second carry over.  `nthreads`: the
+    oracle's worker threads (0: one per core).  Returns (callable, sampled W12
+    bytes, text)."""
     import oracle
     jobs = []
     total = 0
@@ -310,13 +331,13 @@ def oracle_sample_runner(wk: Workload, frac: float):
         for kind, p, x in jobs:
             wdec = oracle.w12_unpack(p)
             if kind == "lin":
-                oracle.gemm_f64(x, wdec)
+                oracle.gemm_f64(x, wdec, nthreads=nthreads)
             else:
-                am, _, _ = oracle.head_argmax(x, wdec)
+                am, _, _ = oracle.head_argmax(x, wdec, nthreads=nthreads)
         t = oracle.tree_build(wk.lat, w.budget)
         oracle.tree_accept(t, np.resize(am, t.R), w.n_req, w.p_max)
 
-    text = (f"first {frac:.4f} of the output channels of every linear and of the LM head "
+    text = (f"first {frac:.4f} of the output channels of one layer's linears and of the LM head "
             f"({total / 1e6:.1f} MB of W12), all {wk.R} rows; decode + FP64 GEMM/argmax + tree build + accept")
     return run, total, text
 
@@ -339,8 +360,16 @@ def cpu_baseline(wk: Workload, target_s=10.0):
         if dt >= 0.8 * target_s or n >= 8:
             break
     cores = os.cpu_count() or 1
-    return {"value": n * b / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{text}; {n} pass(es)", "seconds": round(dt, 2)}
+    out = {"value": n * b / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+           "sample": f"{text}; {n} pass(es)", "seconds": round(dt, 2)}
+    # the same oracle on one core, over a quarter of that sample
+    run1, b1, text1 = oracle_sample_runner(wk, max(1.0 / 512, frac / 4), nthreads=1)
+    t = time.time()
+    run1()
+    dt1 = max(time.time() - t, 1e-3)
+    out["one_core"] = {"value": b1 / dt1 / 1e9, "unit": "GB/s", "cores": 1, "sample": f"{text1}; 1 pass",
+                       "seconds": round(dt1, 2)}
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -393,7 +422,11 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": f"{args.workload}: {DESCRIPTIONS.get(args.workload, '')}", "rows": int(t.R)},
+            "config": {"workload": f"{args.workload}: {DESCRIPTIONS.get(args.workload, '')}", "rows": int(t.R),
+                       "sample": f"each step: the oracle over the first {frac:.4f} of the output channels of one "
+                                 "layer's linears and of the LM head (stacked layers repeat the same shapes), all "
+                                 "rows, plus tree build and acceptance; GB/s of the sampled W12 bytes",
+                       "same_config": False},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": text},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -691,27 +724,81 @@ def gdn_stack(wk: "Workload", K: int, W: int, seed: int = 0):
 # step time vs tree rows
 # ---------------------------------------------------------------------------
 
-def rows_sweep(base: "Workload", budgets, K: int, W: int, device):
-    """Step time and W12 GB/s of the graph-captured step for each node budget
-    of a single-request tree (16 drafted positions, top-16), reusing the
-    packed weights of `base` (only the tree, its rows and the activations
-    change).  Same timing rules as the headline number."""
+class CublasRef:
+    """Context for the W12 step: dense BF16 torch.matmul (cuBLAS) over the
+    same GEMM shapes, every stacked layer with dense weights of its own (so no
+    layer is served from L2), then the LM head's logits and their argmax,
+    captured in one CUDA graph.  Weights are N(0, 0.02) BF16."""
+
+    def __init__(self, wk: "Workload"):
+        import torch
+        self.torch, self.device = torch, wk.device
+        g = torch.Generator(device=wk.device)
+        g.manual_seed(1234)
+        bf = torch.bfloat16
+        self.lin = [(torch.randn((d.n, d.k), generator=g, device=wk.device, dtype=torch.float32) * 0.02).to(bf)
+                    for d in wk.lin]
+        self.head = (torch.randn((wk.head.n, wk.head.k), generator=g, device=wk.device,
+                                 dtype=torch.float32) * 0.02).to(bf)
+        self.bytes = sum(2 * w.numel() for w in self.lin) + 2 * self.head.numel()
+
+    def time_us(self, R: int, K: int, W: int) -> float:
+        torch = self.torch
+        xs = {}
+        for w in self.lin:
+            if w.shape[1] not in xs:
+                xs[w.shape[1]] = torch.randn((R, w.shape[1]), device=self.device, dtype=torch.bfloat16)
+        h = torch.randn((R, self.head.shape[1]), device=self.device, dtype=torch.bfloat16)
+
+        def step():
+            for w in self.lin:
+                torch.matmul(xs[w.shape[1]], w.t())
+            torch.argmax(torch.matmul(h, self.head.t()).float(), dim=1)
+
+        g = _graph_of(step)
+        for _ in range(W):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(K):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        del g
+        return 1e3 * e0.elapsed_time(e1) / K
+
+    def free(self):
+        self.lin, self.head = [], None
+        self.torch.cuda.empty_cache()
+
+
+def parse_sweep(spec: str):
+    """'1,8,32,b192' -> [(1, False), (8, False), (32, False), (192, True)]:
+    node budgets of one request's tree, or ('b' prefix) of 24 requests drafting
+    16/12/8 positions sharing the budget."""
+    out = []
+    for v in spec.split(","):
+        v = v.strip()
+        if v:
+            out.append((int(v[1:]), True) if v.startswith("b") else (int(v), False))
+    return out
+
+
+def rows_sweep(base: "Workload", points, K: int, W: int, device, cublas=None, peak=None):
+    """Step time and W12 GB/s of the graph-captured step at each node budget,
+    reusing the packed weights of `base` (only the tree, its rows and the
+    activations change), with dense cuBLAS BF16 on the same shapes and rows
+    beside it.  Same timing rules as the headline number."""
     import torch
     out = []
-    for b in budgets:
-        wk = Workload(base.name, int(b), device, share=base, one_request=True)
+    for b, batched in points:
+        variant = dict(n_req=24, positions=(16, 12, 8)) if batched else None
+        wk = Workload(base.name, int(b), device, share=base, one_request=not batched, variant=variant)
         for _ in range(W):
             wk.step()
         torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        s = torch.cuda.Stream()
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
-            wk.step()
-        torch.cuda.current_stream().wait_stream(s)
-        torch.cuda.synchronize()
-        with torch.cuda.graph(g):
-            wk.step()
+        g = _graph_of(wk.step)
         for _ in range(W):
             g.replay()
         torch.cuda.synchronize()
@@ -724,8 +811,18 @@ def rows_sweep(base: "Workload", budgets, K: int, W: int, device):
         ms = e0.elapsed_time(e1) / K
         if wk.ws.status() != 0:
             raise RuntimeError(f"device status {wk.w12.status_str(wk.ws.status())} at budget {b}")
-        out.append({"rows": int(wk.R), "step_us": round(1e3 * ms, 2), "w12_gbs": round(wk.w12_bytes() / (ms * 1e-3) / 1e9, 1)})
+        gbs = wk.w12_bytes() / (ms * 1e-3) / 1e9
+        e = {"rows": int(wk.R), "requests": int(wk.wl.n_req), "step_us": round(1e3 * ms, 2), "w12_gbs": round(gbs, 1),
+             "pct_of_8tbs": round(100 * gbs / NOMINAL_HBM_GBS, 2)}
+        if peak:
+            e["pct_of_measured_hbm"] = round(100 * gbs / peak, 2)
         del g
+        if cublas is not None:
+            cu = cublas.time_us(int(wk.R), K, W)
+            e["cublas_bf16_us"] = round(cu, 2)
+            e["w12_speedup_vs_cublas"] = round(cu / (1e3 * ms), 3)
+        out.append(e)
+        del wk
     return out
 
 
@@ -739,13 +836,14 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="w12", choices=["w12", "reference"])
-    ap.add_argument("--workload", default="single_27b")
+    ap.add_argument("--workload", default="full_depth_27b")
     ap.add_argument("--rows", type=int, default=0, help="override the node budget (tree rows)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cublas", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--rows-sweep", default=None,
-                    help="comma-separated node budgets timed after the headline (default: 1,8,32,64 for "
+                    help="comma-separated node budgets timed after the headline, each of one request's tree, "
+                         "or with a 'b' prefix of 24 requests' trees (default: 1,8,32,64,128,192,b192 for "
                          "single-request workloads, none otherwise; 'none' to skip)")
     ap.add_argument("--extras", default="all", choices=["all", "none"],
                     help="the measurements after the headline and its end-to-end pass (quick pass, certified "
@@ -864,14 +962,28 @@ def main():
     if chain:
         lb = [gemm_bytes]
     peak, peak_kind = load_peaks()
-    traffic = committed_traffic(args.workload)
+    traffic = None if chain or per_weight != 1 else committed_traffic(wk.gemm_shapes())
     kernels = {
         "tree_build_us": 1e3 * float(np.mean(tb_ms)),
-        "w12_gemm_us": [round(1e3 * float(v), 2) for v in gemm_ms],
-        "w12_gemm_gbs": [round(b / (float(v) * 1e-3) / 1e9, 1) for b, v in zip(lb, gemm_ms)],
         "argmax_stage2_us": 1e3 * float(per_launch[n_gemm]),
         "accept_us": 1e3 * float(per_launch[n_gemm + 1]),
     }
+    n_lin = len(wk.wl.linears)
+    if chain:
+        kernels["w12_gemm_chain_us"] = [round(1e3 * float(v), 2) for v in gemm_ms]
+    elif per_weight == 1:
+        # per linear of the layer (mean over the stacked layers) and the LM head
+        names = ["qkv", "o", "gate_up", "down"] if n_lin == 4 else [f"linear{i}" for i in range(n_lin)]
+        for i, nm in enumerate(names):
+            sel = range(i, len(wk.lin), n_lin)
+            t = float(np.mean([gemm_ms[j] for j in sel]))
+            kernels[f"{nm}_us"] = round(1e3 * t, 2)
+            kernels[f"{nm}_gbs"] = round(float(np.mean([lb[j] for j in sel])) / (t * 1e-3) / 1e9, 1)
+        kernels["head_us"] = round(1e3 * float(gemm_ms[-1]), 2)
+        kernels["head_gbs"] = round(lb[-1] / (float(gemm_ms[-1]) * 1e-3) / 1e9, 1)
+        kernels["layer_us"] = round(1e3 * float(np.sum(gemm_ms[:-1])) / max(1, wk.wl.layers), 2)
+    else:
+        kernels["w12_gemm_us"] = [round(1e3 * float(v), 2) for v in gemm_ms]
 
     # ------------------------------------------------------------ end to end
     e2e = None
@@ -881,10 +993,15 @@ def main():
         e2e = {"value": None, "unit": "GB/s", "error": str(ex)[:200]}
 
     # ------------------------------------------------------- cuBLAS context
-    cublas = None
+    cublas, cref = None, None
     if not args.no_cublas and rank == 0:
         try:
-            cublas = cublas_reference_us(wk, K)
+            cref = CublasRef(wk)
+            cu = cref.time_us(wk.R, max(10, min(K, 50)), W)
+            cublas = {"us_per_step": round(cu, 2), "bf16_bytes": cref.bytes, "gbs": round(cref.bytes / (cu * 1e-6) / 1e9, 1),
+                      "layers_per_step": wk.wl.layers, "w12_speedup": round(cu / (1e3 * ms), 3),
+                      "note": "torch.matmul BF16 (cuBLAS), dense weights of the same shapes for every stacked layer, "
+                              "LM head logits + argmax, one CUDA graph"}
         except Exception as ex:
             cublas = {"error": str(ex)[:200]}
 
@@ -924,12 +1041,14 @@ def main():
     sweep = None
     spec = args.rows_sweep
     if spec is None:
-        spec = "1,8,32,64" if wk.wl.n_req == 1 else "none"
+        spec = "1,8,32,64,128,192,b192" if wk.wl.n_req == 1 else "none"
     if spec != "none":
         try:
-            sweep = rows_sweep(wk, [int(v) for v in spec.split(",") if v], max(10, min(K, 50)), W, device)
+            sweep = rows_sweep(wk, parse_sweep(spec), max(10, min(K, 50)), W, device, cublas=cref, peak=peak)
         except Exception as ex:  # reported, never hidden
             sweep = [{"error": str(ex)[:200]}]
+    if cref is not None:
+        cref.free()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -941,18 +1060,21 @@ def main():
             "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
             "config": {"workload": f"{args.workload}: {DESCRIPTIONS.get(args.workload, '')}", "rows": wk.R,
-                       "requests": wk.wl.n_req, "w12_bytes_per_step": w12_bytes,
+                       "requests": wk.wl.n_req, "layers": wk.wl.layers, "w12_bytes_per_step": w12_bytes,
                        "l2": "inputs larger than L2 (W12 bytes per step vs 129 MB L2); no flush",
                        "timing": "CUDA-graph replays of the whole step, CUDA events" if graph else "eager launches",
-                       "parallelism": "replicas" if world > 1 else "single GPU", "gemm_kernel": args.gemm},
+                       "parallelism": "replicas" if world > 1 else "single GPU", "gemm_kernel": args.gemm,
+                       "gemm_chain": args.chain},
             "step_us": round(1e3 * ms, 2),
             "pct_of_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
             "pct_of_measured_hbm": round(100 * value / world / peak, 2),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": "k_w12_gemm + k_w12_gemm_tc",
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "kernel": "k_w12_chain" if chain else "k_w12_gemm + k_w12_gemm_tc",
                          "peak_kind": peak_kind,
-                         "note": "all W12 GEMM launches of a step (linears + LM head), serialised, "
-                                 "algorithmic bytes (W12 + activations + outputs) / summed launch time"},
+                         "note": "all W12 GEMM launches of a step (linears + LM head), serialised, algorithmic bytes "
+                                 "(W12 + activations + outputs) / summed launch time; traffic: ncu DRAM bytes read + "
+                                 "written of one layer's launches and the head at the same rows, times the layers"},
             "kernels": kernels,
             "e2e": e2e,
             "cublas_bf16": cublas,
@@ -965,8 +1087,11 @@ def main():
             "tlv_cycle": tlv,
             "gdn_tree": gdn,
         }
-        if sweep and len(sweep) > 1 and all("step_us" in e for e in sweep):
-            line["rows_sweep_flatness"] = round(sweep[-1]["step_us"] / sweep[0]["step_us"], 4)
+        if sweep and all("step_us" in e for e in sweep):
+            one = {e["rows"]: e["step_us"] for e in sweep if e["requests"] == 1}
+            if 1 in one and 64 in one:
+                line["rows_sweep_flatness"] = round(one[64] / one[1], 4)
+                line["rows_sweep_flatness_note"] = "step time at 64 rows / at 1 row, one request's tree"
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()
@@ -1054,33 +1179,6 @@ def measure_e2e(wk: Workload, K: int, w12_bytes: int, world: int = 1, dist=None,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "note": "inputs copied from pinned host memory and results read back every step; two device input "
                     "sets alternate so that step k+1's copies overlap step k's pass"}
-
-
-def cublas_reference_us(wk: Workload, K: int):
-    """torch.matmul (cuBLAS) BF16 with dense weights of the same shapes, for
-    context: the same rows through the same linears and the head (logits
-    only, no argmax)."""
-    import torch
-    shapes = [(d.n, d.k) for d in wk.lin[:len(wk.wl.linears)]] + [(wk.head.n, wk.head.k)]
-    ws = [torch.randn((n, k), dtype=torch.bfloat16, device=wk.device) * 0.02 for n, k in shapes]
-    xs = [torch.randn((wk.R, k), dtype=torch.bfloat16, device=wk.device) for _, k in shapes]
-    for _ in range(3):
-        for x, w in zip(xs, ws):
-            torch.matmul(x, w.t())
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(K):
-        for x, w in zip(xs, ws):
-            torch.matmul(x, w.t())
-    e1.record()
-    torch.cuda.synchronize()
-    us = 1e3 * e0.elapsed_time(e1) / K
-    dense = sum(2 * n * k for n, k in shapes)
-    del ws, xs
-    torch.cuda.empty_cache()
-    return {"us_per_step": round(us, 2), "bf16_bytes": dense, "gbs": round(dense / (us * 1e-6) / 1e9, 1),
-            "layers_per_step": wk.wl.layers}
 
 
 if __name__ == "__main__":

@@ -153,10 +153,11 @@ WORKLOADS: Dict[str, Workload] = {
     # the same with chains (rank-0 candidates only)
     "b4_chain": Workload("b4_chain", LAYER_4B, vocab=151936, hidden=2560,
                          n_req=32, positions=(8, 12, 16), budget=256, n_cand=1),
-    # 64 stacked 27B-like layers + head; rows swept by the caller
+    # 64 stacked 27B-like layers + head; one request's 32-node tree by
+    # default, rows swept by the caller
     "full_depth_27b": Workload("full_depth_27b", LAYER_27B, vocab=151936,
-                               hidden=5120, n_req=24, positions=(16, 12, 8),
-                               budget=192, layers=64),
+                               hidden=5120, n_req=1, positions=(16,),
+                               budget=32, layers=64),
 }
 
 
