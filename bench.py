@@ -438,20 +438,22 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 
 def quick_pass(wk: "Workload", K: int, W: int):
-    """The same layer and LM head read through the quick pass (w12_gemm_q /
-    w12_lmhead_argmax_q: the 8 KB view plane of every record, low mantissa
-    bits at the midpoint): graph-timed step (every linear + the head + the
-    argmax reduction), the head launch alone, and the top-1 agreement of the
-    quick argmax with the exact one on the step's rows."""
+    """The same step read through the quick pass (w12_verify_step_q: the 8 KB
+    view plane of every record, low mantissa bits at the midpoint):
+    graph-timed pass (tree build, every linear, the head, the argmax
+    reduction and acceptance, as the exact step), the head launch alone, and
+    the top-1 agreement of the quick argmax with the exact one on the step's
+    rows."""
     import torch
     w12 = wk.w12
     qs = [torch.empty_like(y) for y in wk.ys]
     qam = torch.empty_like(wk.argmax)
+    qstep_args = w12.VerifyStep(wk.lin, wk.xs, qs, wk.head, wk.h, qam)
+    qtok, qlen = torch.empty_like(wk.acc_tok), torch.empty_like(wk.acc_len)
 
     def qstep():
-        for dw, x, y in zip(wk.lin, wk.xs, qs):
-            w12.w12_gemm(dw, x, wk.ws, y=y, quick=True)
-        w12.w12_lmhead_argmax(wk.head, wk.h, wk.ws, argmax=qam, quick=True)
+        w12.w12_tree_build(wk.dlat, wk.wl.budget, wk.ws, wk.tree)
+        w12.w12_verify_step_q(qstep_args, wk.tree, wk.wl.n_req, wk.wl.p_max, wk.ws, qtok, qlen)
 
     def timed(fn):
         for _ in range(W):

@@ -158,7 +158,13 @@ w12_status w12_status_fetch(void *ws, w12_stream_t stream);
 
 /*
  * Decode a packed tensor to row-major BF16 dst[n][k] (device), escapes
- * restored.  Errors: W12_E_INVAL, W12_E_UNSUPPORTED, W12_E_CUDA.
+ * restored: the exact restore of explainer 4.1 "W12: a 12-bit lossless
+ * weight format" (each in-window weight rebuilt from its sign, exponent
+ * offset against the channel's window and seven mantissa bits; each escaped
+ * weight from its 16-bit escape entry).  dst is caller-owned, 16-byte
+ * aligned.  Asynchronous on the stream.  Errors: W12_E_INVAL (null or
+ * misaligned pointer, malformed weight), W12_E_UNSUPPORTED (n % 128 or
+ * k % 64 not zero), W12_E_CUDA.
  */
 w12_status w12_unpack(const w12_weight *w, uint16_t *dst_bf16, w12_stream_t stream);
 
@@ -184,11 +190,11 @@ w12_status w12_gemm(const w12_weight *w, const uint16_t *x, int32_t R, uint16_t 
 
 /*
  * w12_gemm without a workspace, for callers that cannot allocate device
- * memory where they call it: code running inside a CUDA stream capture
- * (where cudaMalloc may be refused), plugin hosts that give kernels no
- * device allocations, and processes that must keep a fixed footprint.  The
- * paper has no counterpart to this entry point; it computes exactly what
- * w12_gemm computes, with the same kernel.
+ * memory where they call it: plugin hosts that give kernels no device
+ * allocations of their own, and processes that must keep a fixed device
+ * footprint (an allocation there could fail or stall mid-run).  The paper
+ * has no counterpart to this entry point; it computes exactly what w12_gemm
+ * computes, with the same kernel.
  *   - Scratch (split-tile partial sums, tile arrival counters, a status word)
  *     is a file-scope device array of about 4.1 MiB that every GPU loading
  *     the library holds until the process exits.  The call allocates and
@@ -375,10 +381,20 @@ typedef struct {
 } w12_step;
 
 /*
- * One verify pass over a built tree: every linear in order (each may start
+ * One verify pass over a built tree (explainer 1.1 and 2.1: the target
+ * model verifies every draft row of the tree in one forward pass, keeps the
+ * drafts equal to the target's argmax at their parent and appends the bonus
+ * token; poot-llm "What a round guarantees": the accepted tokens are exactly
+ * the greedy autoregressive ones).  Every linear in order (each may start
  * streaming its weights while the previous one finishes), then the LM head
- * with per-row argmax, then greedy acceptance.  Same outputs as the
- * individual calls.  rows = tree->R.
+ * with per-row argmax, then greedy acceptance; same outputs as the
+ * individual calls (w12_gemm, w12_lmhead_argmax, w12_tree_accept).
+ * step: host arrays of device pointers (x_l[R][k_l], y_l[R][n_l], h[R][k],
+ * argmax[R]); rows = tree->R; acc_tok[n_req][p_max + 1], acc_len[n_req],
+ * acc_node[n_req] (nullable) as for w12_tree_accept.  ws sized by
+ * w12_workspace_bytes(R, max n_l, head n, n_req).  Asynchronous.  Errors:
+ * W12_E_INVAL / W12_E_UNSUPPORTED / W12_E_WORKSPACE before any launch,
+ * W12_E_CUDA on a failed launch; device conditions in the status word.
  */
 w12_status w12_verify_step(const w12_step *step, const w12_tree *tree, int32_t n_req, int32_t p_max,
                            int32_t *acc_tok, int32_t *acc_len, int32_t *acc_node, void *ws, size_t ws_bytes,

@@ -778,12 +778,15 @@ int static_scratch_limits(int32_t *max_rows, int32_t *max_tiles)
 
 int launch_gemm_static_scratch(const GemmArgs &in, void *stream)
 {
-    if (in.R < 1 || in.R > kStaticMaxRows || in.w.n_tiles > kStaticMaxTiles || in.num_sms > kStaticMaxCtas)
-        return (int)cudaErrorInvalidValue;
+    if (in.R < 1 || in.R > kStaticMaxRows || in.w.n_tiles > kStaticMaxTiles) return (int)cudaErrorInvalidValue;
     unsigned char *base = nullptr;
     if (int e = static_scratch_on_current_device(&base)) return e;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     GemmArgs a = in;
+    // a device with more SMs than the array has partial slots for runs a
+    // smaller grid (the split points follow the grid, so the result is that
+    // of w12_gemm on a device of kStaticMaxCtas SMs)
+    a.num_sms = std::min(in.num_sms, kStaticMaxCtas);
     a.status = reinterpret_cast<int32_t *>(base);
     a.counters = reinterpret_cast<int32_t *>(base + kStaticStatusBytes);
     a.partial = reinterpret_cast<float *>(base + kStaticStatusBytes + kStaticCounterBytes);

@@ -631,7 +631,7 @@ __global__ void __launch_bounds__(128) k_tree_accept(const int32_t *parent, cons
     }
     if (lane == 0) {
         out[n] = argmax[cur];
-        acc_len[r] = depth[cur] + 1;
+        acc_len[r] = n + 1;   // the tokens written: n drafts and the bonus
         if (acc_node) acc_node[r] = cur;
     }
 }

@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <vector>
 
@@ -84,18 +85,25 @@ bool use_chain(int n_jobs)
     return n_jobs + 1 <= kGridWords;
 }
 
+// SM count of the current device, looked up once per device.  Each device
+// has its own cache entry (an atomic, so host threads driving different
+// devices never read one another's count); devices beyond the table are
+// looked up on every call.
 int num_sms()
 {
+    constexpr int kDevCache = 64;
+    static std::atomic<int> cached[kDevCache];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return kMaxCtas;
-    static int cached_dev = -1, cached = 0;
-    if (dev != cached_dev) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return kMaxCtas;
-        cached_dev = dev;
-        cached = std::min(n, kMaxCtas);
+    if (dev >= 0 && dev < kDevCache) {
+        const int c = cached[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
     }
-    return cached;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return kMaxCtas;
+    n = std::min(n, kMaxCtas);
+    if (dev >= 0 && dev < kDevCache) cached[dev].store(n, std::memory_order_relaxed);
+    return n;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }

@@ -4,8 +4,9 @@ CUDA graph, default GEMM path choice).
 
 The oracle cannot run every output of every linear at these sizes in
 seconds, so the linears are checked on sampled output channels (random ones
-plus the first channels of the tiles where stream-K splits CTA shares).  The
-tree, the full LM-head argmax and the accepted tokens are checked whole.
+plus the first channels of the tiles where stream-K splits CTA shares); for
+the 64-layer stack, in the first, a middle and the last layer.  The tree,
+the full LM-head argmax and the accepted tokens are checked whole.
 """
 import os
 import sys
@@ -38,7 +39,7 @@ def _sample_channels(n, k, n_sms, rng, n_random=96):
     return np.array(sorted(ch), dtype=np.int64)
 
 
-@pytest.mark.parametrize("name", ["single_27b", "batched_27b", "b4_tree"])
+@pytest.mark.parametrize("name", ["single_27b", "batched_27b", "b4_tree", "full_depth_27b"])
 def test_full_size_verify_step(name):
     sys.path.insert(0, ROOT)
     import bench
@@ -77,13 +78,24 @@ def test_full_size_verify_step(name):
 
     rng = np.random.default_rng(1234)
     n_sms = w12.num_sms()
-    for i, (bits, x) in enumerate(zip(wk.lin_bits, wk.x_bits)):
-        n, k = bits.shape
-        cols = _sample_channels(n, k, n_sms, rng)
-        ref = oracle.gemm_f64(x, np.ascontiguousarray(bits[cols]))
-        got = np.ascontiguousarray(_bits(wk.ys[i])[:, cols])
-        got = synth.bf16_bits_to_f32(got).astype(np.float64)
-        assert H.gemm_rel_err(got, ref) <= H.GEMM_REL_TOL, (name, i)
+    n_lin = len(w.linears)
+    # stacked layers: the first, one past the middle and the last layer (three
+    # of the four distinct weight sets; every layer streams its own copy)
+    layers = sorted({0, w.layers // 2 + 1, w.layers - 1}) if w.layers > 1 else [0]
+    for layer in layers:
+        for i, x in enumerate(wk.x_bits):
+            if layer == 0:
+                bits = wk.lin_bits[i]
+            else:
+                n, k = w.linears[i]
+                bits = synth.weights(n, k, w.seed, synth.STREAM_LINEAR + 100 * (layer % 4) + i,
+                                     w.outlier_frac, w.zero_frac)
+            n, k = bits.shape
+            cols = _sample_channels(n, k, n_sms, rng)
+            ref = oracle.gemm_f64(x, np.ascontiguousarray(bits[cols]))
+            got = np.ascontiguousarray(_bits(wk.ys[layer * n_lin + i])[:, cols])
+            got = synth.bf16_bits_to_f32(got).astype(np.float64)
+            assert H.gemm_rel_err(got, ref) <= H.GEMM_REL_TOL, (name, layer, i)
 
     am, _, mg = oracle.head_argmax(wk.h_bits, wk.head_bits)
     gated = mg > H.MARGIN_GATE
