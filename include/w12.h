@@ -352,7 +352,11 @@ typedef struct {
  * with FP32 accumulation; both methods match the FP64 path walk to FP32
  * rounding.  Device checks: a request with more than 64 rows sets
  * W12_E_UNSUPPORTED, a parent outside its request or after its child
- * W12_E_INVAL in the status word (ws as for w12_tree_build).
+ * W12_E_INVAL in the status word (ws as for w12_tree_build); with
+ * W12_GDN_WY, row offsets outside [0, tree->R] also set W12_E_INVAL, and a
+ * bad row range anywhere leaves the whole output unwritten.  W12_GDN_WY on
+ * a tree of several requests uses tensor memory and 226 KB of shared memory
+ * per CTA (one CTA per SM), and its bounded waits report W12_E_TIMEOUT.
  */
 w12_status w12_gdn_tree_verify(const w12_gdn_layer *layer, const w12_tree *tree, int32_t n_req, int32_t method,
                                float *o, void *ws, size_t ws_bytes, w12_stream_t stream);

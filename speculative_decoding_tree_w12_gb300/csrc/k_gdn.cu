@@ -4,32 +4,45 @@
 // d_k) updated by one rank-one step per token,
 //     S <- a S (I - b k k^T) + b v k^T,      o = S q,
 // and over a tree the state is recomputed along each root path from the
-// committed state instead of being snapshotted per node.  Two kernels give
+// committed state instead of being snapshotted per node.  Two methods give
 // the per-node outputs:
 //
 //  * k_gdn_path: the path walk.  Every node replays its root path on a copy
 //    of the committed state (FP32).  One CTA owns 32 state rows (rows of S
 //    update independently), each warp 4 of them in registers.
-//  * k_gdn_wy: the WY form (TreeWY, explainer 4.2).  With g_j the product
-//    of gates along node j's root path, u_j = b_j (v_j - a_j S_parent k_j)
-//    and S_j = g_j S0 + sum over i on j's path of (g_j/g_i) u_i k_i^T,
+//  * the WY form (TreeWY, explainer 4.2).  With g_j the product of gates
+//    along node j's root path, u_j = b_j (v_j - a_j S_parent k_j) and
+//    S_j = g_j S0 + sum over i on j's path of (g_j/g_i) u_i k_i^T,
 //        (I + A) U = B,  A[j,i] = b_j (g_j/g_i) k_i.k_j  (i a strict ancestor)
 //                        B[j]   = b_j (v_j - g_j S0 k_j)
 //        o_j = g_j S0 q_j + sum over i on j's path of (g_j/g_i) (k_i.q_j) u_i.
-//    The state products S0 k and S0 q run on tensor cores: S0 is split into
-//    three BF16 pieces that add up to the FP32 value exactly, each piece is
-//    multiplied by the BF16 keys/queries (exact products) with FP32
-//    accumulation.  k.k and k.q are BF16 products too.  The triangular solve
-//    (by depth level) and the output sums run on the FP32 pipes.
+//    The state products S0 k and S0 q take S0 as three BF16 pieces that add
+//    up to the FP32 value exactly (bit masks and exact subtractions, no
+//    rounding), each piece times the BF16 keys/queries (exact products) with
+//    FP32 accumulation; k.k and q.k are BF16 products too.  Two kernels:
+//      - k_gdn_wy_slice, for a tree of one request: CTAs of (window, head,
+//        32 state rows), the products on warp-level MMAs, the solve by depth
+//        level across the CTA's warps;
+//      - k_gdn_wy, for several requests: CTAs of (window, head) holding all
+//        128 state rows in tensor memory, the products on tcgen05 MMAs, each
+//        state row's column solved by its own threads.
+//    On this part a warp-level m16n8k16 MMA costs tens of cycles of the
+//    tensor pipe, so the sliced kernel pays per request; the tensor-memory
+//    kernel pays a fixed cost per CTA (tensor memory, the state staged by
+//    TMA) and little per request.
 //
 // The committed-state update after acceptance (k_gdn_commit) replays the
 // accepted path, like the path kernel, and writes the state.
 //
-// Grid of every kernel: (request, head, d_v / 32).  Rows of one request are
-// its tree rows [req_row_off[r], req_row_off[r+1]), at most 64; a larger
-// request sets W12_E_UNSUPPORTED in the status word.
+// Grid of the path walk and the commit: (request, head, d_v / 32); of the WY
+// kernels: windows of first rows (several requests per CTA), see below.  Rows
+// of one request are its tree rows [req_row_off[r], req_row_off[r+1]), at
+// most 64; a larger request sets W12_E_UNSUPPORTED in the status word.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <algorithm>
 
 #include "w12_device.cuh"
 
@@ -40,14 +53,15 @@ namespace {
 constexpr int kD = 128;       // head dimension (d_k = d_v)
 constexpr int kVS = 32;       // state rows per CTA
 constexpr int kNR = 64;       // rows per request
-constexpr int kThreads = 256;
-constexpr int kKS = kD + 8;   // BF16 row stride of K / Q in shared memory
-constexpr int kSS = kD + 4;   // FP32 row stride of the state slice
+constexpr int kKS = kD + 16;  // BF16 row stride of K / Q in the slice kernel (rows 8 banks apart)
 constexpr int kPS = kVS + 1;  // FP32 row stride of N x 32 matrices
 constexpr int kMS = kNR + 1;  // FP32 row stride of N x N matrices
+constexpr int kSliceWin = 64; // slice kernel: first rows of the requests one CTA owns
+constexpr int kThreads = 256;
 
 struct GdnParams {
-    int32_t H, n_req;
+    int32_t H, n_req, R, win;
+    uint64_t timeout_ns;
     const float *S0;
     const uint16_t *q, *k, *v;
     const float *alpha, *beta;
@@ -58,19 +72,20 @@ struct GdnParams {
 
 __device__ __forceinline__ float bf(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
-__device__ __forceinline__ uint32_t pack2(__nv_bfloat16 lo, __nv_bfloat16 hi)
+// x = hi + mid + lo exactly, each a BF16 value: hi is x cut to its top 8
+// significant bits (its upper 16 bits), mid the same cut of the remainder,
+// lo what is left (at most 8 significant bits).  Both subtractions are exact,
+// and so is the sum for |x| >= 2^-110 (below that only bits under 2^-126 can
+// drop).  Returned as the BF16 pairs of (x0, x1).
+__device__ __forceinline__ void split3(float x0, float x1, uint32_t &h, uint32_t &m, uint32_t &l)
 {
-    return (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
-}
-
-// x = hi + mid + lo exactly (24 significand bits in three 8-bit pieces)
-__device__ __forceinline__ void split3(float x, __nv_bfloat16 &h, __nv_bfloat16 &m, __nv_bfloat16 &l)
-{
-    h = __float2bfloat16_rn(x);
-    const float r1 = x - __bfloat162float(h);
-    m = __float2bfloat16_rn(r1);
-    const float r2 = r1 - __bfloat162float(m);
-    l = __float2bfloat16_rn(r2);
+    const uint32_t a0 = __float_as_uint(x0), a1 = __float_as_uint(x1);
+    const float r0 = x0 - __uint_as_float(a0 & 0xffff0000u), r1 = x1 - __uint_as_float(a1 & 0xffff0000u);
+    const uint32_t b0 = __float_as_uint(r0), b1 = __float_as_uint(r1);
+    const float q0 = r0 - __uint_as_float(b0 & 0xffff0000u), q1 = r1 - __uint_as_float(b1 & 0xffff0000u);
+    h = __byte_perm(a0, a1, 0x7632);
+    m = __byte_perm(b0, b1, 0x7632);
+    l = __byte_perm(__float_as_uint(q0), __float_as_uint(q1), 0x7632);
 }
 
 __device__ __forceinline__ void mma_bf16(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1)
@@ -79,6 +94,12 @@ __device__ __forceinline__ void mma_bf16(float c[4], const uint32_t a[4], uint32
                  "{%0,%1,%2,%3};"
                  : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// bring [ptr, ptr + bytes) into L2 without waiting (16-byte aligned, bytes a multiple of 16)
+__device__ __forceinline__ void prefetch_l2(const void *ptr, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
 }
 
 // rows of request r, or -1 (and the status word set) when there are too many
@@ -137,226 +158,884 @@ __device__ __forceinline__ void tree_info(const GdnParams &p, TreeInfo &t, int r
 }
 
 // ---------------------------------------------------------------------------
-// WY form
+// WY form for a single request: state-row slices
 // ---------------------------------------------------------------------------
+//
+// Grid (window, head, d_v / 32).  A CTA owns the requests whose first row lies
+// in its window of kSliceWin rows and takes them in packs: runs of whole requests
+// that span at most 64 rows.  One pass over a pack serves all of its requests
+// at once: the ancestor sets, the k.k and q.k products, the solve by depth
+// level and the outputs are per row, and rows of different requests never
+// meet (a parent lies in its child's request).  Only the state products
+// S0 k and S0 q differ by request: each warp takes the pack's requests in
+// turn, its B fragments read straight from the request's state slice in
+// global memory, the next request's fragments loaded while the current
+// one's products run.
+//
+// Inside every 16-wide k step the products pair MMA k-slot 2t + e with
+// feature 4t + e and slot 2t + 8 + e with feature 4t + 2 + e (t = lane % 4,
+// e = 0, 1), for both operands: a sum over k does not depend on the order, and
+// each lane then reads four consecutive features with one load.
 
-struct WyShared {
+struct SliceShared {
     __nv_bfloat16 K[kNR * kKS], Q[kNR * kKS];
-    float S[kVS * kSS];
-    float P[kNR * kPS], Rq[kNR * kPS], U[kNR * kPS];
+    float V[kNR * kPS], P[kNR * kPS], Rq[kNR * kPS], U[kNR * kPS];
     float KK[kNR * kMS], QK[kNR * kMS];
     TreeInfo t;
+    unsigned long long starts;   // bit i: a request of the pack starts at pack row i
+    int32_t rq[kNR];             // the request that starts at pack row i
+    int32_t lvl_cnt[kNR];        // rows per depth level, then each row's place in its level
+    int8_t lidx[kNR];
     int8_t order[kNR];
     int8_t lvl_off[kNR + 2];
-    int32_t maxd;
+    int32_t maxd, pack_end;
 };
 
-__global__ void __launch_bounds__(kThreads, 1) k_gdn_wy(const GdnParams p)
+// B fragments of one 8-row tile of a request's state slice: lane (g, t) holds
+// S[row g][16 s + 4 t .. 16 s + 4 t + 3] for the eight k steps s
+__device__ __forceinline__ const float *state_rows(const GdnParams &p, int r, int h, int vrow)
 {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    WyShared &s = *reinterpret_cast<WyShared *>(smem_raw);
-    const int r = blockIdx.x, h = blockIdx.y, vs = blockIdx.z * kVS;
+    return p.S0 + (((size_t)r * p.H + h) * kD + vrow) * kD;
+}
+
+__device__ __forceinline__ void mma_a(const __nv_bfloat16 *X, int row, int col, uint32_t a[4])
+{
+    const uint2 lo = *reinterpret_cast<const uint2 *>(&X[row * kKS + col]);
+    const uint2 hi = *reinterpret_cast<const uint2 *>(&X[(row + 8) * kKS + col]);
+    a[0] = lo.x;
+    a[2] = lo.y;
+    a[1] = hi.x;
+    a[3] = hi.y;
+}
+
+__global__ void __launch_bounds__(kThreads, 2) k_gdn_wy_slice(const GdnParams p)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    SliceShared &s = *reinterpret_cast<SliceShared *>(smem_raw);
+    const int h = blockIdx.y, vs = blockIdx.z * kVS;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int H = p.H;
-    int row0;
-    const int n = request_rows(p, r, row0);
-    if (n <= 0) return;
-    const int n16 = (n + 15) & ~15;
-    if (tid == 0) s.maxd = 0;
-
-    // every global read issued before the first shared-memory store: the
-    // state slice, K and Q rows (16-byte pieces, zero padding to 16-row
-    // tiles) and the value slice (kept in registers until the state slice's
-    // space is free)
-    const float *S0 = p.S0 + (((size_t)r * H + h) * kD + vs) * kD;
-    float4 sv[kVS * kD / 4 / kThreads];
-#pragma unroll
-    for (int i = 0; i < kVS * kD / 4 / kThreads; ++i)
-        sv[i] = *reinterpret_cast<const float4 *>(S0 + (size_t)(tid + i * kThreads) * 4);
-    uint4 kv[kNR * 16 / kThreads], qv[kNR * 16 / kThreads];
-    uint32_t vv[kNR * 16 / kThreads];
-#pragma unroll
-    for (int i = 0; i < kNR * 16 / kThreads; ++i) {
-        const int e = tid + i * kThreads, j = e >> 4;
-        kv[i] = qv[i] = make_uint4(0, 0, 0, 0);
-        vv[i] = 0;
-        if (j < n) {
-            const size_t base = ((size_t)(row0 + j) * H + h) * kD;
-            kv[i] = *reinterpret_cast<const uint4 *>(p.k + base + (e & 15) * 8);
-            qv[i] = *reinterpret_cast<const uint4 *>(p.q + base + (e & 15) * 8);
-            vv[i] = *reinterpret_cast<const uint32_t *>(p.v + base + vs + (e & 15) * 2);
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < kVS * kD / 4 / kThreads; ++i) {
-        const int e = tid + i * kThreads, v = e / (kD / 4), c4 = (e % (kD / 4)) * 4;
-        *reinterpret_cast<float4 *>(&s.S[v * kSS + c4]) = sv[i];
-    }
-#pragma unroll
-    for (int i = 0; i < kNR * 16 / kThreads; ++i) {
-        const int e = tid + i * kThreads, j = e >> 4;
-        if (j < n16) {
-            *reinterpret_cast<uint4 *>(&s.K[j * kKS + (e & 15) * 8]) = kv[i];
-            *reinterpret_cast<uint4 *>(&s.Q[j * kKS + (e & 15) * 8]) = qv[i];
-        }
-    }
-    // ancestor sets and cumulative gates, then rows ordered by depth level
-    tree_info(p, s.t, row0, n, h);
-    for (int j = tid; j < n; j += kThreads) {
-        const int dj = s.t.depth[j];
-        atomicMax(&s.maxd, dj);
-        int pos = 0;
-        for (int i = 0; i < n; ++i) {
-            const int di = s.t.depth[i];
-            pos += (di < dj) || (di == dj && i < j);
-        }
-        s.order[pos] = (int8_t)j;
-    }
-    __syncthreads();
-    for (int L = tid; L <= s.maxd + 1; L += kThreads) {
-        int c = 0;
-        for (int i = 0; i < n; ++i) c += s.t.depth[i] < L;
-        s.lvl_off[L] = (int8_t)c;
-    }
-    __syncthreads();
-
     const int g8 = lane >> 2, t4 = lane & 3;
-    const int mt_n = n16 / 16;
-    // P = K S^T and Rq = Q S^T (N x 32): warp -> (matrix, 8-column tile), all row tiles
-    {
-        const __nv_bfloat16 *X = (warp >> 2) ? s.Q : s.K;
-        float *Y = (warp >> 2) ? s.Rq : s.P;
-        const int nt = (warp & 3) * 8;
-        float acc[4][4];
+    const int H = p.H;
+    const int w0 = blockIdx.x * kSliceWin, w1 = w0 + kSliceWin;
+
+    // the requests whose first row lies in [w0, w1): [r_lo, r_hi).  Every CTA
+    // checks every request's row range first, so all of them agree on the
+    // requests' places (or all stop).
+    int r_lo = 0, r_hi = 0, bad = 0;
+    for (int base = 0; base < p.n_req; base += kThreads) {
+        const int r = base + tid;
+        int lo = 0, hi = 0;
+        if (r < p.n_req) {
+            const int o0 = p.req_row_off[r], o1 = p.req_row_off[r + 1];
+            const int code = (o1 - o0 < 0 || o1 - o0 > kNR) ? (int)W12_E_UNSUPPORTED
+                             : (o0 < 0 || o1 > p.R)         ? (int)W12_E_INVAL
+                                                            : 0;
+            if (code) {
+                atomicCAS(p.status, 0, code);
+                bad = 1;
+            }
+            lo = o0 < w0;
+            hi = o0 < w1;
+        }
+        r_lo += __syncthreads_count(lo);
+        r_hi += __syncthreads_count(hi);
+    }
+    if (__syncthreads_or(bad) || r_lo >= r_hi) return;
+
+    int a = p.req_row_off[r_lo];
+    const int row_end = p.req_row_off[r_hi];
+    while (a < row_end) {
+        // this pack: the requests that start at or after row a and end by a + 64
+        if (tid == 0) {
+            s.pack_end = a;
+            s.starts = 0ull;
+            s.maxd = 0;
+        }
+        if (tid < kNR) s.lvl_cnt[tid] = 0;
+        __syncthreads();
+        // (each request's state slice starts on its way to L2 at once: the
+        // warps read the slices one request after another)
+        for (int r = r_lo + tid; r < r_hi; r += kThreads) {
+            const int o0 = p.req_row_off[r], o1 = p.req_row_off[r + 1];
+            if (o0 >= a && o1 <= a + kNR && o1 > o0) {
+                atomicMax(&s.pack_end, o1);
+                atomicOr(&s.starts, 1ull << (o0 - a));
+                s.rq[o0 - a] = r;
+                prefetch_l2(state_rows(p, r, h, vs), kVS * kD * sizeof(float));
+            }
+        }
+        __syncthreads();
+        const int n = s.pack_end - a, n16 = (n + 15) & ~15;
+        const unsigned long long starts = s.starts;
+
+        // every global read of the pack issued before its first shared-memory
+        // store: K and Q rows (16-byte pieces, zero padding to 16-row tiles),
+        // the value slice, the rows' parents, gates and strengths, and this
+        // warp's fragments of the first request's state
+        const int mat = warp >> 2, nt = (warp & 3) * 8;
+        const float *srow = state_rows(p, s.rq[0], h, vs + nt + g8) + 4 * t4;
+        float4 sf[kD / 16];
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
+        for (int ks = 0; ks < kD / 16; ++ks) sf[ks] = *reinterpret_cast<const float4 *>(srow + 16 * ks);
+        uint4 kv[kNR * 16 / kThreads], qv[kNR * 16 / kThreads];
+        uint32_t vv[kNR * 16 / kThreads];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[m][e] = 0.f;
-#pragma unroll 2
-        for (int ks = 0; ks < kD; ks += 16) {
-            // B fragment: B[k][n] = S[n][k], split into three BF16 pieces
-            const float *srow = &s.S[(nt + g8) * kSS + ks + t4 * 2];
-            __nv_bfloat16 h0, m0, l0, h1, m1, l1, h2, m2, l2, h3, m3, l3;
-            split3(srow[0], h0, m0, l0);
-            split3(srow[1], h1, m1, l1);
-            split3(srow[8], h2, m2, l2);
-            split3(srow[9], h3, m3, l3);
-            const uint32_t bh0 = pack2(h0, h1), bh1 = pack2(h2, h3);
-            const uint32_t bm0 = pack2(m0, m1), bm1 = pack2(m2, m3);
-            const uint32_t bl0 = pack2(l0, l1), bl1 = pack2(l2, l3);
+        for (int i = 0; i < kNR * 16 / kThreads; ++i) {
+            const int e = tid + i * kThreads, j = e >> 4;
+            kv[i] = qv[i] = make_uint4(0, 0, 0, 0);
+            vv[i] = 0;
+            if (j < n) {
+                const size_t base = ((size_t)(a + j) * H + h) * kD;
+                kv[i] = *reinterpret_cast<const uint4 *>(p.k + base + (e & 15) * 8);
+                qv[i] = *reinterpret_cast<const uint4 *>(p.q + base + (e & 15) * 8);
+                vv[i] = *reinterpret_cast<const uint32_t *>(p.v + base + vs + (e & 15) * 2);
+            }
+        }
+        int pr = -1;
+        float al = 0.f, be = 0.f;
+        if (tid < n) {
+            pr = p.parent[a + tid];
+            al = p.alpha[(size_t)(a + tid) * H + h];
+            be = p.beta[(size_t)(a + tid) * H + h];
+        }
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                if (m < mt_n) {
-                    const __nv_bfloat16 *xr = &X[(m * 16 + g8) * kKS + ks + t4 * 2];
-                    uint32_t a[4];
-                    a[0] = *reinterpret_cast<const uint32_t *>(xr);
-                    a[1] = *reinterpret_cast<const uint32_t *>(xr + 8 * kKS);
-                    a[2] = *reinterpret_cast<const uint32_t *>(xr + 8);
-                    a[3] = *reinterpret_cast<const uint32_t *>(xr + 8 * kKS + 8);
-                    mma_bf16(acc[m], a, bl0, bl1);
-                    mma_bf16(acc[m], a, bm0, bm1);
-                    mma_bf16(acc[m], a, bh0, bh1);
+        for (int i = 0; i < kNR * 16 / kThreads; ++i) {
+            const int e = tid + i * kThreads, j = e >> 4;
+            if (j < n16) {
+                *reinterpret_cast<uint4 *>(&s.K[j * kKS + (e & 15) * 8]) = kv[i];
+                *reinterpret_cast<uint4 *>(&s.Q[j * kKS + (e & 15) * 8]) = qv[i];
+            }
+            if (j < n) {
+                s.V[j * kPS + (e & 15) * 2] = __uint_as_float(vv[i] << 16);
+                s.V[j * kPS + (e & 15) * 2 + 1] = __uint_as_float(vv[i] & 0xffff0000u);
+            }
+        }
+        // parents: inside the row's own request and before the row, else
+        // W12_E_INVAL and the row becomes a root
+        if (tid < n) {
+            const int rs = 63 - __clzll((long long)(starts & (~0ull >> (63 - tid))));   // the request's first row
+            int pl = pr < 0 ? -1 : pr - a;
+            if (pr >= 0 && (pl < rs || pl >= tid)) {
+                atomicCAS(p.status, 0, (int32_t)W12_E_INVAL);
+                pl = -1;
+            }
+            s.t.par[tid] = pl;
+            s.t.alpha[tid] = al;
+            s.t.beta[tid] = be;
+        }
+        __syncthreads();
+        // ancestor sets, cumulative gates, depths
+        if (tid < n) {
+            unsigned long long m = 0ull;
+            float g = s.t.alpha[tid];
+            int d = 0;
+            for (int i = s.t.par[tid]; i >= 0; i = s.t.par[i]) {   // strictly decreasing: ends within n steps
+                m |= 1ull << i;
+                g *= s.t.alpha[i];
+                ++d;
+            }
+            s.t.anc[tid] = m;
+            s.t.g[tid] = g;
+            s.t.ginv[tid] = 1.0f / g;
+            s.t.depth[tid] = d;
+            atomicMax(&s.maxd, d);
+            s.lidx[tid] = (int8_t)atomicAdd(&s.lvl_cnt[d], 1);
+        }
+        __syncthreads();
+        // rows ordered by depth level (rows of different requests share
+        // levels; the order inside a level does not matter): warp 0 scans the
+        // level counts and places the rows while the other warps go on
+        if (warp == 0) {
+            const int maxd = s.maxd;
+            const int c0 = lane <= maxd ? s.lvl_cnt[lane] : 0, c1 = lane + 32 <= maxd ? s.lvl_cnt[lane + 32] : 0;
+            int i0 = c0, i1 = c1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u0 = __shfl_up_sync(0xffffffffu, i0, o), u1 = __shfl_up_sync(0xffffffffu, i1, o);
+                if (lane >= o) {
+                    i0 += u0;
+                    i1 += u1;
                 }
             }
+            i1 += __shfl_sync(0xffffffffu, i0, 31);
+            s.lvl_off[lane] = (int8_t)(i0 - c0);
+            s.lvl_off[lane + 32] = (int8_t)(i1 - c1);
+            if (lane == 0) s.lvl_off[kNR] = (int8_t)n;
+            __syncwarp();
+            for (int j = lane; j < n; j += 32) s.order[s.lvl_off[s.t.depth[j]] + s.lidx[j]] = (int8_t)j;
         }
+
+        // KK = K K^T and QK = Q K^T: warp -> (matrix, two 8-column tiles).  A
+        // tile pair is skipped when no row of it can be an ancestor (or the
+        // row itself) of a row of the other in the same request; those
+        // entries are never read.
+        const __nv_bfloat16 *X = mat ? s.Q : s.K;
+        const int mt_n = n16 / 16;
+        {
+            float *Y = mat ? s.QK : s.KK;
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            if (m < mt_n) {
-                const int r0 = m * 16 + g8, c0 = nt + t4 * 2;
-                Y[r0 * kPS + c0] = acc[m][0];
-                Y[r0 * kPS + c0 + 1] = acc[m][1];
-                Y[(r0 + 8) * kPS + c0] = acc[m][2];
-                Y[(r0 + 8) * kPS + c0 + 1] = acc[m][3];
-            }
-        }
-    }
-    // KK = K K^T and QK = Q K^T (N x N): warp -> (matrix, two 8-column tiles)
-    {
-        const __nv_bfloat16 *X = (warp >> 2) ? s.Q : s.K;
-        float *Y = (warp >> 2) ? s.QK : s.KK;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int nt = ((warp & 3) * 2 + half) * 8;
-            if (nt >= n16) continue;
-            float acc[4][4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[m][e] = 0.f;
-#pragma unroll 2
-            for (int ks = 0; ks < kD; ks += 16) {
-                const __nv_bfloat16 *kr = &s.K[(nt + g8) * kKS + ks + t4 * 2];
-                const uint32_t b0 = *reinterpret_cast<const uint32_t *>(kr);
-                const uint32_t b1 = *reinterpret_cast<const uint32_t *>(kr + 8);
+            for (int half = 0; half < 2; ++half) {
+                const int n0 = ((warp & 3) * 2 + half) * 8;
+                if (n0 >= n16) continue;
+                bool need[4];
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
-                    if (m < mt_n) {
-                        const __nv_bfloat16 *xr = &X[(m * 16 + g8) * kKS + ks + t4 * 2];
-                        uint32_t a[4];
-                        a[0] = *reinterpret_cast<const uint32_t *>(xr);
-                        a[1] = *reinterpret_cast<const uint32_t *>(xr + 8 * kKS);
-                        a[2] = *reinterpret_cast<const uint32_t *>(xr + 8);
-                        a[3] = *reinterpret_cast<const uint32_t *>(xr + 8 * kKS + 8);
-                        mma_bf16(acc[m], a, b0, b1);
+                    const int m0 = m * 16, m1 = m0 + 16;
+                    // rows i in [n0, n0 + 8) and j in [m0, m1), i <= j, one request:
+                    // overlapping ranges, or the request of row m0 starts before n0 + 8
+                    const int rs_m0 = 63 - __clzll((long long)(starts & (~0ull >> (63 - m0))));
+                    need[m] = m < mt_n && n0 < m1 && (n0 + 8 > m0 || rs_m0 < n0 + 8);
+                }
+                float acc[4][4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[m][e] = 0.f;
+#pragma unroll 2
+                for (int ks = 0; ks < kD; ks += 16) {
+                    const uint2 b = *reinterpret_cast<const uint2 *>(&s.K[(n0 + g8) * kKS + ks + t4 * 4]);
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        if (need[m]) {
+                            uint32_t af[4];
+                            mma_a(X, m * 16 + g8, ks + t4 * 4, af);
+                            mma_bf16(acc[m], af, b.x, b.y);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    if (need[m]) {
+                        const int r0 = m * 16 + g8, c0 = n0 + t4 * 2;
+                        Y[r0 * kMS + c0] = acc[m][0];
+                        Y[r0 * kMS + c0 + 1] = acc[m][1];
+                        Y[(r0 + 8) * kMS + c0] = acc[m][2];
+                        Y[(r0 + 8) * kMS + c0 + 1] = acc[m][3];
                     }
                 }
             }
+        }
+
+        // state products, request by request: P = K S^T folded at once into
+        // B = b (v - g P), and Rq = Q S^T.  Warp -> (matrix, 8-column tile);
+        // two accumulators per 16-row tile (even and odd k steps).
+        {
+            unsigned long long m = starts;
+            while (m) {
+                const int st = __ffsll((long long)m) - 1;
+                m &= m - 1;
+                const int en = m ? __ffsll((long long)m) - 1 : n;
+                const float *nrow = m ? state_rows(p, s.rq[en], h, vs + nt + g8) + 4 * t4 : nullptr;
+                const int t0 = st >> 4, t1 = (en - 1) >> 4;
+                float acc[4][2][4];
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                if (m < mt_n) {
-                    const int r0 = m * 16 + g8, c0 = nt + t4 * 2;
-                    Y[r0 * kMS + c0] = acc[m][0];
-                    Y[r0 * kMS + c0 + 1] = acc[m][1];
-                    Y[(r0 + 8) * kMS + c0] = acc[m][2];
-                    Y[(r0 + 8) * kMS + c0 + 1] = acc[m][3];
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int q = 0; q < 2; ++q)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[u][q][e] = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < kD / 16; ++ks) {
+                    uint32_t bh0, bm0, bl0, bh1, bm1, bl1;
+                    split3(sf[ks].x, sf[ks].y, bh0, bm0, bl0);
+                    split3(sf[ks].z, sf[ks].w, bh1, bm1, bl1);
+                    if (nrow) sf[ks] = *reinterpret_cast<const float4 *>(nrow + 16 * ks);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        if (t0 + u <= t1) {
+                            uint32_t af[4];
+                            mma_a(X, (t0 + u) * 16 + g8, 16 * ks + t4 * 4, af);
+                            mma_bf16(acc[u][ks & 1], af, bl0, bl1);
+                            mma_bf16(acc[u][ks & 1], af, bm0, bm1);
+                            mma_bf16(acc[u][ks & 1], af, bh0, bh1);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (t0 + u <= t1) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = (t0 + u) * 16 + g8 + (e >> 1) * 8, c = nt + t4 * 2 + (e & 1);
+                            if (j >= st && j < en) {
+                                const float y = acc[u][0][e] + acc[u][1][e];
+                                if (mat)
+                                    s.Rq[j * kPS + c] = y;
+                                else
+                                    s.P[j * kPS + c] = s.t.beta[j] * (s.V[j * kPS + c] - s.t.g[j] * y);
+                            }
+                        }
+                    }
                 }
             }
         }
-    }
-    __syncthreads();
+        __syncthreads();
 
-    // the value slice moves into the state slice's space, no longer read
-    float *Vf = s.S;
-#pragma unroll
-    for (int i = 0; i < kNR * 16 / kThreads; ++i) {
-        const int e = tid + i * kThreads, j = e >> 4;
-        if (j < n) {
-            Vf[j * kPS + (e & 15) * 2] = __uint_as_float(vv[i] << 16);
-            Vf[j * kPS + (e & 15) * 2 + 1] = __uint_as_float(vv[i] & 0xffff0000u);
-        }
-    }
-    __syncthreads();
-    // forward substitution by depth level: U[j] = B[j] - b_j g_j sum_anc (k_i.k_j / g_i) U[i]
-    const int c = tid & 31, slot = tid >> 5;
-    const int n_lvl = s.maxd + 1;
-    for (int L = 0; L < n_lvl; ++L) {
-        const int lo = s.lvl_off[L], hi = s.lvl_off[L + 1];
-        for (int t = lo + slot; t < hi; t += kThreads / 32) {
-            const int j = s.order[t];
-            float sum = 0.f;
-            unsigned long long m = s.t.anc[j];
-            while (m) {
-                const int i = __ffsll((long long)m) - 1;
-                m &= m - 1;
-                sum = fmaf(s.KK[j * kMS + i] * s.t.ginv[i], s.U[i * kPS + c], sum);
+        // forward substitution by depth level: U[j] = B[j] - b_j g_j sum_anc (k_i.k_j / g_i) U[i]
+        const int c = tid & 31, slot = tid >> 5;
+        const int n_lvl = s.maxd + 1;
+        for (int L = 0; L < n_lvl; ++L) {
+            const int lo = s.lvl_off[L], hi = s.lvl_off[L + 1];
+            for (int t = lo + slot; t < hi; t += kThreads / 32) {
+                const int j = s.order[t];
+                float sum = 0.f;
+                unsigned long long am = s.t.anc[j];
+                while (am) {
+                    const int i = __ffsll((long long)am) - 1;
+                    am &= am - 1;
+                    sum = fmaf(s.KK[j * kMS + i] * s.t.ginv[i], s.U[i * kPS + c], sum);
+                }
+                s.U[j * kPS + c] = s.P[j * kPS + c] - s.t.beta[j] * s.t.g[j] * sum;
             }
-            const float bj = s.t.beta[j], gj = s.t.g[j];
-            const float B = bj * (Vf[j * kPS + c] - gj * s.P[j * kPS + c]);
-            s.U[j * kPS + c] = B - bj * gj * sum;
+            __syncthreads();
+        }
+        // outputs: o_j = g_j (S0 q_j + sum over the path (k_i.q_j / g_i) u_i)
+        for (int j = slot; j < n; j += kThreads / 32) {
+            float sum = s.Rq[j * kPS + c];
+            unsigned long long am = s.t.anc[j] | (1ull << j);
+            while (am) {
+                const int i = __ffsll((long long)am) - 1;
+                am &= am - 1;
+                sum = fmaf(s.QK[j * kMS + i] * s.t.ginv[i], s.U[i * kPS + c], sum);
+            }
+            p.out[((size_t)(a + j) * H + h) * kD + vs + c] = s.t.g[j] * sum;
+        }
+        a += n;
+        __syncthreads();   // the next pack reuses every buffer
+    }
+}
+
+// ---------------------------------------------------------------------------
+// WY form for several requests: tensor memory
+// ---------------------------------------------------------------------------
+//
+// Grid (window, head), one CTA per SM.  A CTA owns the requests whose first
+// row lies in its window of p.win rows and takes them in packs: runs of at
+// most kPackReqs whole requests spanning at most 64 rows.  At a pack's start
+// the tree data of its rows is built (ancestor sets, cumulative gates), the
+// key and query rows go to shared memory as BF16 blocks, one per request (its
+// keys, its queries, zero rows up to a multiple of 16), and every request's
+// state S0[r][h] is sent towards L2.
+//
+// Two warp roles then run the pack's requests as a pipeline:
+//  * splitters (warps 8..11, one state row each: TMEM lane = state row c,
+//    columns = features): the request's state arrives in shared memory by
+//    TMA (sixteen 32 x 32 FP32 boxes, 128-byte swizzle, so that every thread
+//    reads its own row without bank conflicts); once read, the next
+//    request's copy starts.  Once the tensor cores have released the A
+//    columns, the splitters write the state as three exact BF16 pieces into
+//    tensor memory (A of the state products), the threads of the first 2n
+//    lanes also the request's key and query rows (A of k.k and q.k); one
+//    thread issues the MMAs (M = 128, N = the request's block rows):
+//        D [c][  j ] = S0 k_j  and  D [c][n + j] = S0 q_j   (3 pieces x 8 k steps)
+//        D2[j][  i ] = k_j.k_i and  D2[n + j][i] = q_j.k_i  (8 k steps);
+//  * solvers (warps 0..7, two threads per state row c): copy D and D2 out of
+//    tensor memory (which frees them for the next request), then take the
+//    request's rows by depth, a group of rows of one depth at a time (none is
+//    an ancestor of another), half of each group per thread, for their own
+//    column:  u_j = b_j (v_j - g_j S0 k_j) - sum over the ancestors (b_j g_j
+//    k_i.k_j / g_i) u_i,  o_j = g_j S0 q_j + sum over the path (g_j k_i.q_j / g_i) u_i,
+//    one pass over the ancestors for both sums.
+
+constexpr int kWyThreads = 384;
+constexpr int kSolvers = 256;       // warps 0..7: two per quarter of the state rows
+constexpr int kSplitters = 128;     // warps 8..11: one state row per thread
+constexpr int kPackReqs = 8;        // requests per pack: bounds the blocks' zero padding
+constexpr int kXRows = 248;         // block rows: at most 2 * 64 + 14 * kPackReqs
+constexpr uint32_t kStageBytes = kD * kD * sizeof(float);   // one request's state (one head)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColPiece = 0;   // S0 as three BF16 pieces, 64 columns each
+constexpr uint32_t kColX = 192;     // the request's key and query rows
+constexpr uint32_t kColD = 256;     // state products, up to 128 columns
+constexpr uint32_t kColD2 = 384;    // k.k and q.k, up to 64 columns
+constexpr int kBarSplit = 1, kBarSolve = 2;   // named barriers of the two roles
+constexpr int kTri = kNR * (kNR + 1) / 2;     // entries (j, i), i <= j, of an N x N lower triangle
+
+__device__ __forceinline__ int tri(int j, int i) { return j * (j + 1) / 2 + i; }
+
+struct WyShared {
+    uint8_t stage[kStageBytes];   // the state being split: box (row quarter, feature quarter) = 32 rows x 128 B
+    uint8_t X[2][kXRows * 128];   // key/query blocks, BF16, K-major, 128-byte swizzle: [feature half][row][64]
+    float PU[kNR * kD];           // S0 k, replaced row by row by u: [pack row][state row]
+    float Rq[kNR * kD];           // S0 q
+    float KK[kTri], QK[kTri];     // b_j g_j k_i.k_j / g_i and g_j q_j.k_i / g_i of the current request (lower triangles)
+    uint16_t V[kNR * kD];         // value rows (BF16): [pack row][state row]
+    TreeInfo t;
+    unsigned long long starts;    // bit i: a request of the pack starts at pack row i
+    int32_t rq[kNR];              // the request starting at pack row i
+    int32_t blk[kNR];             // its block's first row
+    int8_t order[kNR];            // each request's rows by depth (a request's entries start at its first row)
+    int8_t run[kNR];              // entries from this one on with its depth, in its request (at most 8)
+    int32_t pack_end;
+    uint32_t tmem;
+    int32_t abort;
+    unsigned long long bar_mma;   // the request's MMAs are done
+    unsigned long long bar_dfree; // the solvers have copied D and D2 out
+    unsigned long long bar_stage; // the request's state is in shared memory
+};
+
+static_assert(sizeof(WyShared) + 1024 <= 227 * 1024, "WY shared memory above the per-CTA limit");
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+__device__ __forceinline__ bool elect_lane()
+{
+    uint32_t e;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
+    return e != 0;
+}
+
+// 32 lanes x 16 columns of 32 bits: register j of lane i <- TMEM (lane base + i, col + j)
+__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// named barrier `id` over `threads` threads that also ANDs `v` across them
+__device__ __forceinline__ bool bar_all(int id, int threads, bool v)
+{
+    uint32_t out;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(out)
+                 : "r"((uint32_t)v), "r"(id), "r"(threads)
+                 : "memory");
+    return out != 0;
+}
+
+// byte offset of 16-byte piece `chunk` (features 8 chunk .. 8 chunk + 7 of
+// the half) of block row `row` in one feature half of X
+__device__ __forceinline__ uint32_t x_off(int row, int chunk) { return row * 128 + ((chunk ^ (row & 7)) << 4); }
+
+__device__ __forceinline__ const float *state_of(const GdnParams &p, int r, int h)
+{
+    return p.S0 + ((size_t)r * p.H + h) * kD * kD;
+}
+
+__global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy(const __grid_constant__ CUtensorMap smap, const GdnParams p)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    WyShared &s = *reinterpret_cast<WyShared *>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
+    const int h = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int H = p.H;
+    const int w0 = blockIdx.x * p.win, w1 = w0 + p.win;
+
+    // the requests whose first row lies in [w0, w1): [r_lo, r_hi).  Every CTA
+    // checks every request's row range first, so all of them agree on the
+    // requests' places (or all stop).
+    int r_lo = 0, r_hi = 0, bad = 0;
+    for (int base = 0; base < p.n_req; base += kWyThreads) {
+        const int r = base + tid;
+        int lo = 0, hi = 0;
+        if (r < p.n_req) {
+            const int o0 = p.req_row_off[r], o1 = p.req_row_off[r + 1];
+            const int code = (o1 - o0 < 0 || o1 - o0 > kNR) ? (int)W12_E_UNSUPPORTED
+                             : (o0 < 0 || o1 > p.R)         ? (int)W12_E_INVAL
+                                                            : 0;
+            if (code) {
+                atomicCAS(p.status, 0, code);
+                bad = 1;
+            }
+            lo = o0 < w0;
+            hi = o0 < w1;
+        }
+        r_lo += __syncthreads_count(lo);
+        r_hi += __syncthreads_count(hi);
+    }
+    if (__syncthreads_or(bad) || r_lo >= r_hi) return;
+
+    const uint32_t bar_mma = smem_u32(&s.bar_mma), bar_dfree = smem_u32(&s.bar_dfree);
+    const uint32_t bar_stage = smem_u32(&s.bar_stage), stage = smem_u32(s.stage);
+    if (tid == 0) {
+        mbar_init(bar_mma, 1);
+        mbar_init(bar_dfree, kSolvers / 32);   // one arrival per solver warp
+        mbar_init(bar_stage, 1);
+        prefetch_tmap(&smap);
+        s.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(smem_u32(&s.tmem), kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s.tmem;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;   // this warp's TMEM lane quarter
+    const uint32_t x0 = smem_u32(s.X[0]), x1 = smem_u32(s.X[1]);
+    const bool splitter = warp >= 8;
+    const int c = (warp & 3) * 32 + lane;           // state row: TMEM lane
+    const int hs = (warp >> 2) & 1;                 // a solver's half of the work on its row
+    // request r's state (head h) into the stage: sixteen 32 x 32 boxes
+    auto stage_state = [&](int r) {
+        mbar_expect_tx(bar_stage, kStageBytes);
+        const int row0 = (r * H + h) * kD;
+#pragma unroll
+        for (int b = 0; b < 16; ++b)
+            tma_load_2d(stage + b * 4096, &smap, (b & 3) * 32, row0 + (b >> 2) * 32, bar_stage);
+    };
+    uint32_t rc = 0;                                // requests taken so far (barrier phases)
+    uint32_t n_staged = 0;                          // thread kSolvers: state copies issued
+    bool go = true;
+    bool issue_ok = true;                           // warp 8: the last MMA issue went ahead
+
+    int a = p.req_row_off[r_lo];
+    const int row_end = p.req_row_off[r_hi];
+    while (a < row_end && go) {
+        // reads that need only the pack's first row, issued before the pack is
+        // known (all in bounds; rows past the pack are never used): the rows'
+        // parents, gates and strengths, and the value rows
+        int pr = -1;
+        float al = 0.f, be = 0.f;
+        const int rows_avail = min(kNR, p.R - a);
+        if (tid < rows_avail) {
+            pr = p.parent[a + tid];
+            al = p.alpha[(size_t)(a + tid) * H + h];
+            be = p.beta[(size_t)(a + tid) * H + h];
+        }
+        for (int e = tid; e < rows_avail * 16; e += kWyThreads) {
+            const int j = e >> 4, ch = e & 15;
+            cp_async16(smem_u32(&s.V[j * kD + ch * 8]), p.v + ((size_t)(a + j) * H + h) * kD + ch * 8);
+        }
+        // this pack: up to kPackReqs requests that start at or after row a and end by a + 64
+        if (tid == 0) {
+            s.pack_end = a;
+            s.starts = 0ull;
         }
         __syncthreads();
-    }
-    // outputs: o_j = g_j (S0 q_j + sum over the path (k_i.q_j / g_i) u_i)
-    for (int j = slot; j < n; j += kThreads / 32) {
-        float sum = s.Rq[j * kPS + c];
-        unsigned long long m = s.t.anc[j] | (1ull << j);
-        while (m) {
-            const int i = __ffsll((long long)m) - 1;
-            m &= m - 1;
-            sum = fmaf(s.QK[j * kMS + i] * s.t.ginv[i], s.U[i * kPS + c], sum);
+        for (int r = r_lo + tid; r < r_hi; r += kWyThreads) {
+            const int o0 = p.req_row_off[r], o1 = p.req_row_off[r + 1];
+            if (o0 >= a && o1 <= a + kNR && o1 > o0) {
+                atomicOr(&s.starts, 1ull << (o0 - a));
+                s.rq[o0 - a] = r;
+                s.blk[o0 - a] = o1 - o0;   // rows, for the block offsets below
+            }
         }
-        p.out[((size_t)(row0 + j) * H + h) * kD + vs + c] = s.t.g[j] * sum;
+        __syncthreads();
+        if (tid == 0) {
+            unsigned long long m = s.starts;
+            int blk = 0, end = 0;
+            for (int q = 0; q < kPackReqs && m; ++q) {
+                const int st = __ffsll((long long)m) - 1;
+                m &= m - 1;
+                const int rows = s.blk[st];
+                s.blk[st] = blk;
+                blk += (2 * rows + 15) & ~15;
+                end = st + rows;
+            }
+            if (m) s.starts &= (1ull << (__ffsll((long long)m) - 1)) - 1;   // the rest goes to the next pack
+            s.pack_end = a + end;
+        }
+        __syncthreads();
+        const int n = s.pack_end - a;
+        const unsigned long long starts = s.starts;
+        if (tid == kSolvers) {   // the first request's state
+            stage_state(s.rq[0]);
+            ++n_staged;
+        }
+
+        // the rest of the pack's reads: the key / query blocks (asynchronous
+        // copies into shared memory) and every other request's state towards L2
+        {
+            unsigned long long m = starts;
+            while (m) {
+                const int st = __ffsll((long long)m) - 1;
+                m &= m - 1;
+                const int en = m ? __ffsll((long long)m) - 1 : n, nr = en - st;
+                const int blk = s.blk[st], brows = (2 * nr + 15) & ~15;
+                for (int e = tid; e < brows * 16; e += kWyThreads) {
+                    const int q = e >> 4, ch = e & 15, row = blk + q;
+                    if (q < 2 * nr) {
+                        const uint16_t *src = (q < nr ? p.k + ((size_t)(a + st + q) * H + h) * kD
+                                                      : p.q + ((size_t)(a + st + q - nr) * H + h) * kD) + ch * 8;
+                        cp_async16((ch < 8 ? x0 : x1) + x_off(row, ch & 7), src);
+                    } else {
+                        *reinterpret_cast<uint4 *>(&s.X[ch >> 3][x_off(row, ch & 7)]) = make_uint4(0, 0, 0, 0);
+                    }
+                }
+            }
+        }
+        if (tid < n) {
+            // parents: inside the row's own request and before the row, else
+            // W12_E_INVAL and the row becomes a root
+            const int rs = 63 - __clzll((long long)(starts & (~0ull >> (63 - tid))));   // the request's first row
+            int pl = pr < 0 ? -1 : pr - a;
+            if (pr >= 0 && (pl < rs || pl >= tid)) {
+                atomicCAS(p.status, 0, (int32_t)W12_E_INVAL);
+                pl = -1;
+            }
+            s.t.par[tid] = pl;
+            s.t.alpha[tid] = al;
+            s.t.beta[tid] = be;
+        }
+        {
+            unsigned long long m = starts;
+            for (int q = 0; m; ++q) {   // four threads per request, a quarter of its state each
+                const int st = __ffsll((long long)m) - 1;
+                m &= m - 1;
+                if (q > 0 && q == (tid >> 2))
+                    prefetch_l2(state_of(p, s.rq[st], h) + (tid & 3) * (kD * kD / 4), kD * kD / 4 * sizeof(float));
+            }
+        }
+        __syncthreads();
+        // ancestor sets and cumulative gates
+        if (tid < n) {
+            unsigned long long m = 0ull;
+            float g = s.t.alpha[tid];
+            for (int i = s.t.par[tid]; i >= 0; i = s.t.par[i]) {   // strictly decreasing: ends within n steps
+                m |= 1ull << i;
+                g *= s.t.alpha[i];
+            }
+            s.t.anc[tid] = m;
+            s.t.g[tid] = g;
+            s.t.ginv[tid] = 1.0f / g;
+            s.t.depth[tid] = __popcll(m);
+        }
+        __syncthreads();
+        // each request's rows ordered by depth, then by row
+        if (tid < n) {
+            const unsigned long long below = starts & (~0ull >> (63 - tid));
+            const unsigned long long above = starts & ~below;
+            const int rs = 63 - __clzll((long long)below), re = above ? __ffsll((long long)above) - 1 : n;
+            const int dj = s.t.depth[tid];
+            int pos = rs;
+            for (int i = rs; i < re; ++i) {
+                const int di = s.t.depth[i];
+                pos += (di < dj) || (di == dj && i < tid);
+            }
+            s.order[pos] = (int8_t)tid;
+            // the run of entries with this depth from position pos on
+            int later = 0;
+            for (int i = rs; i < re; ++i) later += s.t.depth[i] == dj && i > tid;
+            s.run[pos] = (int8_t)min(later + 1, 8);
+        }
+        cp_async_wait_all();
+        __syncthreads();
+
+        unsigned long long m = starts;
+        if (splitter) {
+            // ------------------------------------------------------------ splitters
+            while (m && go) {
+                const int st = __ffsll((long long)m) - 1;
+                m &= m - 1;
+                const int en = m ? __ffsll((long long)m) - 1 : n, nr = en - st;
+                const int blk = s.blk[st];
+                // the state is staged and the previous request's MMAs have read
+                // the A columns: warp 8 polls, the other splitters wait in the
+                // barrier (every splitter decides alike: a stop anywhere stops
+                // them all here)
+                bool ok = issue_ok;
+                if (warp == 8) {
+                    if (rc > 0) ok = ok && mbar_wait(bar_mma, (rc - 1) & 1u, p.timeout_ns, p.status, &s.abort);
+                    ok = ok && mbar_wait(bar_stage, rc & 1u, p.timeout_ns, p.status, &s.abort);
+                    ok = __all_sync(0xffffffffu, ok);
+                }
+                if (!bar_all(kBarSplit, kSplitters, ok)) {
+                    go = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t w[32];
+#pragma unroll 1
+                for (int kh = 0; kh < 2; ++kh) {
+                    // features [64 kh, 64 kh + 64) of state row c: feature quarters 2 kh, 2 kh + 1
+                    float4 sv[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const uint32_t box = (uint32_t)((warp & 3) * 4 + 2 * kh + (i >> 3)) * 4096u;
+                        sv[i] = *reinterpret_cast<const float4 *>(s.stage + box + lane * 128 + (((i & 7) ^ (lane & 7)) << 4));
+                    }
+#pragma unroll
+                    for (int piece = 0; piece < 3; ++piece) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const uint32_t b0 = __float_as_uint(sv[i].x), b1 = __float_as_uint(sv[i].y);
+                            const uint32_t b2 = __float_as_uint(sv[i].z), b3 = __float_as_uint(sv[i].w);
+                            w[2 * i] = __byte_perm(b0, b1, 0x7632);
+                            w[2 * i + 1] = __byte_perm(b2, b3, 0x7632);
+                            if (piece < 2) {   // the remainder after this piece (exact), two at a time
+                                const float2 m1 = make_float2(-1.f, -1.f);
+                                const float2 lo = __ffma2_rn(make_float2(__uint_as_float(b0 & 0xffff0000u),
+                                                                         __uint_as_float(b1 & 0xffff0000u)),
+                                                             m1, make_float2(sv[i].x, sv[i].y));
+                                const float2 hi = __ffma2_rn(make_float2(__uint_as_float(b2 & 0xffff0000u),
+                                                                         __uint_as_float(b3 & 0xffff0000u)),
+                                                             m1, make_float2(sv[i].z, sv[i].w));
+                                sv[i] = make_float4(lo.x, lo.y, hi.x, hi.y);
+                            }
+                        }
+                        // (the source registers are read at issue: one completion wait below)
+                        tmem_st_x32(tmem + lane_base + kColPiece + 64 * piece + 32 * kh, w);
+                    }
+                    // the request's key and query rows (lanes below 2 nr; the
+                    // other lanes of those warps copy a valid row, never read)
+                    if ((warp & 3) * 32 < 2 * nr) {
+                        const int row = blk + min(c, 2 * nr - 1);
+                        const uint8_t *xs = s.X[kh];
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch) {
+                            const uint4 v = *reinterpret_cast<const uint4 *>(xs + x_off(row, ch));
+                            w[4 * ch] = v.x;
+                            w[4 * ch + 1] = v.y;
+                            w[4 * ch + 2] = v.z;
+                            w[4 * ch + 3] = v.w;
+                        }
+                        tmem_st_x32(tmem + lane_base + kColX + 32 * kh, w);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                named_bar(kBarSplit, kSplitters);   // the stage is read, the A columns written
+                if (tid == kSolvers && m) {   // the next request's state (this thread issues every copy)
+                    stage_state(s.rq[en]);
+                    ++n_staged;
+                }
+                if (warp == 8) {
+                    // the solvers have copied the previous request's D and D2 out
+                    bool ok = rc == 0 || mbar_wait(bar_dfree, (rc - 1) & 1u, p.timeout_ns, p.status, &s.abort);
+                    ok = __all_sync(0xffffffffu, ok);
+                    tc_fence_after();
+                    if (ok && elect_lane()) {
+                        const uint32_t N = (2 * nr + 15) & ~15, N2 = (nr + 15) & ~15;
+                        const uint32_t id = idesc_bf16_f32(128, N), id2 = idesc_bf16_f32(128, N2);
+                        const uint64_t b0 = smem_desc_sw128(x0 + blk * 128), b1 = smem_desc_sw128(x1 + blk * 128);
+#pragma unroll
+                        for (int piece = 0; piece < 3; ++piece)
+#pragma unroll
+                            for (int ks = 0; ks < 8; ++ks)
+                                tc_mma_ts(tmem + kColD, tmem + kColPiece + 64 * piece + 8 * ks,
+                                          (ks < 4 ? b0 : b1) + (uint64_t)((ks & 3) * 2), id, (piece | ks) ? 1u : 0u);
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            tc_mma_ts(tmem + kColD2, tmem + kColX + 8 * ks,
+                                      (ks < 4 ? b0 : b1) + (uint64_t)((ks & 3) * 2), id2, ks ? 1u : 0u);
+                        tc_commit(bar_mma);
+                    }
+                    __syncwarp();
+                    if (!ok) {
+                        issue_ok = false;   // the other splitters see it at their next vote,
+                        s.abort = 1;        // the solvers' waits end at once
+                    }
+                }
+                ++rc;
+            }
+        } else {
+            // -------------------------------------------------------------- solvers
+            while (m && go) {
+                const int st = __ffsll((long long)m) - 1;
+                m &= m - 1;
+                const int en = m ? __ffsll((long long)m) - 1 : n, nr = en - st;
+                // the MMAs are done: warp 0 polls, the other solvers wait in the barrier
+                bool ok = true;
+                if (warp == 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_mma, rc & 1u, p.timeout_ns, p.status, &s.abort));
+                if (!bar_all(kBarSolve, kSolvers, ok)) {
+                    go = false;
+                    break;
+                }
+                tc_fence_after();
+                // D -> S0 k and S0 q rows; D2 -> the scaled k.k and q.k rows.  The
+                // two warps of a lane quarter take alternate 16-column chunks.
+                const bool d2 = (warp & 3) * 32 < 2 * nr;   // this warp's lanes hold rows of D2
+                for (int c0 = 16 * hs; c0 < 2 * nr; c0 += 32) {
+                    uint32_t v[16], v2[16];
+                    tmem_ld_x16(tmem + lane_base + kColD + c0, v);
+                    if (d2 && c0 < nr) tmem_ld_x16(tmem + lane_base + kColD2 + c0, v2);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int col = c0 + i;
+                        if (col < nr)
+                            s.PU[(st + col) * kD + c] = __uint_as_float(v[i]);
+                        else if (col < 2 * nr)
+                            s.Rq[(st + col - nr) * kD + c] = __uint_as_float(v[i]);
+                    }
+                    if (d2 && c0 < nr && c < 2 * nr) {
+                        const int jj = c < nr ? c : c - nr, j = st + jj;
+                        const float f = c < nr ? s.t.beta[j] * s.t.g[j] : s.t.g[j];
+                        float *dst = c < nr ? s.KK : s.QK;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (c0 + i <= jj) dst[tri(jj, c0 + i)] = __uint_as_float(v2[i]) * s.t.ginv[st + c0 + i] * f;
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_dfree);   // D, D2 free for the next request's MMAs
+                ++rc;
+                named_bar(kBarSolve, kSolvers);
+                // rows by depth, up to eight rows of one depth at a time (none is
+                // an ancestor of another, and all have `depth` ancestors), four of
+                // them per thread: one pass over the ancestors for u_j and o_j
+                for (int t = st; t < en;) {
+                    const int d = s.t.depth[s.order[t]], gsz = s.run[t];
+                    const int mine = (gsz - hs + 1) >> 1;   // entries hs, hs + 2, ... of the group
+                    if (mine > 0) {
+                        int jr[4], tb[4];
+                        float u[4], o[4];
+                        unsigned long long am[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int j = s.order[t + hs + 2 * min(k, mine - 1)];   // the last one again past the end
+                            jr[k] = j;
+                            tb[k] = tri(j - st, 0) - st;                          // entry (j, i) at index tb + i
+                            const float vj = __uint_as_float((uint32_t)s.V[j * kD + c] << 16);
+                            u[k] = s.t.beta[j] * (vj - s.t.g[j] * s.PU[j * kD + c]);
+                            o[k] = s.t.g[j] * s.Rq[j * kD + c];
+                            am[k] = s.t.anc[j];
+                        }
+                        for (int step = 0; step < d; ++step) {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const int i = __ffsll((long long)am[k]) - 1;
+                                am[k] &= am[k] - 1;
+                                const float ui = s.PU[i * kD + c];
+                                u[k] = fmaf(-s.KK[tb[k] + i], ui, u[k]);
+                                o[k] = fmaf(s.QK[tb[k] + i], ui, o[k]);
+                            }
+                        }
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            if (k < mine) {
+                                s.PU[jr[k] * kD + c] = u[k];
+                                p.out[((size_t)(a + jr[k]) * H + h) * kD + c] = fmaf(s.QK[tb[k] + jr[k]], u[k], o[k]);
+                            }
+                        }
+                    }
+                    t += gsz;
+                    named_bar(kBarSolve, kSolvers);   // the next depth reads this group's u
+                }
+            }
+        }
+        if (__syncthreads_or(!go)) go = false;   // the pack is done (or stopped) on both sides
+        a += n;
     }
+
+    // release tensor memory once no MMA is in flight and leave no copy into
+    // shared memory running: after a stop, one more bounded wait for the last
+    // commit and the last state copy
+    if (!go && rc > 0) {
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(bar_mma, (rc - 1) & 1u) && globaltimer() - t0 < p.timeout_ns) {
+        }
+    }
+    if (!go && tid == kSolvers && n_staged > 0) {
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(bar_stage, (n_staged - 1) & 1u) && globaltimer() - t0 < p.timeout_ns) {
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ---------------------------------------------------------------------------
@@ -404,7 +1083,7 @@ __device__ __forceinline__ void walk(const PathShared &s, unsigned long long pat
 template <bool kCommit>
 __global__ void __launch_bounds__(kThreads, 1) k_gdn_path(const GdnParams p)
 {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     PathShared &s = *reinterpret_cast<PathShared *>(smem_raw);
     const int r = blockIdx.x, h = blockIdx.y, vs = blockIdx.z * kVS;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -471,16 +1150,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_gdn_path(const GdnParams p)
     }
 }
 
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn_gdn()
+{
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
 }  // namespace
 
 namespace w12i {
 
 int launch_gdn(const GdnArgs &a, int mode, void *stream)
 {
-    if (a.H < 1 || a.n_req < 1) return (int)cudaErrorInvalidValue;
+    if (a.H < 1 || a.n_req < 1 || a.R < 1) return (int)cudaErrorInvalidValue;
     GdnParams p{};
     p.H = a.H;
     p.n_req = a.n_req;
+    p.R = a.R;
+    p.timeout_ns = a.timeout_ns;
     p.S0 = a.S0;
     p.q = a.q;
     p.k = a.k;
@@ -499,12 +1199,37 @@ int launch_gdn(const GdnArgs &a, int mode, void *stream)
     cfg.gridDim = dim3(a.n_req, a.H, kD / kVS);
     cfg.blockDim = dim3(kThreads);
     cfg.stream = static_cast<cudaStream_t>(stream);
+    if (mode == kGdnWy && a.n_req == 1) {
+        // one request: (window, head, 32-row slice) CTAs, two per SM
+        cfg.gridDim = dim3((a.R + kSliceWin - 1) / kSliceWin, a.H, kD / kVS);
+        cfg.dynamicSmemBytes = sizeof(SliceShared);
+        cudaError_t e = cudaFuncSetAttribute(k_gdn_wy_slice, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)cfg.dynamicSmemBytes);
+        if (e != cudaSuccess) return (int)e;
+        return (int)cudaLaunchKernelEx(&cfg, k_gdn_wy_slice, p);
+    }
     if (mode == kGdnWy) {
-        cfg.dynamicSmemBytes = sizeof(WyShared);
+        // several requests: windows sized so that the (window, head) CTAs fit one wave
+        const int wins = std::max(1, a.num_sms / a.H);
+        p.win = (a.R + wins - 1) / wins;
+        cfg.gridDim = dim3((a.R + p.win - 1) / p.win, a.H);
+        cfg.blockDim = dim3(kWyThreads);
+        cfg.dynamicSmemBytes = sizeof(WyShared) + 1024;
+        // the states as rows of 128 FP32 features, copied in 32 x 32 boxes
+        EncodeTiledFn enc = encode_fn_gdn();
+        if (!enc) return (int)cudaErrorNotSupported;
+        CUtensorMap smap;
+        const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)a.n_req * a.H * kD};
+        const cuuint64_t strides[1] = {(cuuint64_t)kD * sizeof(float)};
+        const cuuint32_t box[2] = {32, 32}, estr[2] = {1, 1};
+        if (enc(&smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(a.S0), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return (int)cudaErrorInvalidValue;
         cudaError_t e = cudaFuncSetAttribute(k_gdn_wy, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)cfg.dynamicSmemBytes);
         if (e != cudaSuccess) return (int)e;
-        return (int)cudaLaunchKernelEx(&cfg, k_gdn_wy, p);
+        return (int)cudaLaunchKernelEx(&cfg, k_gdn_wy, smap, p);
     }
     cfg.dynamicSmemBytes = sizeof(PathShared);
     const auto kern = mode == kGdnCommit ? k_gdn_path<true> : k_gdn_path<false>;

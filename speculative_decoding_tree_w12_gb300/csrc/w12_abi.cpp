@@ -698,6 +698,9 @@ w12_status gdn_args(const w12_gdn_layer *L, const w12_tree *tree, int32_t n_req,
     a = GdnArgs{};
     a.H = L->n_heads;
     a.n_req = n_req;
+    a.R = tree->R;
+    a.num_sms = num_sms();
+    a.timeout_ns = g_timeout_ns;
     a.S0 = L->S0;
     a.q = L->q;
     a.k = L->k;

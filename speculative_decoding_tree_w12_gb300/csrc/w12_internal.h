@@ -144,7 +144,9 @@ constexpr int kGdnWy = 0, kGdnPath = 1, kGdnCommit = 2;
 constexpr int kGdnDim = 128;        // head dimension
 constexpr int kGdnMaxRows = 64;     // tree rows of one request
 struct GdnArgs {
-    int32_t H, n_req;
+    int32_t H, n_req, R;
+    int num_sms;             // SMs of the device (sizes the WY kernel's grid)
+    uint64_t timeout_ns;     // bounded waits of the WY kernel
     const float *S0;
     const uint16_t *q, *k, *v;
     const float *alpha, *beta;

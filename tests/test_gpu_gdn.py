@@ -117,3 +117,71 @@ def test_gdn_flags_a_request_over_64_rows(w12):
     w12.w12_gdn_tree_verify(layer, tree, w.n_req, ws, w12.W12_GDN_PATH)
     torch.cuda.synchronize()
     assert ws.status() == w12.W12_E_UNSUPPORTED
+
+
+def _hand_tree(w12, sizes, seed, extra_root=0.1):
+    """A tree with the given rows per request (zero allowed): each request's
+    first row is a root, every later row hangs under a random earlier row of
+    its request or, with probability extra_root, is one more root."""
+    g = np.random.default_rng(seed)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    R = int(off[-1])
+    parent = np.full(R, -1, np.int32)
+    req = np.empty(R, np.int32)
+    for r, n in enumerate(sizes):
+        o = int(off[r])
+        req[o:o + n] = r
+        for j in range(1, n):
+            parent[o + j] = -1 if g.random() < extra_root else o + int(g.integers(0, j))
+    z = np.zeros(R, np.int32)
+    t = oracle.Tree(R, parent, z, z.astype(np.uint8), req, z.astype(np.float32), z.astype(np.uint8), off)
+    dt = w12.DeviceTree(max(R, 1), len(sizes))
+    dt.parent[:R] = torch.from_numpy(parent).cuda()
+    dt.req_row_off.copy_(torch.from_numpy(off))
+    dt.c.R = R
+    return t, dt
+
+
+PACKS = [
+    # windows holding one 64-row request, several packs, a request that crosses
+    # a window edge, an empty request, and runs of 16-row requests
+    ("mixed", [64, 1, 1, 63, 5, 40, 24, 0, 7, 33, 31, 2, 16, 16, 16, 16, 3], 3),
+    # 60 requests of 1 to 4 rows: up to 64 requests start in one window
+    ("tiny", [1, 4, 2, 3] * 15, 2),
+    # every size from 1 to 12
+    ("ramp", list(range(1, 13)), 2),
+]
+
+
+@pytest.mark.parametrize("name,sizes,H", PACKS)
+def test_gdn_wy_packs_requests_of_mixed_sizes(w12, name, sizes, H):
+    """The WY kernel takes the requests whose first row lies in one 64-row
+    window together, in runs of at most 64 rows; outputs must not depend on
+    where a request falls."""
+    t, dt = _hand_tree(w12, sizes, 11)
+    x = synth.gdn_inputs(t.R, len(sizes), H, 128, seed=13)
+    ref = oracle.gdn_tree_path(x.S0, x.q, x.k, x.v, x.alpha, x.beta, t)
+    ws = w12.Workspace(1, 0, 0, len(sizes))
+    layer = _layer(w12, x)
+    o_wy = w12.w12_gdn_tree_verify(layer, dt, len(sizes), ws, w12.W12_GDN_WY)
+    o_path = w12.w12_gdn_tree_verify(layer, dt, len(sizes), ws, w12.W12_GDN_PATH)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    e_wy = _rel_err(o_wy.cpu().numpy().astype(np.float64), ref)
+    e_path = _rel_err(o_path.cpu().numpy().astype(np.float64), ref)
+    assert e_wy <= 1e-4 and e_path <= 1e-4, (e_wy, e_path)
+
+
+def test_gdn_wy_flags_row_offsets_past_the_tree(w12):
+    """Row offsets that run past the tree's rows: the WY kernel checks every
+    request's range before any other read, sets W12_E_INVAL and writes nothing."""
+    t, dt = _hand_tree(w12, [10, 6], 3)
+    x = synth.gdn_inputs(t.R, 2, 1, 128, seed=3)
+    ws = w12.Workspace(1, 0, 0, 2)
+    layer = _layer(w12, x)
+    dt.req_row_off.copy_(torch.tensor([0, 10, 20], dtype=torch.int32))
+    o = torch.full((t.R, 1, 128), 7.0, device="cuda")
+    w12.w12_gdn_tree_verify(layer, dt, 2, ws, w12.W12_GDN_WY, out=o)
+    torch.cuda.synchronize()
+    assert ws.status() == w12.W12_E_INVAL
+    assert bool((o == 7.0).all())
