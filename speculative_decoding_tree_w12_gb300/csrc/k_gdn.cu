@@ -514,8 +514,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gdn_wy_slice(const GdnParams p)
 // most kPackReqs whole requests spanning at most 64 rows.  At a pack's start
 // the tree data of its rows is built (ancestor sets, cumulative gates), the
 // key and query rows go to shared memory as BF16 blocks, one per request (its
-// keys, its queries, zero rows up to a multiple of 16), and every request's
-// state S0[r][h] is sent towards L2.
+// keys, its queries, zero rows up to a multiple of 16).
 //
 // Two warp roles then run the pack's requests as a pipeline:
 //  * splitters (warps 8..11, one state row each: TMEM lane = state row c,
@@ -549,6 +548,8 @@ constexpr uint32_t kColX = 192;     // the request's key and query rows
 constexpr uint32_t kColD = 256;     // state products, up to 128 columns
 constexpr uint32_t kColD2 = 384;    // k.k and q.k, up to 64 columns
 constexpr int kBarSplit = 1, kBarSolve = 2;   // named barriers of the two roles
+constexpr int kBarGroup = 3;                  // and of the two solver groups (3, 4)
+constexpr int kHalfTri = 1040;                // a group's k.k / q.k entries: requests of up to 45 rows
 constexpr int kTri = kNR * (kNR + 1) / 2;     // entries (j, i), i <= j, of an N x N lower triangle
 
 __device__ __forceinline__ int tri(int j, int i) { return j * (j + 1) / 2 + i; }
@@ -567,9 +568,10 @@ struct WyShared {
     int8_t order[kNR];            // each request's rows by depth (a request's entries start at its first row)
     int8_t run[kNR];              // entries from this one on with its depth, in its request (at most 8)
     int32_t pack_end;
+    int32_t two_groups;           // the pack's requests are solved by two groups of solvers
     uint32_t tmem;
     int32_t abort;
-    unsigned long long bar_mma;   // the request's MMAs are done
+    unsigned long long bar_mma[2];   // request r's MMAs are done: bar_mma[r % 2], phase r / 2
     unsigned long long bar_dfree; // the solvers have copied D and D2 out
     unsigned long long bar_stage; // the request's state is in shared memory
 };
@@ -655,11 +657,17 @@ __global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy(const __grid_constant_
     }
     if (__syncthreads_or(bad) || r_lo >= r_hi) return;
 
-    const uint32_t bar_mma = smem_u32(&s.bar_mma), bar_dfree = smem_u32(&s.bar_dfree);
+    // (two barriers for the MMAs: a waiter for request r has always seen
+    // request r - 2 complete, so the parity it waits for is never two phases
+    // ahead, whichever solver group takes r)
+    const uint32_t bar_mma0 = smem_u32(&s.bar_mma[0]), bar_dfree = smem_u32(&s.bar_dfree);
+    auto bar_mma = [&](uint32_t r) { return bar_mma0 + 8u * (r & 1u); };
+    auto mma_par = [](uint32_t r) { return (r >> 1) & 1u; };
     const uint32_t bar_stage = smem_u32(&s.bar_stage), stage = smem_u32(s.stage);
     if (tid == 0) {
-        mbar_init(bar_mma, 1);
-        mbar_init(bar_dfree, kSolvers / 32);   // one arrival per solver warp
+        mbar_init(bar_mma(0), 1);
+        mbar_init(bar_mma(1), 1);
+        mbar_init(bar_dfree, 4);   // one arrival per warp of the solver group (or of warps 0..3)
         mbar_init(bar_stage, 1);
         prefetch_tmap(&smap);
         s.abort = 0;
@@ -723,17 +731,19 @@ __global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy(const __grid_constant_
         __syncthreads();
         if (tid == 0) {
             unsigned long long m = s.starts;
-            int blk = 0, end = 0;
-            for (int q = 0; q < kPackReqs && m; ++q) {
+            int blk = 0, end = 0, q = 0, big = 0;
+            for (; q < kPackReqs && m; ++q) {
                 const int st = __ffsll((long long)m) - 1;
                 m &= m - 1;
                 const int rows = s.blk[st];
                 s.blk[st] = blk;
                 blk += (2 * rows + 15) & ~15;
                 end = st + rows;
+                big |= rows * (rows + 1) / 2 > kHalfTri;
             }
             if (m) s.starts &= (1ull << (__ffsll((long long)m) - 1)) - 1;   // the rest goes to the next pack
             s.pack_end = a + end;
+            s.two_groups = q > 1 && !big;
         }
         __syncthreads();
         const int n = s.pack_end - a;
@@ -744,7 +754,8 @@ __global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy(const __grid_constant_
         }
 
         // the rest of the pack's reads: the key / query blocks (asynchronous
-        // copies into shared memory) and every other request's state towards L2
+        // copies into shared memory; each later request's state is copied by
+        // TMA once the previous one has been split)
         {
             unsigned long long m = starts;
             while (m) {
@@ -776,15 +787,6 @@ __global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy(const __grid_constant_
             s.t.par[tid] = pl;
             s.t.alpha[tid] = al;
             s.t.beta[tid] = be;
-        }
-        {
-            unsigned long long m = starts;
-            for (int q = 0; m; ++q) {   // four threads per request, a quarter of its state each
-                const int st = __ffsll((long long)m) - 1;
-                m &= m - 1;
-                if (q > 0 && q == (tid >> 2))
-                    prefetch_l2(state_of(p, s.rq[st], h) + (tid & 3) * (kD * kD / 4), kD * kD / 4 * sizeof(float));
-            }
         }
         __syncthreads();
         // ancestor sets and cumulative gates
@@ -835,7 +837,7 @@ __global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy(const __grid_constant_
                 // them all here)
                 bool ok = issue_ok;
                 if (warp == 8) {
-                    if (rc > 0) ok = ok && mbar_wait(bar_mma, (rc - 1) & 1u, p.timeout_ns, p.status, &s.abort);
+                    if (rc > 0) ok = ok && mbar_wait(bar_mma(rc - 1), mma_par(rc - 1), p.timeout_ns, p.status, &s.abort);
                     ok = ok && mbar_wait(bar_stage, rc & 1u, p.timeout_ns, p.status, &s.abort);
                     ok = __all_sync(0xffffffffu, ok);
                 }
@@ -918,7 +920,7 @@ __global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy(const __grid_constant_
                         for (int ks = 0; ks < 8; ++ks)
                             tc_mma_ts(tmem + kColD2, tmem + kColX + 8 * ks,
                                       (ks < 4 ? b0 : b1) + (uint64_t)((ks & 3) * 2), id2, ks ? 1u : 0u);
-                        tc_commit(bar_mma);
+                        tc_commit(bar_mma(rc));
                     }
                     __syncwarp();
                     if (!ok) {
@@ -930,22 +932,33 @@ __global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy(const __grid_constant_
             }
         } else {
             // -------------------------------------------------------------- solvers
-            while (m && go) {
+            // Two groups of four warps take alternate requests when every
+            // request of the pack fits half of the k.k / q.k buffers; else all
+            // eight warps take each request, two threads per column.
+            const bool two = s.two_groups != 0;
+            const int grp = warp >> 2;                          // 0: warps 0..3, 1: warps 4..7
+            const int bar_id = two ? kBarGroup + grp : kBarSolve, bar_n = two ? 128 : kSolvers;
+            const int nsplit = two ? 1 : 2, part = two ? 0 : hs;   // column chunks / group rows shared by nsplit warps
+            const int poller = two ? 4 * grp : 0;
+            float *KKb = s.KK + (two ? grp * kHalfTri : 0), *QKb = s.QK + (two ? grp * kHalfTri : 0);
+            uint32_t rq_i = rc;                                   // this request's number
+            for (int q = 0; m && go; ++q, ++rq_i) {
                 const int st = __ffsll((long long)m) - 1;
                 m &= m - 1;
                 const int en = m ? __ffsll((long long)m) - 1 : n, nr = en - st;
-                // the MMAs are done: warp 0 polls, the other solvers wait in the barrier
+                if (two && (q & 1) != grp) continue;
+                // the MMAs are done: one warp polls, the others wait in the barrier
                 bool ok = true;
-                if (warp == 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_mma, rc & 1u, p.timeout_ns, p.status, &s.abort));
-                if (!bar_all(kBarSolve, kSolvers, ok)) {
+                if (warp == poller)
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar_mma(rq_i), mma_par(rq_i), p.timeout_ns, p.status, &s.abort));
+                if (!bar_all(bar_id, bar_n, ok)) {
                     go = false;
                     break;
                 }
                 tc_fence_after();
-                // D -> S0 k and S0 q rows; D2 -> the scaled k.k and q.k rows.  The
-                // two warps of a lane quarter take alternate 16-column chunks.
+                // D -> S0 k and S0 q rows; D2 -> the scaled k.k and q.k rows
                 const bool d2 = (warp & 3) * 32 < 2 * nr;   // this warp's lanes hold rows of D2
-                for (int c0 = 16 * hs; c0 < 2 * nr; c0 += 32) {
+                for (int c0 = 16 * part; c0 < 2 * nr; c0 += 16 * nsplit) {
                     uint32_t v[16], v2[16];
                     tmem_ld_x16(tmem + lane_base + kColD + c0, v);
                     if (d2 && c0 < nr) tmem_ld_x16(tmem + lane_base + kColD2 + c0, v2);
@@ -961,32 +974,30 @@ __global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy(const __grid_constant_
                     if (d2 && c0 < nr && c < 2 * nr) {
                         const int jj = c < nr ? c : c - nr, j = st + jj;
                         const float f = c < nr ? s.t.beta[j] * s.t.g[j] : s.t.g[j];
-                        float *dst = c < nr ? s.KK : s.QK;
+                        float *dst = c < nr ? KKb : QKb;
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
                             if (c0 + i <= jj) dst[tri(jj, c0 + i)] = __uint_as_float(v2[i]) * s.t.ginv[st + c0 + i] * f;
                     }
                 }
                 tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_dfree);   // D, D2 free for the next request's MMAs
-                ++rc;
-                named_bar(kBarSolve, kSolvers);
-                // rows by depth, up to eight rows of one depth at a time (none is
-                // an ancestor of another, and all have `depth` ancestors), four of
-                // them per thread: one pass over the ancestors for u_j and o_j
+                named_bar(bar_id, bar_n);
+                if ((two || warp < 4) && lane == 0) mbar_arrive(bar_dfree);   // D, D2 free for the next MMAs
+                // rows by depth, a run of rows of one depth at a time (none is an
+                // ancestor of another, and all have `depth` ancestors), up to four
+                // per thread: one pass over the ancestors for u_j and o_j
                 for (int t = st; t < en;) {
-                    const int d = s.t.depth[s.order[t]], gsz = s.run[t];
-                    const int mine = (gsz - hs + 1) >> 1;   // entries hs, hs + 2, ... of the group
+                    const int d = s.t.depth[s.order[t]], gsz = min((int)s.run[t], 4 * nsplit);
+                    const int mine = (gsz - part + nsplit - 1) / nsplit;   // entries part, part + nsplit, ...
                     if (mine > 0) {
                         int jr[4], tb[4];
                         float u[4], o[4];
                         unsigned long long am[4];
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
-                            const int j = s.order[t + hs + 2 * min(k, mine - 1)];   // the last one again past the end
+                            const int j = s.order[t + part + nsplit * min(k, mine - 1)];   // the last one again past the end
                             jr[k] = j;
-                            tb[k] = tri(j - st, 0) - st;                          // entry (j, i) at index tb + i
+                            tb[k] = tri(j - st, 0) - st;                                    // entry (j, i) at index tb + i
                             const float vj = __uint_as_float((uint32_t)s.V[j * kD + c] << 16);
                             u[k] = s.t.beta[j] * (vj - s.t.g[j] * s.PU[j * kD + c]);
                             o[k] = s.t.g[j] * s.Rq[j * kD + c];
@@ -998,22 +1009,23 @@ __global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy(const __grid_constant_
                                 const int i = __ffsll((long long)am[k]) - 1;
                                 am[k] &= am[k] - 1;
                                 const float ui = s.PU[i * kD + c];
-                                u[k] = fmaf(-s.KK[tb[k] + i], ui, u[k]);
-                                o[k] = fmaf(s.QK[tb[k] + i], ui, o[k]);
+                                u[k] = fmaf(-KKb[tb[k] + i], ui, u[k]);
+                                o[k] = fmaf(QKb[tb[k] + i], ui, o[k]);
                             }
                         }
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
                             if (k < mine) {
                                 s.PU[jr[k] * kD + c] = u[k];
-                                p.out[((size_t)(a + jr[k]) * H + h) * kD + c] = fmaf(s.QK[tb[k] + jr[k]], u[k], o[k]);
+                                p.out[((size_t)(a + jr[k]) * H + h) * kD + c] = fmaf(QKb[tb[k] + jr[k]], u[k], o[k]);
                             }
                         }
                     }
                     t += gsz;
-                    named_bar(kBarSolve, kSolvers);   // the next depth reads this group's u
+                    named_bar(bar_id, bar_n);   // the next depth reads these rows' u
                 }
             }
+            rc += __popcll(starts);   // (both roles count the pack's requests)
         }
         if (__syncthreads_or(!go)) go = false;   // the pack is done (or stopped) on both sides
         a += n;
@@ -1024,7 +1036,7 @@ __global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy(const __grid_constant_
     // commit and the last state copy
     if (!go && rc > 0) {
         const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(bar_mma, (rc - 1) & 1u) && globaltimer() - t0 < p.timeout_ns) {
+        while (!mbar_try_wait(bar_mma(rc - 1), mma_par(rc - 1)) && globaltimer() - t0 < p.timeout_ns) {
         }
     }
     if (!go && tid == kSolvers && n_staged > 0) {
