@@ -722,6 +722,20 @@ def gdn_stack(wk: "Workload", K: int, W: int, seed: int = 0):
             "inputs": "synthetic: N(0, 0.05) states, unit-norm q/k, N(0, 1) v, gates U[0.85, 1), strengths U[0.05, 0.95]"}
 
 
+def gdn_batched(wk: "Workload", K: int, W: int):
+    """The same 48-layer recurrent stack over the batched_27b tree (24
+    requests drafting 16/12/8 positions, 192 rows): the WY form runs on the
+    tensor-memory kernel there, on the sliced kernel for one request."""
+    import types
+    w12, synth = wk.w12, wk.synth
+    dev = wk.argmax.device
+    w = synth.WORKLOADS["batched_27b"]
+    ws = w12.Workspace(w.budget, 0, 0, w.n_req, dev)
+    tree = w12.w12_tree_build(w12.DeviceLattice(synth.lattice(w, 0), dev), w.budget, ws)
+    sub = types.SimpleNamespace(w12=w12, synth=synth, argmax=wk.argmax, wl=w, R=tree.R, tree=tree)
+    return gdn_stack(sub, K, W)
+
+
 # ---------------------------------------------------------------------------
 # step time vs tree rows
 # ---------------------------------------------------------------------------
@@ -1032,12 +1046,20 @@ def main():
         tlv = {"error": str(ex)[:200]}
 
     # ------------------------------------------- recurrent-layer verification
-    gdn = None
+    gdn = gdn_b = None
     try:
         if args.extras == "all":
             gdn = gdn_stack(wk, max(10, min(K, 50)), W)
     except Exception as ex:  # reported, never hidden
         gdn = {"error": str(ex)[:200]}
+    try:
+        if args.extras == "all":
+            gdn_b = gdn_batched(wk, max(10, min(K, 50)), W)
+            if gdn and "wy_us" in gdn:
+                # per layer, batched tree over the workload's tree
+                gdn_b["wy_over_workload_tree"] = round(gdn_b["wy_us"] / gdn["wy_us"], 3)
+    except Exception as ex:  # reported, never hidden
+        gdn_b = {"error": str(ex)[:200]}
 
     # --------------------------------------------------- step time vs rows
     sweep = None
@@ -1088,6 +1110,7 @@ def main():
             "certified_head": cert,
             "tlv_cycle": tlv,
             "gdn_tree": gdn,
+            "gdn_tree_batched": gdn_b,
         }
         if sweep and all("step_us" in e for e in sweep):
             one = {e["rows"]: e["step_us"] for e in sweep if e["requests"] == 1}
