@@ -15,7 +15,8 @@ autoregressive decoding through the combined tree under any Q-pass argmax,
 tree invariants); the recurrent-layer tree functions by
 ``tests/test_oracle_gdn.py`` (closed forms for pure decay and for a unit key
 written at full strength, independence from rows off the root path, an
-independent WY-form restatement, the commit state).
+independent WY-form restatement (outputs and the WY vectors u), the commit
+state, and the commit rebuilt from the WY vectors).
 """
 from __future__ import annotations
 
@@ -355,6 +356,34 @@ def gdn_tree_path(S0: np.ndarray, q: np.ndarray, k: np.ndarray, v: np.ndarray, a
             S = a64[i][:, None, None] * (S - b64[i][:, None, None] * Sk[:, :, None] * kf[i][:, None, :]) \
                 + b64[i][:, None, None] * vf[i][:, :, None] * kf[i][:, None, :]
         out[j] = np.einsum("hvk,hk->hv", S, qf[j])
+    return out
+
+
+def gdn_wy_u(S0: np.ndarray, k: np.ndarray, v: np.ndarray, alpha: np.ndarray, beta: np.ndarray, tree: Tree):
+    """The WY vectors of every tree row (FP64), by their definition (SpecPilot
+    explainer 4.2, TreeWY): u_j = b_j (v_j - a_j S_p k_j), where S_p is the
+    state the row's update applies to (its parent's state after the parent's
+    update, or the request's committed state for a root), found by walking
+    the root path as gdn_tree_path does.  With them the state after row j is
+    g_j S0 + sum over i on j's root path of (g_j / g_i) u_i k_i^T (g the
+    product of the gates along the path).  Returns float64 [R][H][d_v]."""
+    kf, vf = _bf16_to_f64(k), _bf16_to_f64(v)
+    a64, b64 = np.asarray(alpha, np.float64), np.asarray(beta, np.float64)
+    R, H, _ = kf.shape
+    out = np.empty((R, H, vf.shape[2]), np.float64)
+    for j in range(R):
+        path = []
+        i = int(tree.parent[j])
+        while i >= 0:
+            path.append(i)
+            i = int(tree.parent[i])
+        S = np.array(S0[int(tree.req[j])], np.float64)
+        for i in reversed(path):
+            Sk = np.einsum("hvk,hk->hv", S, kf[i])
+            S = a64[i][:, None, None] * (S - b64[i][:, None, None] * Sk[:, :, None] * kf[i][:, None, :]) \
+                + b64[i][:, None, None] * vf[i][:, :, None] * kf[i][:, None, :]
+        Sk = np.einsum("hvk,hk->hv", S, kf[j])
+        out[j] = b64[j][:, None] * (vf[j] - a64[j][:, None] * Sk)
     return out
 
 

@@ -86,7 +86,7 @@ def test_rows_off_the_root_path_do_not_matter(kw):
         assert np.array_equal(o2[j], o[j])
 
 
-def _wy_reference(S0, q, k, v, alpha, beta, tree):
+def _wy_reference(S0, q, k, v, alpha, beta, tree, u_out=None):
     """The tree in WY form, written independently of the oracle's loop: per
     request and head, with g the cumulative gate along each root path and
     anc/path the strict/inclusive ancestor relations,
@@ -119,6 +119,8 @@ def _wy_reference(S0, q, k, v, alpha, beta, tree):
             U = np.linalg.solve(np.eye(n) + A, B)
             C = np.where(incl, ratio * (Q @ K.T), 0.0)
             out[rows, h] = gcum[:, None] * (Q @ S.T) + C @ U
+            if u_out is not None:
+                u_out[rows, h] = U
     return out
 
 
@@ -142,3 +144,46 @@ def test_commit_state_reproduces_the_accepted_rows_output(kw):
     qf = synth.bf16_bits_to_f32(x.q).astype(np.float64)
     for r, j in enumerate(acc):
         assert np.allclose(np.einsum("hvk,hk->hv", S[r], qf[j]), o[j], rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("kw", TREES)
+def test_wy_vectors_equal_the_triangular_solve(kw):
+    """oracle.gdn_wy_u (u_j from the state each row's update applies to)
+    against U of the independent WY restatement, (I + A) U = B by a dense
+    solve."""
+    t, w = _tree(kw, 15)
+    x = synth.gdn_inputs(t.R, w.n_req, 3, 32, seed=16)
+    U = np.zeros((t.R, 3, 32))
+    _wy_reference(x.S0, x.q, x.k, x.v, x.alpha, x.beta, t, u_out=U)
+    u = oracle.gdn_wy_u(x.S0, x.k, x.v, x.alpha, x.beta, t)
+    assert np.max(np.abs(u - U)) <= 1e-12 * max(1.0, np.max(np.abs(U)))
+
+
+@pytest.mark.parametrize("kw", TREES)
+def test_commit_from_wy_vectors_equals_the_replay(kw):
+    """The accepted state in WY form, g S0 + sum over the path of (g / g_i)
+    u_i k_i^T, against the committed state replayed step by step."""
+    t, w = _tree(kw, 17)
+    x = synth.gdn_inputs(t.R, w.n_req, 2, 16, seed=18)
+    g = np.random.default_rng(19)
+    acc = np.asarray([g.integers(t.req_row_off[r], t.req_row_off[r + 1]) for r in range(w.n_req)], np.int32)
+    ref = oracle.gdn_commit(x.S0, x.k, x.v, x.alpha, x.beta, t, acc)
+    u = oracle.gdn_wy_u(x.S0, x.k, x.v, x.alpha, x.beta, t)
+    kf = synth.bf16_bits_to_f32(x.k).astype(np.float64)
+    a64 = x.alpha.astype(np.float64)
+    for r, j in enumerate(acc):
+        path = []
+        i = int(j)
+        while i >= 0:
+            path.append(i)
+            i = int(t.parent[i])
+        gcum = {}
+        run = np.ones(2)
+        for i in reversed(path):
+            run = run * a64[i]
+            gcum[i] = run.copy()
+        gacc = gcum[int(j)]
+        S = gacc[:, None, None] * x.S0[r].astype(np.float64)
+        for i in path:
+            S += (gacc / gcum[i])[:, None, None] * u[i][:, :, None] * kf[i][:, None, :]
+        assert np.allclose(S, ref[r], rtol=1e-11, atol=1e-13)
