@@ -654,9 +654,11 @@ def gdn_stack(wk: "Workload", K: int, W: int, seed: int = 0):
     4.2): 48 Gated DeltaNet layers of 32 heads of 128 (synthetic committed
     states and q/k/v/gates, 4 distinct input sets, each layer with its own
     device copy), one launch per layer as a real stack would need, captured
-    in a CUDA graph.  Times the WY kernel, the path-walk kernel and the
-    commit replay of one accepted row per request; bytes are the states read
-    (and written by the commit) plus q/k/v/gates in and outputs out."""
+    in a CUDA graph.  Times the WY kernel, the path-walk kernel, the
+    commit replay of one accepted row per request, the WY kernel writing its
+    vectors u, and the commit from those vectors (one pass over the states);
+    bytes are the states read (and written by the commits) plus q/k/v/gates
+    in and outputs out."""
     import torch
     w12, synth = wk.w12, wk.synth
     dev = wk.argmax.device
@@ -680,6 +682,16 @@ def gdn_stack(wk: "Workload", K: int, W: int, seed: int = 0):
     def commit():
         for L, st in zip(layers, states):
             w12.w12_gdn_commit(L, wk.tree, n_req, acc, ws, state=st)
+
+    us = [torch.empty((R, GDN_HEADS, GDN_DIM), dtype=torch.float32, device=dev) for _ in range(GDN_LAYERS)]
+
+    def run_wy_u():
+        for L, o, u in zip(layers, outs, us):
+            w12.w12_gdn_wy_verify(L, wk.tree, n_req, ws, out=o, u=u)
+
+    def commit_wy():
+        for L, st, u in zip(layers, states, us):
+            w12.w12_gdn_wy_commit(L, wk.tree, n_req, acc, u, ws, state=st)
 
     def timed(fn):
         for _ in range(W):
@@ -708,6 +720,8 @@ def gdn_stack(wk: "Workload", K: int, W: int, seed: int = 0):
     ms_wy = timed(lambda: run(w12.W12_GDN_WY))
     ms_path = timed(lambda: run(w12.W12_GDN_PATH))
     ms_commit = timed(commit)
+    ms_wy_u = timed(run_wy_u)
+    ms_commit_wy = timed(commit_wy)
     if ws.status() != 0:
         raise RuntimeError(f"device status {w12.status_str(ws.status())}")
     state_b = n_req * GDN_HEADS * GDN_DIM * GDN_DIM * 4
@@ -716,8 +730,10 @@ def gdn_stack(wk: "Workload", K: int, W: int, seed: int = 0):
     commit_bytes = GDN_LAYERS * (2 * state_b + R * GDN_HEADS * (2 * GDN_DIM * 2 + 2 * 4))
     return {"layers": GDN_LAYERS, "heads": GDN_HEADS, "head_dim": GDN_DIM, "rows": int(R), "requests": int(n_req),
             "wy_us": round(1e3 * ms_wy, 2), "path_us": round(1e3 * ms_path, 2), "commit_us": round(1e3 * ms_commit, 2),
+            "wy_with_u_us": round(1e3 * ms_wy_u, 2), "commit_wy_us": round(1e3 * ms_commit_wy, 2),
             "verify_bytes": int(verify_bytes), "wy_gbs": round(verify_bytes / (ms_wy * 1e-3) / 1e9, 1),
             "commit_gbs": round(commit_bytes / (ms_commit * 1e-3) / 1e9, 1),
+            "commit_wy_gbs": round(commit_bytes / (ms_commit_wy * 1e-3) / 1e9, 1),
             "timing": "CUDA graph of the 48 per-layer launches, CUDA events",
             "inputs": "synthetic: N(0, 0.05) states, unit-norm q/k, N(0, 1) v, gates U[0.85, 1), strengths U[0.05, 0.95]"}
 

@@ -370,6 +370,28 @@ w12_status w12_gdn_tree_verify(const w12_gdn_layer *layer, const w12_tree *tree,
 w12_status w12_gdn_commit(const w12_gdn_layer *layer, const w12_tree *tree, int32_t n_req, const int32_t *acc_node,
                           float *state, void *ws, size_t ws_bytes, w12_stream_t stream);
 
+/*
+ * The WY form with its vectors kept for the commit (explainer 4.2, TreeWY):
+ * the outputs o as w12_gdn_tree_verify(W12_GDN_WY) gives them, and
+ * u (device FP32 [R][H][d], caller-owned) with u_j = b_j (v_j - a_j S k_j),
+ * S the state row j's update applies to.  The state after row j is then
+ * g_j S0 + sum over i on j's root path of (g_j / g_i) u_i k_i^T, g the
+ * product of the gates along the path.  Same checks and status words as
+ * w12_gdn_tree_verify; o and u must not be NULL.
+ */
+w12_status w12_gdn_wy_verify(const w12_gdn_layer *layer, const w12_tree *tree, int32_t n_req, float *o, float *u,
+                             void *ws, size_t ws_bytes, w12_stream_t stream);
+
+/*
+ * The committed states from those vectors, in one pass over S0 (no replay):
+ * state[r] = g S0[r] + sum over i on acc_node[r]'s root path of (g / g_i) u_i k_i^T,
+ * with u from w12_gdn_wy_verify on the same layer and tree.  state as for
+ * w12_gdn_commit (16-byte aligned; may be S0 itself).  Device checks: a row
+ * outside the request sets W12_E_INVAL (the state is then left as S0[r]).
+ */
+w12_status w12_gdn_wy_commit(const w12_gdn_layer *layer, const w12_tree *tree, int32_t n_req, const int32_t *acc_node,
+                             const float *u, float *state, void *ws, size_t ws_bytes, w12_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * The verify step
  * ---------------------------------------------------------------------- */

@@ -106,6 +106,8 @@ def lib():
             "w12_tlv_chain": ([p, p, i32, i32, p, p], C.c_int),
             "w12_gdn_tree_verify": ([p, p, i32, i32, p, p, sz, p], C.c_int),
             "w12_gdn_commit": ([p, p, i32, p, p, p, sz, p], C.c_int),
+            "w12_gdn_wy_verify": ([p, p, i32, p, p, p, sz, p], C.c_int),
+            "w12_gdn_wy_commit": ([p, p, i32, p, p, p, p, sz, p], C.c_int),
             "w12_tlv_splice": ([p, p, p, p, i32, i32, p, p, p, p, sz, p], C.c_int),
             "w12_debug_set": ([i32, C.c_uint64], None),
             "w12_debug_num_sms": ([], i32),
@@ -469,6 +471,30 @@ def w12_gdn_commit(layer: GdnLayer, tree: DeviceTree, n_req: int, acc_node, ws: 
         state = torch.empty_like(layer.S0)
     _check(lib().w12_gdn_commit(C.byref(layer.c), C.byref(tree.c), int(n_req), C.c_void_p(acc_node.data_ptr()),
                                 C.c_void_p(state.data_ptr()), ws.ptr, ws.nbytes, _stream(stream)), "w12_gdn_commit")
+    return state
+
+
+def w12_gdn_wy_verify(layer: GdnLayer, tree: DeviceTree, n_req: int, ws: Workspace, out=None, u=None, stream=None):
+    """WY-form outputs and the WY vectors u (both float32 [R][H][d])."""
+    import torch
+    if out is None:
+        out = torch.empty((tree.R, layer.H, layer.d), dtype=torch.float32, device=layer.q.device)
+    if u is None:
+        u = torch.empty((tree.R, layer.H, layer.d), dtype=torch.float32, device=layer.q.device)
+    _check(lib().w12_gdn_wy_verify(C.byref(layer.c), C.byref(tree.c), int(n_req), C.c_void_p(out.data_ptr()),
+                                   C.c_void_p(u.data_ptr()), ws.ptr, ws.nbytes, _stream(stream)), "w12_gdn_wy_verify")
+    return out, u
+
+
+def w12_gdn_wy_commit(layer: GdnLayer, tree: DeviceTree, n_req: int, acc_node, u, ws: Workspace, state=None,
+                      stream=None):
+    """The committed states from the WY vectors u of w12_gdn_wy_verify."""
+    import torch
+    if state is None:
+        state = torch.empty_like(layer.S0)
+    _check(lib().w12_gdn_wy_commit(C.byref(layer.c), C.byref(tree.c), int(n_req), C.c_void_p(acc_node.data_ptr()),
+                                   C.c_void_p(u.data_ptr()), C.c_void_p(state.data_ptr()), ws.ptr, ws.nbytes,
+                                   _stream(stream)), "w12_gdn_wy_commit")
     return state
 
 

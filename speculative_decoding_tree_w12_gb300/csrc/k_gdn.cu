@@ -31,8 +31,10 @@
 //    kernel pays a fixed cost per CTA (tensor memory, the state staged by
 //    TMA) and little per request.
 //
-// The committed-state update after acceptance (k_gdn_commit) replays the
-// accepted path, like the path kernel, and writes the state.
+// The committed-state update after acceptance either replays the accepted
+// path (k_gdn_path<true>, like the path kernel) or, given the WY vectors u the
+// WY form wrote, adds the path's rank-one terms to the committed state in one
+// pass (k_gdn_wy_commit).
 //
 // Grid of the path walk and the commit: (request, head, d_v / 32); of the WY
 // kernels: windows of first rows (several requests per CTA), see below.  Rows
@@ -67,6 +69,7 @@ struct GdnParams {
     const float *alpha, *beta;
     const int32_t *parent, *req_row_off, *acc_node;
     float *out;          // o [R][H][d] or, for the commit, the state [n_req][H][d][d]
+    float *u;            // the WY vectors u [R][H][d]: written by the WY form when not null, read by its commit
     int32_t *status;
 };
 
@@ -499,6 +502,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gdn_wy_slice(const GdnParams p)
                 sum = fmaf(s.QK[j * kMS + i] * s.t.ginv[i], s.U[i * kPS + c], sum);
             }
             p.out[((size_t)(a + j) * H + h) * kD + vs + c] = s.t.g[j] * sum;
+            if (p.u) p.u[((size_t)(a + j) * H + h) * kD + vs + c] = s.U[j * kPS + c];
         }
         a += n;
         __syncthreads();   // the next pack reuses every buffer
@@ -618,11 +622,6 @@ __device__ __forceinline__ bool bar_all(int id, int threads, bool v)
 // byte offset of 16-byte piece `chunk` (features 8 chunk .. 8 chunk + 7 of
 // the half) of block row `row` in one feature half of X
 __device__ __forceinline__ uint32_t x_off(int row, int chunk) { return row * 128 + ((chunk ^ (row & 7)) << 4); }
-
-__device__ __forceinline__ const float *state_of(const GdnParams &p, int r, int h)
-{
-    return p.S0 + ((size_t)r * p.H + h) * kD * kD;
-}
 
 __global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy(const __grid_constant__ CUtensorMap smap, const GdnParams p)
 {
@@ -1018,6 +1017,7 @@ __global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy(const __grid_constant_
                             if (k < mine) {
                                 s.PU[jr[k] * kD + c] = u[k];
                                 p.out[((size_t)(a + jr[k]) * H + h) * kD + c] = fmaf(QKb[tb[k] + jr[k]], u[k], o[k]);
+                                if (p.u) p.u[((size_t)(a + jr[k]) * H + h) * kD + c] = u[k];
                             }
                         }
                     }
@@ -1163,6 +1163,110 @@ __global__ void __launch_bounds__(kThreads, 1) k_gdn_path(const GdnParams p)
 }
 
 
+// ---------------------------------------------------------------------------
+// commit from the WY vectors
+// ---------------------------------------------------------------------------
+//
+// The state after the accepted row j in WY form (explainer 4.2):
+//     S_j = g_j S0 + sum over i on j's root path of (g_j / g_i) u_i k_i^T,
+// with the u_i the WY form wrote.  One pass over the committed state: each
+// thread reads four float4 of the slice, adds the path's rank-one terms and
+// writes them back (in place if the state is S0).  Grid (request, head,
+// d_v / 32).
+
+struct WyCommitShared {
+    float K[kNR * kD];     // the path's keys (FP32), in path order (accepted row first)
+    float Uc[kNR * kVS];   // their WY vectors, this CTA's 32 state rows
+    float coef[kNR];       // g_acc / g_i per path entry
+    int32_t path[kNR];
+    int32_t par[kNR];
+    float alpha[kNR];
+    int32_t plen;
+    float gacc;
+};
+
+__global__ void __launch_bounds__(kThreads) k_gdn_wy_commit(const GdnParams p)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    WyCommitShared &s = *reinterpret_cast<WyCommitShared *>(smem_raw);
+    const int r = blockIdx.x, h = blockIdx.y, vs = blockIdx.z * kVS;
+    const int tid = threadIdx.x;
+    const int H = p.H;
+    // the committed slice (rows vs .. vs + 31) first
+    const float *S0 = p.S0 + (((size_t)r * H + h) * kD + vs) * kD;
+    float4 sv[kVS * kD / 4 / kThreads];
+#pragma unroll
+    for (int i = 0; i < kVS * kD / 4 / kThreads; ++i)
+        sv[i] = *reinterpret_cast<const float4 *>(S0 + (size_t)(tid + i * kThreads) * 4);
+    int row0;
+    const int n = request_rows(p, r, row0);
+    if (n <= 0) return;
+    if (tid < n) {
+        const int pr = p.parent[row0 + tid];
+        int pl = pr < 0 ? -1 : pr - row0;
+        if (pr >= 0 && (pl < 0 || pl >= tid)) {
+            atomicCAS(p.status, 0, (int32_t)W12_E_INVAL);
+            pl = -1;
+        }
+        s.par[tid] = pl;
+        s.alpha[tid] = p.alpha[(size_t)(row0 + tid) * H + h];
+    }
+    __syncthreads();
+    if (tid == 0) {
+        // the accepted row's root path (strictly decreasing rows: at most n
+        // steps), then the cumulative gates from the root down
+        const int node = p.acc_node[r] - row0;
+        int len = 0;
+        if (node >= 0 && node < n) {
+            for (int i = node; i >= 0; i = s.par[i]) s.path[len++] = i;
+        } else {
+            atomicCAS(p.status, 0, (int32_t)W12_E_INVAL);   // the state stays S0[r]
+        }
+        float g = 1.f;
+        for (int q = len - 1; q >= 0; --q) {
+            g *= s.alpha[s.path[q]];
+            s.coef[q] = g;
+        }
+        s.gacc = g;
+        for (int q = 0; q < len; ++q) s.coef[q] = g / s.coef[q];
+        s.plen = len;
+    }
+    __syncthreads();
+    const int len = s.plen;
+    for (int e = tid; e < len * 16; e += kThreads) {
+        const int q = e >> 4, ch = e & 15;
+        const uint4 kv = *reinterpret_cast<const uint4 *>(p.k + ((size_t)(row0 + s.path[q]) * H + h) * kD + ch * 8);
+        const uint32_t w4[4] = {kv.x, kv.y, kv.z, kv.w};
+        float *dst = &s.K[q * kD + ch * 8];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            dst[2 * t] = __uint_as_float(w4[t] << 16);
+            dst[2 * t + 1] = __uint_as_float(w4[t] & 0xffff0000u);
+        }
+    }
+    for (int e = tid; e < len * kVS; e += kThreads) {
+        const int q = e / kVS, c = e % kVS;
+        s.Uc[q * kVS + c] = p.u[((size_t)(row0 + s.path[q]) * H + h) * kD + vs + c];
+    }
+    __syncthreads();
+    const float gacc = s.gacc;
+    float *dst = p.out + (((size_t)r * H + h) * kD + vs) * kD;
+#pragma unroll
+    for (int i = 0; i < kVS * kD / 4 / kThreads; ++i) {
+        const int e = tid + i * kThreads, row = e >> 5, c4 = (e & 31) * 4;
+        float4 x = make_float4(gacc * sv[i].x, gacc * sv[i].y, gacc * sv[i].z, gacc * sv[i].w);
+        for (int q = 0; q < len; ++q) {
+            const float w = s.coef[q] * s.Uc[q * kVS + row];
+            const float4 kk = *reinterpret_cast<const float4 *>(&s.K[q * kD + c4]);
+            x.x = fmaf(w, kk.x, x.x);
+            x.y = fmaf(w, kk.y, x.y);
+            x.z = fmaf(w, kk.z, x.z);
+            x.w = fmaf(w, kk.w, x.w);
+        }
+        *reinterpret_cast<float4 *>(dst + (size_t)row * kD + c4) = x;
+    }
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -1203,6 +1307,7 @@ int launch_gdn(const GdnArgs &a, int mode, void *stream)
     p.req_row_off = a.req_row_off;
     p.acc_node = a.acc_node;
     p.out = a.out;
+    p.u = a.u;
     p.status = a.status;
     // plain launches: with an early start the next layer's CTAs would share
     // SMs with this one's and leave others idle (one CTA per SM is the
@@ -1242,6 +1347,13 @@ int launch_gdn(const GdnArgs &a, int mode, void *stream)
                                              (int)cfg.dynamicSmemBytes);
         if (e != cudaSuccess) return (int)e;
         return (int)cudaLaunchKernelEx(&cfg, k_gdn_wy, smap, p);
+    }
+    if (mode == kGdnCommitWy) {
+        cfg.dynamicSmemBytes = sizeof(WyCommitShared);
+        cudaError_t e = cudaFuncSetAttribute(k_gdn_wy_commit, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)cfg.dynamicSmemBytes);
+        if (e != cudaSuccess) return (int)e;
+        return (int)cudaLaunchKernelEx(&cfg, k_gdn_wy_commit, p);
     }
     cfg.dynamicSmemBytes = sizeof(PathShared);
     const auto kern = mode == kGdnCommit ? k_gdn_path<true> : k_gdn_path<false>;

@@ -731,6 +731,39 @@ w12_status w12_gdn_tree_verify(const w12_gdn_layer *layer, const w12_tree *tree,
     return cuda_status(launch_gdn(a, method == W12_GDN_WY ? kGdnWy : kGdnPath, stream));
 }
 
+w12_status w12_gdn_wy_verify(const w12_gdn_layer *layer, const w12_tree *tree, int32_t n_req, float *o, float *u,
+                             void *ws, size_t ws_bytes, w12_stream_t stream)
+{
+    GdnArgs a;
+    w12_status s = gdn_args(layer, tree, n_req, a);
+    if (s != W12_OK) return s;
+    if (!o || !u) return W12_E_INVAL;
+    const WsLayout L = layout_for(1, 0, 0, n_req);
+    if ((s = ws_check(ws, ws_bytes, L)) != W12_OK) return s;
+    Ws W{static_cast<uint8_t *>(ws), L};
+    a.out = o;
+    a.u = u;
+    a.status = W.status();
+    return cuda_status(launch_gdn(a, kGdnWy, stream));
+}
+
+w12_status w12_gdn_wy_commit(const w12_gdn_layer *layer, const w12_tree *tree, int32_t n_req, const int32_t *acc_node,
+                             const float *u, float *state, void *ws, size_t ws_bytes, w12_stream_t stream)
+{
+    GdnArgs a;
+    w12_status s = gdn_args(layer, tree, n_req, a);
+    if (s != W12_OK) return s;
+    if (!acc_node || !u || !state || !aligned(state, 16)) return W12_E_INVAL;
+    const WsLayout L = layout_for(1, 0, 0, n_req);
+    if ((s = ws_check(ws, ws_bytes, L)) != W12_OK) return s;
+    Ws W{static_cast<uint8_t *>(ws), L};
+    a.acc_node = acc_node;
+    a.u = const_cast<float *>(u);
+    a.out = state;
+    a.status = W.status();
+    return cuda_status(launch_gdn(a, kGdnCommitWy, stream));
+}
+
 w12_status w12_gdn_commit(const w12_gdn_layer *layer, const w12_tree *tree, int32_t n_req, const int32_t *acc_node,
                           float *state, void *ws, size_t ws_bytes, w12_stream_t stream)
 {

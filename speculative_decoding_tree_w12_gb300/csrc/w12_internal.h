@@ -140,7 +140,7 @@ int launch_cert_rescore(const DevWeight &w, const uint16_t *h, int32_t R, const 
                         double *part_v, int32_t *part_i, int32_t *argmax, float *maxlogit, int32_t *cnt_out,
                         void *stream);
 // recurrent-layer tree verification (k_gdn.cu)
-constexpr int kGdnWy = 0, kGdnPath = 1, kGdnCommit = 2;
+constexpr int kGdnWy = 0, kGdnPath = 1, kGdnCommit = 2, kGdnCommitWy = 3;
 constexpr int kGdnDim = 128;        // head dimension
 constexpr int kGdnMaxRows = 64;     // tree rows of one request
 struct GdnArgs {
@@ -152,6 +152,7 @@ struct GdnArgs {
     const float *alpha, *beta;
     const int32_t *parent, *req_row_off, *acc_node;
     float *out;
+    float *u;                // WY vectors [R][H][d]: written by kGdnWy when not null, read by kGdnCommitWy
     int32_t *status;
 };
 int launch_gdn(const GdnArgs &a, int mode, void *stream);

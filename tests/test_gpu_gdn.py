@@ -185,3 +185,46 @@ def test_gdn_wy_flags_row_offsets_past_the_tree(w12):
     torch.cuda.synchronize()
     assert ws.status() == w12.W12_E_INVAL
     assert bool((o == 7.0).all())
+
+
+WY_COMMIT_CASES = CASES[:6] + [("bench_batched", dict(n_req=24, positions=(16, 12, 8), budget=192, n_cand=16), 32)]
+
+
+@pytest.mark.parametrize("name,kw,H", WY_COMMIT_CASES)
+def test_gdn_wy_vectors_and_commit_match_fp64(w12, name, kw, H):
+    """w12_gdn_wy_verify's outputs equal w12_gdn_tree_verify's (same
+    kernels), its WY vectors match oracle.gdn_wy_u, and w12_gdn_wy_commit's
+    states match the replayed FP64 commit (also written in place over S0)."""
+    w, lat, t, x = _case(kw, H, 21)
+    ws = w12.Workspace(1, 0, 0, w.n_req)
+    tree = w12.w12_tree_build(w12.DeviceLattice(lat), w.budget, ws)
+    layer = _layer(w12, x)
+    o, u = w12.w12_gdn_wy_verify(layer, tree, w.n_req, ws)
+    o_ref = w12.w12_gdn_tree_verify(layer, tree, w.n_req, ws, w12.W12_GDN_WY)
+    g = np.random.default_rng(22)
+    acc = np.asarray([g.integers(t.req_row_off[r], t.req_row_off[r + 1]) for r in range(w.n_req)], np.int32)
+    st = w12.w12_gdn_wy_commit(layer, tree, w.n_req, torch.from_numpy(acc).cuda(), u, ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    assert torch.equal(o, o_ref)
+    u_ref = oracle.gdn_wy_u(x.S0, x.k, x.v, x.alpha, x.beta, t)
+    assert _rel_err(u.cpu().numpy().astype(np.float64), u_ref) <= 1e-4
+    ref = oracle.gdn_commit(x.S0, x.k, x.v, x.alpha, x.beta, t, acc)
+    assert _rel_err(st.cpu().numpy().astype(np.float64).reshape(-1, 128), ref.reshape(-1, 128)) <= 1e-4
+    st2 = w12.w12_gdn_wy_commit(layer, tree, w.n_req, torch.from_numpy(acc).cuda(), u, ws, state=layer.S0)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    assert torch.equal(st2, st)
+
+
+def test_gdn_wy_commit_flags_a_row_outside_its_request(w12):
+    w, lat, t, x = _case(dict(n_req=3, positions=(2, 4, 6), budget=30, n_cand=16), 2, 23)
+    ws = w12.Workspace(1, 0, 0, w.n_req)
+    tree = w12.w12_tree_build(w12.DeviceLattice(lat), w.budget, ws)
+    layer = _layer(w12, x)
+    _, u = w12.w12_gdn_wy_verify(layer, tree, w.n_req, ws)
+    acc = np.asarray([t.req_row_off[0], t.req_row_off[0], t.req_row_off[2]], np.int32)   # request 1: a row of request 0
+    st = w12.w12_gdn_wy_commit(layer, tree, w.n_req, torch.from_numpy(acc).cuda(), u, ws)
+    torch.cuda.synchronize()
+    assert ws.status() == w12.W12_E_INVAL
+    assert torch.equal(st[1], layer.S0[1])
