@@ -1022,7 +1022,11 @@ __global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy(const __grid_constant_
                         }
                     }
                     t += gsz;
-                    named_bar(bar_id, bar_n);   // the next depth reads these rows' u
+                    // the next depth reads these rows' u: with two threads per
+                    // column a barrier; with one, the thread's own order (and
+                    // the vote before the group's next request orders the
+                    // solve before that request's k.k / q.k writes)
+                    if (!two) named_bar(bar_id, bar_n);
                 }
             }
             rc += __popcll(starts);   // (both roles count the pack's requests)
