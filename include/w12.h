@@ -385,8 +385,8 @@ w12_status w12_gdn_wy_verify(const w12_gdn_layer *layer, const w12_tree *tree, i
 /*
  * The committed states from those vectors, in one pass over S0 (no replay):
  * state[r] = g S0[r] + sum over i on acc_node[r]'s root path of (g / g_i) u_i k_i^T,
- * with u from w12_gdn_wy_verify on the same layer and tree.  state as for
- * w12_gdn_commit (16-byte aligned; may be S0 itself).  Device checks: a row
+ * with u from w12_gdn_wy_verify on the same layer and tree (16-byte
+ * aligned).  state as for w12_gdn_commit (16-byte aligned; may be S0 itself).  Device checks: a row
  * outside the request sets W12_E_INVAL (the state is then left as S0[r]).
  */
 w12_status w12_gdn_wy_commit(const w12_gdn_layer *layer, const w12_tree *tree, int32_t n_req, const int32_t *acc_node,

@@ -1179,10 +1179,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gdn_path(const GdnParams p)
 // d_v / 32).
 
 struct WyCommitShared {
-    float K[kNR * kD];     // the path's keys (FP32), in path order (accepted row first)
+    uint16_t K[kNR * kD];  // keys of the request's rows (BF16)
     float Uc[kNR * kVS];   // their WY vectors, this CTA's 32 state rows
     float coef[kNR];       // g_acc / g_i per path entry
-    int32_t path[kNR];
+    int32_t path[kNR];     // the accepted row's root path, accepted row first
     int32_t par[kNR];
     float alpha[kNR];
     int32_t plen;
@@ -1196,7 +1196,9 @@ __global__ void __launch_bounds__(kThreads) k_gdn_wy_commit(const GdnParams p)
     const int r = blockIdx.x, h = blockIdx.y, vs = blockIdx.z * kVS;
     const int tid = threadIdx.x;
     const int H = p.H;
-    // the committed slice (rows vs .. vs + 31) first
+    // every read issued before the path is known: the committed slice (rows
+    // vs .. vs + 31), the keys and this slice of the WY vectors of all the
+    // request's rows (asynchronous copies), the rows' parents and gates
     const float *S0 = p.S0 + (((size_t)r * H + h) * kD + vs) * kD;
     float4 sv[kVS * kD / 4 / kThreads];
 #pragma unroll
@@ -1205,6 +1207,18 @@ __global__ void __launch_bounds__(kThreads) k_gdn_wy_commit(const GdnParams p)
     int row0;
     const int n = request_rows(p, r, row0);
     if (n <= 0) return;
+    if (row0 < 0 || row0 + n > p.R) {   // rows past the tree: nothing read, nothing written
+        if (tid == 0) atomicCAS(p.status, 0, (int32_t)W12_E_INVAL);
+        return;
+    }
+    for (int e = tid; e < n * 16; e += kThreads) {
+        const int j = e >> 4, ch = e & 15;
+        cp_async16(smem_u32(&s.K[j * kD + ch * 8]), p.k + ((size_t)(row0 + j) * H + h) * kD + ch * 8);
+    }
+    for (int e = tid; e < n * (kVS / 4); e += kThreads) {
+        const int j = e / (kVS / 4), ch = e % (kVS / 4);
+        cp_async16(smem_u32(&s.Uc[j * kVS + ch * 4]), p.u + ((size_t)(row0 + j) * H + h) * kD + vs + ch * 4);
+    }
     if (tid < n) {
         const int pr = p.parent[row0 + tid];
         int pl = pr < 0 ? -1 : pr - row0;
@@ -1235,24 +1249,9 @@ __global__ void __launch_bounds__(kThreads) k_gdn_wy_commit(const GdnParams p)
         for (int q = 0; q < len; ++q) s.coef[q] = g / s.coef[q];
         s.plen = len;
     }
+    cp_async_wait_all();
     __syncthreads();
     const int len = s.plen;
-    for (int e = tid; e < len * 16; e += kThreads) {
-        const int q = e >> 4, ch = e & 15;
-        const uint4 kv = *reinterpret_cast<const uint4 *>(p.k + ((size_t)(row0 + s.path[q]) * H + h) * kD + ch * 8);
-        const uint32_t w4[4] = {kv.x, kv.y, kv.z, kv.w};
-        float *dst = &s.K[q * kD + ch * 8];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            dst[2 * t] = __uint_as_float(w4[t] << 16);
-            dst[2 * t + 1] = __uint_as_float(w4[t] & 0xffff0000u);
-        }
-    }
-    for (int e = tid; e < len * kVS; e += kThreads) {
-        const int q = e / kVS, c = e % kVS;
-        s.Uc[q * kVS + c] = p.u[((size_t)(row0 + s.path[q]) * H + h) * kD + vs + c];
-    }
-    __syncthreads();
     const float gacc = s.gacc;
     float *dst = p.out + (((size_t)r * H + h) * kD + vs) * kD;
 #pragma unroll
@@ -1260,12 +1259,13 @@ __global__ void __launch_bounds__(kThreads) k_gdn_wy_commit(const GdnParams p)
         const int e = tid + i * kThreads, row = e >> 5, c4 = (e & 31) * 4;
         float4 x = make_float4(gacc * sv[i].x, gacc * sv[i].y, gacc * sv[i].z, gacc * sv[i].w);
         for (int q = 0; q < len; ++q) {
-            const float w = s.coef[q] * s.Uc[q * kVS + row];
-            const float4 kk = *reinterpret_cast<const float4 *>(&s.K[q * kD + c4]);
-            x.x = fmaf(w, kk.x, x.x);
-            x.y = fmaf(w, kk.y, x.y);
-            x.z = fmaf(w, kk.z, x.z);
-            x.w = fmaf(w, kk.w, x.w);
+            const int j = s.path[q];
+            const float w = s.coef[q] * s.Uc[j * kVS + row];
+            const uint2 kb = *reinterpret_cast<const uint2 *>(&s.K[j * kD + c4]);
+            x.x = fmaf(w, __uint_as_float(kb.x << 16), x.x);
+            x.y = fmaf(w, __uint_as_float(kb.x & 0xffff0000u), x.y);
+            x.z = fmaf(w, __uint_as_float(kb.y << 16), x.z);
+            x.w = fmaf(w, __uint_as_float(kb.y & 0xffff0000u), x.w);
         }
         *reinterpret_cast<float4 *>(dst + (size_t)row * kD + c4) = x;
     }

@@ -753,7 +753,7 @@ w12_status w12_gdn_wy_commit(const w12_gdn_layer *layer, const w12_tree *tree, i
     GdnArgs a;
     w12_status s = gdn_args(layer, tree, n_req, a);
     if (s != W12_OK) return s;
-    if (!acc_node || !u || !state || !aligned(state, 16)) return W12_E_INVAL;
+    if (!acc_node || !u || !state || !aligned(state, 16) || !aligned(u, 16)) return W12_E_INVAL;
     const WsLayout L = layout_for(1, 0, 0, n_req);
     if ((s = ws_check(ws, ws_bytes, L)) != W12_OK) return s;
     Ws W{static_cast<uint8_t *>(ws), L};
