@@ -532,13 +532,23 @@ __global__ void __launch_bounds__(kThreads, 2) k_gdn_wy_slice(const GdnParams p)
 //    thread issues the MMAs (M = 128, N = the request's block rows):
 //        D [c][  j ] = S0 k_j  and  D [c][n + j] = S0 q_j   (3 pieces x 8 k steps)
 //        D2[j][  i ] = k_j.k_i and  D2[n + j][i] = q_j.k_i  (8 k steps);
-//  * solvers (warps 0..7, two threads per state row c): copy D and D2 out of
-//    tensor memory (which frees them for the next request), then take the
-//    request's rows by depth, a group of rows of one depth at a time (none is
-//    an ancestor of another), half of each group per thread, for their own
-//    column:  u_j = b_j (v_j - g_j S0 k_j) - sum over the ancestors (b_j g_j
-//    k_i.k_j / g_i) u_i,  o_j = g_j S0 q_j + sum over the path (g_j k_i.q_j / g_i) u_i,
-//    one pass over the ancestors for both sums.
+//  * solvers (warps 0..7): copy D and D2 out of tensor memory (which frees
+//    them for the next request), then take the request's rows by depth, a
+//    group of rows of one depth at a time (none is an ancestor of another),
+//    each thread for its own state row's column:
+//        u_j = b_j (v_j - g_j S0 k_j) - sum over the ancestors (b_j g_j k_i.k_j / g_i) u_i,
+//        o_j = g_j S0 q_j + sum over the path (g_j k_i.q_j / g_i) u_i,
+//    one pass over the ancestors for both sums.  When every request of the
+//    pack has at most 45 rows, two groups of four warps take alternate
+//    requests (one thread per column, each group with its own half of the
+//    k.k / q.k buffers); otherwise all eight warps take each request, two
+//    threads per column sharing each depth group.
+//
+// Hand-offs: request r's MMAs complete bar_mma[r % 2] (a waiter has always
+// seen request r - 2 complete, so its parity is never two phases ahead);
+// bar_dfree counts the solver warps that have copied D and D2 out; bar_stage
+// the state copies.  Every wait is bounded; each role decides to stop with a
+// barrier reduction, so that a stop never leaves a named barrier short.
 
 constexpr int kWyThreads = 384;
 constexpr int kSolvers = 256;       // warps 0..7: two per quarter of the state rows
