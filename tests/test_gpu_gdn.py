@@ -150,6 +150,15 @@ PACKS = [
     ("tiny", [1, 4, 2, 3] * 15, 2),
     # every size from 1 to 12
     ("ramp", list(range(1, 13)), 2),
+    # the two-solver-group threshold: with 64 heads the windows are wide, so
+    # a 45-row request shares a pack with small ones (two groups) and a
+    # 46-row one does too (one group)
+    ("threshold", [45, 46, 3, 1, 45], 64),
+    ("threshold_big", [3, 46, 1], 64),
+    # 64 heads: the tensor-memory kernel's windows shrink to fit one wave
+    ("heads_64", [8] * 6, 64),
+    # 500 one-row requests: more requests than threads in the row-range check
+    ("many_requests", [1] * 500, 1),
 ]
 
 
@@ -228,3 +237,32 @@ def test_gdn_wy_commit_flags_a_row_outside_its_request(w12):
     torch.cuda.synchronize()
     assert ws.status() == w12.W12_E_INVAL
     assert torch.equal(st[1], layer.S0[1])
+
+
+
+@pytest.mark.parametrize("name,sizes,H", PACKS + [("one_of_64_then_tiny", [64] + [1] * 20, 2)])
+def test_gdn_wy_vectors_and_commit_on_hand_packs(w12, name, sizes, H):
+    """w12_gdn_wy_verify and w12_gdn_wy_commit on the hand-made packs: the
+    outputs, the WY vectors and the committed states of non-empty requests
+    (an empty request has no row to accept and keeps no state) against the
+    FP64 oracle."""
+    t, dt = _hand_tree(w12, sizes, 31)
+    n_req = len(sizes)
+    x = synth.gdn_inputs(t.R, n_req, H, 128, seed=32)
+    ws = w12.Workspace(1, 0, 0, n_req)
+    layer = _layer(w12, x)
+    o, u = w12.w12_gdn_wy_verify(layer, dt, n_req, ws)
+    g = np.random.default_rng(33)
+    off = t.req_row_off
+    acc = np.asarray([g.integers(off[r], off[r + 1]) if sizes[r] else off[r] for r in range(n_req)], np.int32)
+    st = w12.w12_gdn_wy_commit(layer, dt, n_req, torch.from_numpy(acc).cuda(), u, ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    o_ref = oracle.gdn_tree_path(x.S0, x.q, x.k, x.v, x.alpha, x.beta, t)
+    u_ref = oracle.gdn_wy_u(x.S0, x.k, x.v, x.alpha, x.beta, t)
+    assert _rel_err(o.cpu().numpy().astype(np.float64), o_ref) <= 1e-4
+    assert _rel_err(u.cpu().numpy().astype(np.float64), u_ref) <= 1e-4
+    full = [r for r in range(n_req) if sizes[r]]
+    s_ref = oracle.gdn_commit(x.S0[full], x.k, x.v, x.alpha, x.beta, t, acc[full])
+    got = st.cpu().numpy().astype(np.float64)[full]
+    assert _rel_err(got.reshape(-1, 128), s_ref.reshape(-1, 128)) <= 1e-4
