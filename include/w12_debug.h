@@ -20,6 +20,11 @@ extern "C" {
  *                first record but never copies it, so that CTA's consumers
  *                time out; the kernel records W12_E_TIMEOUT in the workspace
  *                status word and every CTA returns with no copy in flight.
+ *                In the recurrent layer's tensor-memory WY kernel (trees of
+ *                several requests), CTA (0, 0) never copies its first
+ *                request's state: its splitters' wait runs out, both warp
+ *                roles stop, W12_E_TIMEOUT is recorded and tensor memory is
+ *                released.
  *   flags bit 1: run every GEMM on the tensor-memory (tcgen05) kernel.
  *   flags bit 2: run every GEMM on the warp-MMA kernel (64 rows per pass).
  *                Without either bit the library picks by row count.

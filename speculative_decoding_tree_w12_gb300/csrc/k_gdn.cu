@@ -71,6 +71,7 @@ struct GdnParams {
     float *out;          // o [R][H][d] or, for the commit, the state [n_req][H][d][d]
     float *u;            // the WY vectors u [R][H][d]: written by the WY form when not null, read by its commit
     int32_t *status;
+    int32_t debug_flags; // bit 0: CTA (0, 0) of the tensor-memory WY kernel never copies its first state (test hook)
 };
 
 __device__ __forceinline__ float bf(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
@@ -758,8 +759,11 @@ __global__ void __launch_bounds__(kWyThreads, 1) k_gdn_wy(const __grid_constant_
         const int n = s.pack_end - a;
         const unsigned long long starts = s.starts;
         if (tid == kSolvers) {   // the first request's state
-            stage_state(s.rq[0]);
-            ++n_staged;
+            const bool withheld = (p.debug_flags & 1) && blockIdx.x == 0 && blockIdx.y == 0 && rc == 0;
+            if (!withheld) {   // (the test hook leaves the first copy out: the splitters' wait runs out)
+                stage_state(s.rq[0]);
+                ++n_staged;
+            }
         }
 
         // the rest of the pack's reads: the key / query blocks (asynchronous
@@ -1322,6 +1326,7 @@ int launch_gdn(const GdnArgs &a, int mode, void *stream)
     p.acc_node = a.acc_node;
     p.out = a.out;
     p.u = a.u;
+    p.debug_flags = a.debug_flags;
     p.status = a.status;
     // plain launches: with an early start the next layer's CTAs would share
     // SMs with this one's and leave others idle (one CTA per SM is the

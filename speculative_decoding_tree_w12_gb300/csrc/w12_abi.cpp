@@ -701,6 +701,7 @@ w12_status gdn_args(const w12_gdn_layer *L, const w12_tree *tree, int32_t n_req,
     a.R = tree->R;
     a.num_sms = num_sms();
     a.timeout_ns = g_timeout_ns;
+    a.debug_flags = g_debug_flags;
     a.S0 = L->S0;
     a.q = L->q;
     a.k = L->k;

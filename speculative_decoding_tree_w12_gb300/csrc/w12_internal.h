@@ -154,6 +154,7 @@ struct GdnArgs {
     float *out;
     float *u;                // WY vectors [R][H][d]: written by kGdnWy when not null, read by kGdnCommitWy
     int32_t *status;
+    int32_t debug_flags;     // w12_debug_set flags (bit 0: the tensor-memory WY kernel's test hook)
 };
 int launch_gdn(const GdnArgs &a, int mode, void *stream);
 

@@ -266,3 +266,29 @@ def test_gdn_wy_vectors_and_commit_on_hand_packs(w12, name, sizes, H):
     s_ref = oracle.gdn_commit(x.S0[full], x.k, x.v, x.alpha, x.beta, t, acc[full])
     got = st.cpu().numpy().astype(np.float64)[full]
     assert _rel_err(got.reshape(-1, 128), s_ref.reshape(-1, 128)) <= 1e-4
+
+
+def test_gdn_wy_tensor_memory_wait_times_out_cleanly(w12):
+    """CTA (0, 0) of the tensor-memory WY kernel never copies its first
+    request's state (test hook): its splitters give up after 50 ms, both warp
+    roles stop, tensor memory is released, the status word reads
+    W12_E_TIMEOUT, and the context stays usable: the same call without the
+    hook matches the oracle."""
+    w, lat, t, x = _case(dict(n_req=3, positions=(2, 4, 6), budget=30, n_cand=16), 2, 41)
+    ws = w12.Workspace(1, 0, 0, w.n_req)
+    tree = w12.w12_tree_build(w12.DeviceLattice(lat), w.budget, ws)
+    layer = _layer(w12, x)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    w12.debug_set(1, 50_000_000)
+    try:
+        w12.w12_gdn_tree_verify(layer, tree, w.n_req, ws, w12.W12_GDN_WY)
+        torch.cuda.synchronize()
+        assert ws.status() == w12.W12_E_TIMEOUT
+    finally:
+        w12.debug_set(0, 0)
+    o = w12.w12_gdn_tree_verify(layer, tree, w.n_req, ws, w12.W12_GDN_WY)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    ref = oracle.gdn_tree_path(x.S0, x.q, x.k, x.v, x.alpha, x.beta, t)
+    assert _rel_err(o.cpu().numpy().astype(np.float64), ref) <= 1e-4
