@@ -266,7 +266,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
                 }
                 if (moved) {
                     t_idle = 0;
-                } else if (*abort_flag) {
+                    continue;
+                }
+                // both rings full: back off so that this warp's polls do not
+                // take issue slots from the decode warps of its scheduler
+                __nanosleep(64);
+                if (*abort_flag) {
                     stalled = true;
                 } else if (t_idle == 0) {
                     t_idle = globaltimer();

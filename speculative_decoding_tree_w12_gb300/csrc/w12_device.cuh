@@ -122,6 +122,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// As mbar_try_wait, with a suspend-time hint: a thread whose phase is not yet
+// complete sleeps until it completes or about `hint_ns` pass, instead of
+// returning after the (short) system default and polling again.  A sleeping
+// warp issues nothing, so it leaves the issue slots of its scheduler to the
+// warps that have work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Non-blocking probe of a phase (never suspends the thread, unlike try_wait):
 // for a thread that polls several barriers in turn.
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
@@ -143,25 +159,26 @@ __device__ __forceinline__ uint64_t globaltimer()
 }
 
 // Wait for the phase of parity `parity` to complete.  Gives up after
-// `timeout_ns` (checked every 256 polls), records W12_E_TIMEOUT in *status
-// and returns false.  Also returns false early once *abort is set.  The
-// first polls run without reading the (slow) global timer.
+// `timeout_ns`, records W12_E_TIMEOUT in *status and returns false.  Also
+// returns false once *abort is set.  After one plain poll the thread sleeps
+// in try_wait (woken by the phase, or after kWaitSleepNs to look at the clock
+// and the abort flag), so a waiting warp does not take issue slots from the
+// warps of its scheduler that have work.
+constexpr uint32_t kWaitSleepNs = 20000;
+
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns, int32_t *status,
                                           volatile int32_t *abort)
 {
-#pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0) {
-            if (*abort) return false;
-            if (globaltimer() - t0 > timeout_ns) {
-                atomicCAS(status, 0, static_cast<int32_t>(W12_E_TIMEOUT));
-                *abort = 1;
-                return false;
-            }
+#pragma unroll 1
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+        if (*abort) return false;
+        if (globaltimer() - t0 > timeout_ns) {
+            atomicCAS(status, 0, static_cast<int32_t>(W12_E_TIMEOUT));
+            *abort = 1;
+            return false;
         }
     }
 }
