@@ -13,8 +13,11 @@
 //   * consumer warps decode the records in registers straight into mma.sync
 //     A fragments (output channels are M, tree rows are N), patch escapes,
 //     and accumulate in FP32;
-//   * a tile split between CTAs is reduced by the last CTA to arrive, reading
-//     the partial sums in CTA order (no waiting, deterministic);
+//   * at a tile's end the consumer warps drop their accumulators in shared
+//     memory and go on with the next tile; an epilogue warp writes the tile,
+//     or publishes its partial sum when the tile is split between CTAs, and
+//     the last CTA to arrive at a split tile sums the partials in CTA order
+//     (no waiting, deterministic);
 //   * the LM-head epilogue reduces each 128-token tile to (max, index) per row.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -61,7 +64,9 @@ struct Cfg {
     static constexpr int kWarpsN = 8 / MB;                    // consumer warps across the 128 channels (16 * MB each)
     static constexpr int kConsumerWarps = kWarpsN * WK;
     static constexpr int kConsumers = kConsumerWarps * 32;
-    static constexpr int kThreads = kConsumers + 32;          // + producer warp
+    static constexpr int kProducerWarp = kConsumerWarps;
+    static constexpr int kEpilogueWarp = kConsumerWarps + 1;
+    static constexpr int kThreads = kConsumers + 64;          // + producer and epilogue warps
     static constexpr int kKgPerWarp = 4 / WK;                 // 16-K groups per consumer warp
     static constexpr int kRedStride = 132;                    // padded row stride of the reduction tile
     static constexpr int kRedBytes = WK * kRows * kRedStride * 4;
@@ -84,7 +89,7 @@ __host__ __device__ inline SmemPlan smem_plan(int stages, int max_recs, int esc_
     s.red_off = o;
     o += C::kRedBytes;
     s.bar_off = o;
-    o += 2 * stages * 8 + 8;
+    o += 2 * stages * 8 + 24;
     s.flag_off = o;
     o += 16;
     s.escoff_off = o;
@@ -126,6 +131,8 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV, MB>::kThreads, 1)
     const uint32_t bar_full = smem_u32(smem + sp.bar_off);
     const uint32_t bar_empty = bar_full + 8 * S;
     const uint32_t bar_cons = bar_empty + 8 * S;
+    const uint32_t bar_red_full = bar_cons + 8;    // the consumers' accumulators are in red
+    const uint32_t bar_red_empty = bar_cons + 16;  // the epilogue has read them
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(smem + sp.flag_off);
     int32_t *last_flag = reinterpret_cast<int32_t *>(smem + sp.flag_off + 4);
     int32_t *esc_off_s = reinterpret_cast<int32_t *>(smem + sp.escoff_off);
@@ -139,13 +146,15 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV, MB>::kThreads, 1)
             mbar_init(bar_empty + 8 * s, C::kConsumerWarps);
         }
         mbar_init(bar_cons, C::kConsumerWarps);   // one arrival per consumer warp
+        mbar_init(bar_red_full, C::kConsumerWarps);
+        mbar_init(bar_red_empty, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
     pdl_launch_dependents();
 
-    if (warp == C::kConsumerWarps) {
+    if (warp == C::kProducerWarp) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             prefetch_tmap(&xmap);
@@ -205,6 +214,149 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV, MB>::kThreads, 1)
         return;
     }
 
+    // ---------------------------------------------------- finishing a tile
+    // Tile nt from the K-slice sums in red, by the nthr threads tid = 0 ..
+    // nthr - 1 (whole warps): written when this CTA holds all of its records;
+    // else this CTA's partial sum is published (slot 0 for the CTA's first
+    // tile, 1 for its last) and the last of the tile's contributors to arrive
+    // sums every partial in CTA order and writes the result.  red_read() runs
+    // as soon as red has been read; sync() is a barrier over the threads
+    // (false: aborted); *flag is a shared word for the last-arrival decision.
+    const int64_t nt_first = rec_begin / KT;
+    auto finish_tile = [&](int64_t nt, int tid, int nthr, auto &&sync, auto &&red_read, int32_t *flag) -> bool {
+        const int rows = min(p.R, C::kRows);
+        const int wi = tid >> 5, nw = nthr >> 5;
+        auto from_red = [&](int row, int c4) {
+            float4 v = *reinterpret_cast<const float4 *>(red + row * C::kRedStride + c4);
+#pragma unroll
+            for (int sl = 1; sl < WK; ++sl) {
+                const float4 w = *reinterpret_cast<const float4 *>(red + (sl * C::kRows + row) * C::kRedStride + c4);
+                v.x += w.x, v.y += w.y, v.z += w.z, v.w += w.w;
+            }
+            return v;
+        };
+        // BF16 (round to nearest even) rows of 128 channels, or per row the
+        // (max, lowest index) over the tile's 128 tokens (a warp reduces four
+        // of its rows side by side); get(row, c4) gives 4 channels from c4
+        auto emit = [&](auto &&get) {
+            if (p.mode == w12i::kModeLinear) {
+#pragma unroll 4
+                for (int e = tid; e < rows * 32; e += nthr) {
+                    const int row = e >> 5, c4 = (e & 31) * 4;
+                    const float4 v = get(row, c4);
+                    uint2 packed;
+                    packed.x = pack_bf16x2(v.x, v.y);
+                    packed.y = pack_bf16x2(v.z, v.w);
+                    *reinterpret_cast<uint2 *>(p.y + row * p.ldy + nt * w12i::kTileN + c4) = packed;
+                }
+                return;
+            }
+            constexpr int kU = 4;
+            const int lane = tid & 31;
+            for (int r0 = wi; r0 < rows; r0 += kU * nw) {
+                float bv[kU];
+                int32_t bi[kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    bv[u] = __int_as_float(0x7fc00000);
+                    bi[u] = 0x7fffffff;
+                    const int row = r0 + u * nw;
+                    if (row < rows) {
+                        const float4 v = get(row, lane * 4);
+                        const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (beats(vv[q], lane * 4 + q, bv[u], bi[u])) bv[u] = vv[q], bi[u] = lane * 4 + q;
+                    }
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                    for (int u = 0; u < kU; ++u) {
+                        const float ov = __shfl_xor_sync(0xffffffffu, bv[u], off);
+                        const int32_t oi = __shfl_xor_sync(0xffffffffu, bi[u], off);
+                        if (beats(ov, oi, bv[u], bi[u])) bv[u] = ov, bi[u] = oi;
+                    }
+                if (lane == 0) {
+#pragma unroll
+                    for (int u = 0; u < kU; ++u) {
+                        const int row = r0 + u * nw;
+                        if (row < rows) {
+                            p.s1_val[(int64_t)row * p.n_tiles + nt] = bv[u];
+                            p.s1_idx[(int64_t)row * p.n_tiles + nt] = (bi[u] == 0x7fffffff)
+                                                                          ? (int32_t)(nt * w12i::kTileN)
+                                                                          : (int32_t)(nt * w12i::kTileN + bi[u]);
+                        }
+                    }
+                }
+            }
+        };
+
+        const int64_t t0 = nt * KT, t1 = t0 + KT;
+        if (rec_begin <= t0 && rec_end >= t1) {
+            emit(from_red);
+            red_read();
+            return sync();
+        }
+        float *mine = p.partial + ((int64_t)(cta * 2 + (nt == nt_first ? 0 : 1)) * C::kRows) * w12i::kTileN;
+        for (int e = tid; e < rows * 32; e += nthr) {
+            const int row = e >> 5, c4 = (e & 31) * 4;
+            __stcg(reinterpret_cast<float4 *>(mine + row * w12i::kTileN + c4), from_red(row, c4));
+        }
+        red_read();
+        __threadfence();
+        if (!sync()) return false;
+        const int c_first = cta_of_record(t0, G, T), c_last = cta_of_record(t1 - 1, G, T);
+        if (tid == 0) *flag = (atomicAdd(p.counters + nt, 1) == c_last - c_first);
+        if (!sync()) return false;
+        if (*reinterpret_cast<volatile int32_t *>(flag) == 0) return true;
+        __threadfence();
+        // Every contributor after the first starts inside this tile (its slot
+        // 0); the first one's slot depends on where it starts.
+        const int sl_first = (first_record(c_first, G, T) >= t0) ? 0 : 1;
+        const float *part0 = p.partial + (int64_t)(c_first * 2 + sl_first) * C::kRows * w12i::kTileN;
+        const float *part1 = p.partial + (int64_t)((c_first + 1) * 2) * C::kRows * w12i::kTileN;
+        constexpr int64_t kSlot2 = 2 * (int64_t)C::kRows * w12i::kTileN;   // floats between CTAs' slot 0
+        const int n_later = c_last - c_first;
+        emit([&](int row, int c4) {
+            const int off = row * w12i::kTileN + c4;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 w0 = __ldcg(reinterpret_cast<const float4 *>(part0 + off));
+            v.x += w0.x, v.y += w0.y, v.z += w0.z, v.w += w0.w;
+            for (int c = 0; c < n_later; ++c) {
+                const float4 w = __ldcg(reinterpret_cast<const float4 *>(part1 + c * kSlot2 + off));
+                v.x += w.x, v.y += w.y, v.z += w.z, v.w += w.w;
+            }
+            return v;
+        });
+        if (tid == 0) p.counters[nt] = 0;   // ready for the next launch using this slot
+        return sync();
+    };
+
+    if (warp == C::kEpilogueWarp) {
+        // ------------------------------------------------------------ epilogue
+        // The tiles the consumers hand over (all of this CTA's but the last),
+        // in order.  red goes back to the consumers as soon as it has been read.
+        const int64_t nt_last = (rec_end - 1) / KT;
+        int32_t *eflag = last_flag + 1;
+        auto wsync = [&]() -> bool {
+            __syncwarp();
+            return true;
+        };
+        auto release = [&]() {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_red_empty);
+        };
+        uint32_t ph = 0;
+        for (int64_t nt = nt_first; nt < nt_last; ++nt) {
+            const bool ok = mbar_wait(bar_red_full, ph, p.timeout_ns, p.status, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) return;
+            ph ^= 1u;
+            if (!finish_tile(nt, lane, 32, wsync, release, eflag)) return;
+        }
+        return;
+    }
+
     // ---------------------------------------------------------------- consumers
     const int cw = warp;                 // consumer warp 0 .. kConsumerWarps-1
     constexpr int kWarpsN = C::kWarpsN;
@@ -221,7 +373,6 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV, MB>::kThreads, 1)
         return ok;
     };
     // shared caches: escape offsets/entries of this CTA's records, window bases
-    const int64_t nt_first = rec_begin / KT;
     const int nt_span = (int)((rec_end - 1) / KT - nt_first + 1);
     const bool base_cached = nt_span <= p.base_tiles;
     for (int i = ctid; i <= nrec; i += C::kConsumers) esc_off_s[i] = __ldg(p.esc_off + rec_begin + i);
@@ -278,11 +429,17 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV, MB>::kThreads, 1)
                 for (int q = 0; q < 4; ++q) acc[mb][nb][q] = 0.f;
     };
 
-    // finish tile nt: combine the K-slices, then write (owned tile) or publish
-    // a partial and let the last contributor finish it
-    auto flush = [&](int64_t nt) -> bool {
+    // End of tile nt.  In the record loop the warps drop their accumulators
+    // into red (once the epilogue warp has read the previous ones), hand the
+    // tile to the epilogue warp and go on; the CTA's last tile, whose end is
+    // the critical path, is finished by all consumer threads.
+    uint32_t n_handed = 0;   // tiles handed to the epilogue warp
+    auto drop_acc = [&]() -> bool {
         if (*abort_flag) return false;
-        // 1. every consumer warp drops its accumulators into red[wk][row][ch]
+        if (n_handed > 0 && !mbar_try_wait(bar_red_empty, (n_handed - 1) & 1u) &&
+            !mbar_wait(bar_red_empty, (n_handed - 1) & 1u, p.timeout_ns, p.status, abort_flag))
+            return false;
+        // red[wk][row][ch]
 #pragma unroll
         for (int mb = 0; mb < MB; ++mb)
 #pragma unroll
@@ -295,126 +452,18 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV, MB>::kThreads, 1)
                 rb[row * C::kRedStride + ch + 8] = acc[mb][nb][2];
                 rb[(row + 1) * C::kRedStride + ch + 8] = acc[mb][nb][3];
             }
-        if (!cons_sync()) return false;
-        const int R = p.R;
-        const int rows = min(R, C::kRows);
-        // the tile's value at (row, 4 channels from c4): the K-slices summed in
-        // slice order, or (nslices = 1) red[0] once it holds the finished sum
-        auto tile4 = [&](int row, int c4, int nslices) {
-            float4 v = *reinterpret_cast<const float4 *>(red + row * C::kRedStride + c4);
-#pragma unroll
-            for (int sl = 1; sl < WK; ++sl) {
-                if (sl >= nslices) break;
-                const float4 w = *reinterpret_cast<const float4 *>(red + (sl * C::kRows + row) * C::kRedStride + c4);
-                v.x += w.x, v.y += w.y, v.z += w.z, v.w += w.w;
-            }
-            return v;
-        };
-
-        const int64_t t0 = nt * KT, t1 = t0 + KT;
-        const bool owned = rec_begin <= t0 && rec_end >= t1;
-        bool finish = owned;
-        int nslices = WK;
-        if (!owned) {
-            // 2. publish this CTA's partial (slot 0 for its first tile, 1 for its last)
-            const int slot = (nt == nt_first) ? 0 : 1;
-            float *mine = p.partial + ((int64_t)(cta * 2 + slot) * C::kRows) * w12i::kTileN;
-            for (int e = ctid; e < rows * 32; e += C::kConsumers) {
-                const int row = e >> 5, c4 = (e & 31) * 4;
-                __stcg(reinterpret_cast<float4 *>(mine + row * w12i::kTileN + c4), tile4(row, c4, WK));
-            }
-            __threadfence();
-            if (!cons_sync()) return false;
-            const int c_first = cta_of_record(t0, G, T), c_last = cta_of_record(t1 - 1, G, T);
-            if (ctid == 0) {
-                const int old = atomicAdd(p.counters + nt, 1);
-                *last_flag = (old == c_last - c_first);
-            }
-            if (!cons_sync()) return false;
-            finish = *last_flag != 0;
-            if (finish) {
-                __threadfence();
-                // 3. the last contributor sums every partial in CTA order into
-                // red[0].  Every contributor after the first starts inside this
-                // tile (its slot 0); the first one's slot depends on where it starts.
-                const int sl_first = (first_record(c_first, G, T) >= t0) ? 0 : 1;
-                const float *part0 = p.partial + (int64_t)(c_first * 2 + sl_first) * C::kRows * w12i::kTileN;
-                const float *part1 = p.partial + (int64_t)((c_first + 1) * 2) * C::kRows * w12i::kTileN;
-                constexpr int64_t kSlot2 = 2 * (int64_t)C::kRows * w12i::kTileN;   // floats between CTAs' slot 0
-                for (int e = ctid; e < rows * 32; e += C::kConsumers) {
-                    const int off = (e >> 5) * w12i::kTileN + (e & 31) * 4;
-                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                    {
-                        const float4 w = __ldcg(reinterpret_cast<const float4 *>(part0 + off));
-                        v.x += w.x, v.y += w.y, v.z += w.z, v.w += w.w;
-                    }
-#pragma unroll 4
-                    for (int c = 0; c < c_last - c_first; ++c) {
-                        const float4 w = __ldcg(reinterpret_cast<const float4 *>(part1 + c * kSlot2 + off));
-                        v.x += w.x, v.y += w.y, v.z += w.z, v.w += w.w;
-                    }
-                    *reinterpret_cast<float4 *>(red + (e >> 5) * C::kRedStride + (e & 31) * 4) = v;
-                }
-                if (ctid == 0) p.counters[nt] = 0;   // ready for the next launch using this slot
-                if (!cons_sync()) return false;
-                nslices = 1;
-            }
-        }
-        if (finish) {
-            if (p.mode == w12i::kModeLinear) {
-                // 4a. BF16 (round to nearest even) rows of 128 channels
-                for (int e = ctid; e < rows * 32; e += C::kConsumers) {
-                    const int row = e >> 5, c4 = (e & 31) * 4;
-                    const float4 v = tile4(row, c4, nslices);
-                    uint2 packed;
-                    packed.x = pack_bf16x2(v.x, v.y);
-                    packed.y = pack_bf16x2(v.z, v.w);
-                    *reinterpret_cast<uint2 *>(p.y + row * p.ldy + nt * w12i::kTileN + c4) = packed;
-                }
-            } else {
-                // 4b. per row: (max, lowest index) over the tile's 128 tokens; a
-                // warp reduces four of its rows side by side
-                constexpr int kU = 4;
-                for (int r0 = cw; r0 < rows; r0 += kU * C::kConsumerWarps) {
-                    float bv[kU];
-                    int32_t bi[kU];
-#pragma unroll
-                    for (int u = 0; u < kU; ++u) {
-                        bv[u] = __int_as_float(0x7fc00000);
-                        bi[u] = 0x7fffffff;
-                        const int row = r0 + u * C::kConsumerWarps;
-                        if (row < rows) {
-                            const float4 v = tile4(row, lane * 4, nslices);
-                            const float vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                if (beats(vv[q], lane * 4 + q, bv[u], bi[u])) bv[u] = vv[q], bi[u] = lane * 4 + q;
-                        }
-                    }
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-                        for (int u = 0; u < kU; ++u) {
-                            const float ov = __shfl_xor_sync(0xffffffffu, bv[u], off);
-                            const int32_t oi = __shfl_xor_sync(0xffffffffu, bi[u], off);
-                            if (beats(ov, oi, bv[u], bi[u])) bv[u] = ov, bi[u] = oi;
-                        }
-                    if (lane == 0) {
-#pragma unroll
-                        for (int u = 0; u < kU; ++u) {
-                            const int row = r0 + u * C::kConsumerWarps;
-                            if (row < rows) {
-                                p.s1_val[(int64_t)row * p.n_tiles + nt] = bv[u];
-                                p.s1_idx[(int64_t)row * p.n_tiles + nt] = (bi[u] == 0x7fffffff)
-                                                                              ? (int32_t)(nt * w12i::kTileN)
-                                                                              : (int32_t)(nt * w12i::kTileN + bi[u]);
-                            }
-                        }
-                    }
-                }
-            }
-        }
-        return cons_sync();
+        return true;
+    };
+    auto flush = [&](int64_t) -> bool {
+        if (!drop_acc()) return false;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_red_full);
+        ++n_handed;
+        return true;
+    };
+    auto flush_last = [&](int64_t nt) -> bool {
+        if (!drop_acc() || !cons_sync()) return false;
+        return finish_tile(nt, ctid, C::kConsumers, cons_sync, [] {}, last_flag);
     };
 
     int64_t nt = nt_first;
@@ -567,7 +616,7 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV, MB>::kThreads, 1)
         if (lane == 0) mbar_arrive(bar_empty + 8 * s);
         if (++s == S) s = 0, full_phase ^= 1u;
     }
-    if (cur_nt >= 0) flush(cur_nt);
+    if (cur_nt >= 0) flush_last(cur_nt);
 }
 
 // second stage of the LM-head argmax: one CTA per row, fixed-order reduction
