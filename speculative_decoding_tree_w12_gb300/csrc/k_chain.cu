@@ -432,13 +432,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_chain(const __grid_constant
                 // loads and decode, so that those overlap the MMAs of pair q - Q.
                 // The MMA warp commits every pair, so the wait ends even after an
                 // abort; it is never skipped (the buffer's named barrier is
-                // reused only after its sync).
+                // reused only after its sync: a second arrival before that sync
+                // would leave the MMA warp waiting at the barrier for good).  The
+                // MMA warp may itself sit in one bounded wait before it commits,
+                // so this wait is allowed several of those limits.
                 bool buf_free = q < Q;
                 auto wait_buffer = [&]() {
                     if (buf_free) return true;
                     buf_free = true;
                     int32_t no_abort = 0;
-                    return mbar_wait(bar_done + 8 * iq, iph ^ 1u, p.timeout_ns, p.status, &no_abort);
+                    return mbar_wait(bar_done + 8 * iq, iph ^ 1u, kReuseWaits * p.timeout_ns, p.status, &no_abort);
                 };
                 bool ok = !*abort_flag;
                 if (ok) ok = mbar_wait(bar_rfull + 8 * s, sph, p.timeout_ns, p.status, abort_flag);
@@ -491,13 +494,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_chain(const __grid_constant
                                 const uint32_t en = mi.esc_cached ? es[e] : __ldg(p.job[j].esc + mi.e_lo + e);
                                 const int nl = (en >> 22) & 0x7F;
                                 if ((nl >> 5) != quarter) continue;   // warp-uniform skip
-                                const int kl = (en >> 16) & 0x3F, col = kl >> 1;
-                                const uint32_t val = en & 0xFFFFu;
-                                const bool mine = nl == c, upper = kl & 1;
-#pragma unroll
-                                for (int w = 0; w < 32; ++w)
-                                    if (mine && w == col)
-                                        a[w] = upper ? ((a[w] & 0x0000FFFFu) | (val << 16)) : ((a[w] & 0xFFFF0000u) | val);
+                                const int kl = (en >> 16) & 0x3F;
+                                if (nl == c) patch_half(a, kl >> 1, en & 0xFFFFu, kl & 1);
                             }
                         }
                         if (u == 0) wait_buffer();
@@ -857,6 +855,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_chain(const __grid_constant
             }
         }
         if (!ok) {
+            // this CTA stops too: its MMA warp must not wait a full limit for
+            // activations that will not come
+            *abort_flag = 1;
             if (p.grid_abort) *(volatile int32_t *)p.grid_abort = 1;
         }
         // leave no copy in flight: the last use of every slot that was filled

@@ -535,17 +535,9 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV, MB>::kThreads, 1)
                 if (lane != ((nl & 7) * 4 + ((kk & 7) >> 1))) continue;
                 const int mb_e = (nl >> 4) % MB, kgl_e = (kl >> 4) % C::kKgPerWarp;
                 const int j_e = (kk >> 3) * 2 + ((nl >> 3) & 1);
-                const uint32_t val = ent & 0xFFFFu;
-                const bool upper = kk & 1;
-#pragma unroll
-                for (int mb = 0; mb < MB; ++mb)
-#pragma unroll
-                    for (int kgl = 0; kgl < C::kKgPerWarp; ++kgl)
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            if (mb == mb_e && kgl == kgl_e && j == j_e)
-                                fa[mb][kgl][j] = upper ? ((fa[mb][kgl][j] & 0x0000FFFFu) | (val << 16))
-                                                       : ((fa[mb][kgl][j] & 0xFFFF0000u) | val);
+                // fa[mb][kgl][j] as one array of MB * kKgPerWarp * 4 registers
+                patch_half(reinterpret_cast<uint32_t(&)[MB * C::kKgPerWarp * 4]>(fa),
+                           (mb_e * C::kKgPerWarp + kgl_e) * 4 + j_e, ent & 0xFFFFu, kk & 1);
             }
         }
     };

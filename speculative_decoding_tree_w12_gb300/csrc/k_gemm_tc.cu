@@ -359,9 +359,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
                     // A buffer ab last held record i - Q: its MMAs must be done.
                     // The MMA warp commits every record, so this wait ends even
                     // after an abort; it is never skipped (the buffer's named
-                    // barrier is reused only after its sync).
+                    // barrier is reused only after its sync: a second arrival
+                    // before that sync would leave the MMA warp waiting at the
+                    // barrier for good).  The MMA warp may itself sit in one
+                    // bounded wait before it commits, so this wait is allowed
+                    // several of those limits and never gives up first.
                     int32_t no_abort = 0;
-                    if (!mbar_wait(bar_done + 8 * iq, iph ^ 1u, p.timeout_ns, p.status, &no_abort)) ok = false;
+                    if (!mbar_wait(bar_done + 8 * iq, iph ^ 1u, kReuseWaits * p.timeout_ns, p.status, &no_abort))
+                        ok = false;
                 }
                 ok = __all_sync(0xffffffffu, ok && !*abort_flag);
                 if (ok) {
@@ -398,13 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_w12_gemm_tc(const __grid_consta
                         const uint32_t en = esc_cached ? esc_s[e] : __ldg(p.esc + e_lo + e);
                         const int nl = (en >> 22) & 0x7F;
                         if ((nl >> 5) != quarter) continue;   // warp-uniform skip
-                        const int kl = (en >> 16) & 0x3F, col = kl >> 1;
-                        const uint32_t val = en & 0xFFFFu;
-                        const bool mine = nl == c, upper = kl & 1;
-#pragma unroll
-                        for (int w = 0; w < 32; ++w)
-                            if (mine && w == col)
-                                a[w] = upper ? ((a[w] & 0x0000FFFFu) | (val << 16)) : ((a[w] & 0xFFFF0000u) | val);
+                        const int kl = (en >> 16) & 0x3F;
+                        if (nl == c) patch_half(a, kl >> 1, en & 0xFFFFu, kl & 1);
                     }
                     tmem_st_x32(tmem + ((uint32_t)(quarter * 32) << 16) + a_col(g, ab), a);
                     tmem_st_wait();

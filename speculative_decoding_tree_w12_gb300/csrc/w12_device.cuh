@@ -78,6 +78,57 @@ __device__ __forceinline__ void decode_word(uint32_t v, uint32_t nib, ChanConst 
     pairQ = mad_u32(wQ, mul16, bitmux(sQ, cc.c1, cc.c2));
 }
 
+// Escape patch: put the exact BF16 value `val` in the upper (upper = true) or
+// lower half of a[idx], where idx is known only at run time.  A switch keeps
+// a[] in registers at the cost of one jump; a compare-and-select over every
+// entry costs a few instructions per entry.
+template <int N>
+__device__ __forceinline__ void patch_half(uint32_t (&a)[N], int idx, uint32_t val, bool upper)
+{
+    static_assert(N <= 32, "at most 32 registers");
+    switch (idx) {
+#define W12_PATCH_CASE(k)                                                                        \
+    case k:                                                                                      \
+        if constexpr (k < N)                                                                     \
+            a[k] = upper ? ((a[k] & 0x0000FFFFu) | (val << 16)) : ((a[k] & 0xFFFF0000u) | val); \
+        break;
+    W12_PATCH_CASE(0)
+    W12_PATCH_CASE(1)
+    W12_PATCH_CASE(2)
+    W12_PATCH_CASE(3)
+    W12_PATCH_CASE(4)
+    W12_PATCH_CASE(5)
+    W12_PATCH_CASE(6)
+    W12_PATCH_CASE(7)
+    W12_PATCH_CASE(8)
+    W12_PATCH_CASE(9)
+    W12_PATCH_CASE(10)
+    W12_PATCH_CASE(11)
+    W12_PATCH_CASE(12)
+    W12_PATCH_CASE(13)
+    W12_PATCH_CASE(14)
+    W12_PATCH_CASE(15)
+    W12_PATCH_CASE(16)
+    W12_PATCH_CASE(17)
+    W12_PATCH_CASE(18)
+    W12_PATCH_CASE(19)
+    W12_PATCH_CASE(20)
+    W12_PATCH_CASE(21)
+    W12_PATCH_CASE(22)
+    W12_PATCH_CASE(23)
+    W12_PATCH_CASE(24)
+    W12_PATCH_CASE(25)
+    W12_PATCH_CASE(26)
+    W12_PATCH_CASE(27)
+    W12_PATCH_CASE(28)
+    W12_PATCH_CASE(29)
+    W12_PATCH_CASE(30)
+    W12_PATCH_CASE(31)
+#undef W12_PATCH_CASE
+    default: break;
+    }
+}
+
 // position of weight kk (0..15) of a 16-K group inside its 16-byte chunk
 __device__ __forceinline__ int chunk_pos(int kk) { return ((kk & 7) >> 1) * 4 + (kk >> 3) * 2 + (kk & 1); }
 
@@ -165,6 +216,11 @@ __device__ __forceinline__ uint64_t globaltimer()
 // and the abort flag), so a waiting warp does not take issue slots from the
 // warps of its scheduler that have work.
 constexpr uint32_t kWaitSleepNs = 20000;
+
+// A wait that guards the reuse of a named barrier (an arrival must not come
+// twice before the barrier's sync) gets this many wait limits: the other side
+// may first sit out one bounded wait of its own, and must get there first.
+constexpr uint64_t kReuseWaits = 4;
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns, int32_t *status,
                                           volatile int32_t *abort)
