@@ -741,24 +741,24 @@ int launch_gemm(const GemmArgs &a, void *stream)
                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return (int)cudaErrorInvalidValue;
-    // Two 16-K groups of consumer warps: 16 warps of 16 channels up to 16 rows
-    // (more warps hide the decode chain's latency; the register cap of 544
-    // threads still fits those row counts), 8 warps of 32 channels above.  Two
-    // records per stage up to 32 rows (one wait and one release per 24 KB),
-    // one record per stage at 64 rows.
+    // Two 16-K groups of consumer warps, 16 warps of 16 channels: more warps
+    // hide the decode chain's latency, and the four on a scheduler overlap one
+    // another's decode and MMAs (the register cap of 576 threads still fits
+    // every row count).  Two records per stage up to 32 rows (one wait and one
+    // release per 24 KB), one record per stage at 64 rows.
     if (a.qview) {
         switch (nb8) {
         case 1: return launch_t<1, 2, 2, true, 1>(a, xmap, st);
         case 2: return launch_t<2, 2, 2, true, 1>(a, xmap, st);
-        case 4: return launch_t<4, 2, 2, true, 2>(a, xmap, st);
-        default: return launch_t<8, 2, 1, true>(a, xmap, st);
+        case 4: return launch_t<4, 2, 2, true, 1>(a, xmap, st);
+        default: return launch_t<8, 2, 1, true, 1>(a, xmap, st);
         }
     }
     switch (nb8) {
     case 1: return launch_t<1, 2, 2, false, 1>(a, xmap, st);
     case 2: return launch_t<2, 2, 2, false, 1>(a, xmap, st);
-    case 4: return launch_t<4, 2, 2, false, 2>(a, xmap, st);
-    default: return launch_t<8, 2, 1>(a, xmap, st);
+    case 4: return launch_t<4, 2, 2, false, 1>(a, xmap, st);
+    default: return launch_t<8, 2, 1, false, 1>(a, xmap, st);
     }
 }
 
