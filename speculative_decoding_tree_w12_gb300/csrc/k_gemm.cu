@@ -572,8 +572,11 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV, MB>::kThreads, 1)
     auto rec_x = [&](int q) { return x_s + (s * RPS + q) * C::kXBytes; };
 
     for (int i = 0; i < nrec;) {
-        // escape bits of the stage's records (bit cw: record i, bit 16 + cw: record i + 1)
-        const uint32_t em = (uint32_t)emask_s[i] | ((i + 1 < nrec) ? (uint32_t)emask_s[i + 1] << 16 : 0u);
+        // escape bits of the stage's records (bit 16 * r + cw: record i + r)
+        uint64_t em = 0;
+#pragma unroll
+        for (int r = 0; r < RPS; ++r)
+            if (i + r < nrec) em |= (uint64_t)emask_s[i + r] << (16 * r);
         if (!mbar_try_wait(bar_full + 8 * s, full_phase) &&
             !mbar_wait(bar_full + 8 * s, full_phase, p.timeout_ns, p.status, abort_flag))
             return;
@@ -584,21 +587,21 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV, MB>::kThreads, 1)
                 cur_nt = nt;
                 load_consts(nt);
             }
-            if (RPS == 2 && q == 0 && i + 1 < nrec && kt + 1 < KT) {
-                // both records of the stage belong to this tile: interleave them
+            if (RPS >= 2 && q + 1 < RPS && i + 1 < nrec && kt + 1 < KT) {
+                // two records of the stage in this tile: interleave them
                 Frag f0, f1;
-                decode_rec(rec_words(0), f0);
-                decode_rec(rec_words(1), f1);
-                patch_rec(i, f0, (em >> cw) & 1u);
-                patch_rec(i + 1, f1, (em >> (16 + cw)) & 1u);
-                mma_rec(rec_x(0), f0);
-                mma_rec(rec_x(1), f1);
+                decode_rec(rec_words(q), f0);
+                decode_rec(rec_words(q + 1), f1);
+                patch_rec(i, f0, (uint32_t)(em >> (16 * q + cw)) & 1u);
+                patch_rec(i + 1, f1, (uint32_t)(em >> (16 * (q + 1) + cw)) & 1u);
+                mma_rec(rec_x(q), f0);
+                mma_rec(rec_x(q + 1), f1);
                 q += 2, i += 2, kt += 2;
                 if (kt == KT) kt = 0, ++nt;
             } else {
                 Frag f0;
                 decode_rec(rec_words(q), f0);
-                patch_rec(i, f0, (em >> (16 * q + cw)) & 1u);
+                patch_rec(i, f0, (uint32_t)(em >> (16 * q + cw)) & 1u);
                 mma_rec(rec_x(q), f0);
                 ++q, ++i;
                 if (++kt == KT) kt = 0, ++nt;
@@ -744,8 +747,10 @@ int launch_gemm(const GemmArgs &a, void *stream)
     // Two 16-K groups of consumer warps, 16 warps of 16 channels: more warps
     // hide the decode chain's latency, and the four on a scheduler overlap one
     // another's decode and MMAs (the register cap of 576 threads still fits
-    // every row count).  Two records per stage up to 32 rows (one wait and one
-    // release per 24 KB), one record per stage at 64 rows.
+    // every row count).  Records per stage: four up to 16 rows (one wait and
+    // one release per 48 KB: at these row counts the per-stage work is a large
+    // part of a record's), two at 17-32 rows (with 32-row activation blocks
+    // four would leave fewer records in flight), one at 64 rows.
     if (a.qview) {
         switch (nb8) {
         case 1: return launch_t<1, 2, 2, true, 1>(a, xmap, st);
@@ -755,8 +760,8 @@ int launch_gemm(const GemmArgs &a, void *stream)
         }
     }
     switch (nb8) {
-    case 1: return launch_t<1, 2, 2, false, 1>(a, xmap, st);
-    case 2: return launch_t<2, 2, 2, false, 1>(a, xmap, st);
+    case 1: return launch_t<1, 2, 4, false, 1>(a, xmap, st);
+    case 2: return launch_t<2, 2, 4, false, 1>(a, xmap, st);
     case 4: return launch_t<4, 2, 2, false, 1>(a, xmap, st);
     default: return launch_t<8, 2, 1, false, 1>(a, xmap, st);
     }
