@@ -25,6 +25,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <mutex>
+#include <type_traits>
 
 #include "w12_device.cuh"
 
@@ -573,10 +574,11 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV, MB>::kThreads, 1)
 
     for (int i = 0; i < nrec;) {
         // escape bits of the stage's records (bit 16 * r + cw: record i + r)
-        uint64_t em = 0;
+        using EscBits = std::conditional_t<(RPS > 2), uint64_t, uint32_t>;
+        EscBits em = 0;
 #pragma unroll
         for (int r = 0; r < RPS; ++r)
-            if (i + r < nrec) em |= (uint64_t)emask_s[i + r] << (16 * r);
+            if (i + r < nrec) em |= (EscBits)emask_s[i + r] << (16 * r);
         if (!mbar_try_wait(bar_full + 8 * s, full_phase) &&
             !mbar_wait(bar_full + 8 * s, full_phase, p.timeout_ns, p.status, abort_flag))
             return;
@@ -587,15 +589,17 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV, MB>::kThreads, 1)
                 cur_nt = nt;
                 load_consts(nt);
             }
-            if (RPS >= 2 && q + 1 < RPS && i + 1 < nrec && kt + 1 < KT) {
-                // two records of the stage in this tile: interleave them
+            // two records of the stage in this tile: interleave them (with two
+            // records a stage, only as its first and second)
+            if (RPS >= 2 && (RPS == 2 ? q == 0 : q + 1 < RPS) && i + 1 < nrec && kt + 1 < KT) {
+                const int q0 = RPS == 2 ? 0 : q;
                 Frag f0, f1;
-                decode_rec(rec_words(q), f0);
-                decode_rec(rec_words(q + 1), f1);
-                patch_rec(i, f0, (uint32_t)(em >> (16 * q + cw)) & 1u);
-                patch_rec(i + 1, f1, (uint32_t)(em >> (16 * (q + 1) + cw)) & 1u);
-                mma_rec(rec_x(q), f0);
-                mma_rec(rec_x(q + 1), f1);
+                decode_rec(rec_words(q0), f0);
+                decode_rec(rec_words(q0 + 1), f1);
+                patch_rec(i, f0, (uint32_t)(em >> (16 * q0 + cw)) & 1u);
+                patch_rec(i + 1, f1, (uint32_t)(em >> (16 * (q0 + 1) + cw)) & 1u);
+                mma_rec(rec_x(q0), f0);
+                mma_rec(rec_x(q0 + 1), f1);
                 q += 2, i += 2, kt += 2;
                 if (kt == KT) kt = 0, ++nt;
             } else {
