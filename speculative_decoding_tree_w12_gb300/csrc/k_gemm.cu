@@ -17,7 +17,9 @@
 //     memory and go on with the next tile; an epilogue warp writes the tile,
 //     or publishes its partial sum when the tile is split between CTAs, and
 //     the last CTA to arrive at a split tile sums the partials in CTA order
-//     (no waiting, deterministic);
+//     (no waiting, deterministic).  The CTA's last tile, whose end is the
+//     launch's critical path, is finished the same way by all consumer
+//     threads;
 //   * the LM-head epilogue reduces each 128-token tile to (max, index) per row.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -489,7 +491,7 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV, MB>::kThreads, 1)
         }
     }
     using Frag = uint32_t[MB][C::kKgPerWarp][4];
-    // decode this warp's 32 channels x (16 * kKgPerWarp) K of one record
+    // decode this warp's 16 * MB channels x (16 * kKgPerWarp) K of one record
     auto decode_rec = [&](const uint32_t *rw, Frag &fa) {
 #pragma unroll
         for (int mb = 0; mb < MB; ++mb) {
@@ -512,7 +514,7 @@ __global__ void __launch_bounds__(Cfg<NB8, WK, RPS, QV, MB>::kThreads, 1)
         }
     };
     // escaped slots of record i: the warp reads up to 32 entries at once,
-    // keeps the ones inside its 32 channels x (16 * kKgPerWarp) K, and the
+    // keeps the ones inside its 16 * MB channels x (16 * kKgPerWarp) K, and the
     // owning lane replaces the filler by the exact value
     auto patch_rec = [&](int i, Frag &fa, bool has) {
         if (!has) return;
