@@ -101,6 +101,7 @@ GEMM_CASES = [
     (128, 512, 256, 0.0, 0.0),
     (128, 64, 5, 0.0, 0.0),          # a single record
     (9 * 128, 64 * 37, 12, 0.0, 0.0),
+    (65536, 128, 8, 0.01, 0.0),      # tiles of two records: a tile end every other record
 ]
 
 
@@ -143,7 +144,8 @@ def test_gemm_exact_integer_case(w12, path):
 # LM head argmax
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("V,K,R", [(4096, 512, 8), (8192, 1024, 33), (1280, 2560, 70), (2048, 384, 256)])
+@pytest.mark.parametrize("V,K,R", [(4096, 512, 8), (8192, 1024, 33), (1280, 2560, 70), (2048, 384, 256),
+                                   (65536, 128, 8)])
 def test_lmhead_argmax_matches_oracle(w12, path, V, K, R):
     wh = synth.weights(V, K, V + R, 2000, 0.005, 0.005)
     h = synth.activations(R, K, V + R, 5)
