@@ -197,6 +197,20 @@ def test_gdn_refusals_before_launch(L):
     # workspace too small, commit without accepted rows
     assert L.w12_gdn_tree_verify(C.byref(good), C.byref(tr), 1, 0, out, ws, 16, None) == w12.W12_E_WORKSPACE
     assert L.w12_gdn_commit(C.byref(good), C.byref(tr), 1, None, out, ws, 1 << 30, None) == w12.W12_E_INVAL
+    # the WY form's own entry points: outputs, vectors, alignment, workspace
+    u = C.c_void_p(0x80000)
+    node = C.c_void_p(0x90000)
+    assert L.w12_gdn_wy_verify(C.byref(bad_d), C.byref(tr), 1, out, u, ws, 1 << 30, None) == w12.W12_E_UNSUPPORTED
+    assert L.w12_gdn_wy_verify(C.byref(good), C.byref(tr), 1, None, u, ws, 1 << 30, None) == w12.W12_E_INVAL
+    assert L.w12_gdn_wy_verify(C.byref(good), C.byref(tr), 1, out, None, ws, 1 << 30, None) == w12.W12_E_INVAL
+    assert L.w12_gdn_wy_verify(C.byref(good), C.byref(tr), 1, out, u, ws, 16, None) == w12.W12_E_WORKSPACE
+    assert L.w12_gdn_wy_commit(C.byref(good), C.byref(tr), 1, None, u, out, ws, 1 << 30, None) == w12.W12_E_INVAL
+    assert L.w12_gdn_wy_commit(C.byref(good), C.byref(tr), 1, node, None, out, ws, 1 << 30, None) == w12.W12_E_INVAL
+    assert L.w12_gdn_wy_commit(C.byref(good), C.byref(tr), 1, node, u, C.c_void_p(0x70004), ws, 1 << 30,
+                               None) == w12.W12_E_INVAL
+    assert L.w12_gdn_wy_commit(C.byref(good), C.byref(tr), 1, node, C.c_void_p(0x80008), out, ws, 1 << 30,
+                               None) == w12.W12_E_INVAL
+    assert L.w12_gdn_wy_commit(C.byref(good), C.byref(tr), 1, node, u, out, ws, 16, None) == w12.W12_E_WORKSPACE
 
 
 def test_binding_signatures_match_the_header(L):
